@@ -1,0 +1,189 @@
+/*
+ * fa.h -- C ABI of the GB300 (sm_103a) exact-attention library.
+ *
+ * What is computed (FlashAttention: Fast and Memory-Efficient Exact Attention
+ * with IO-Awareness, hackmd summary, section "Standard Attention
+ * Implementation"): for every batch b and head h, with Q, K, V in R^{N x d},
+ *     S = scale * Q K^T,   P = softmax(S + mask) row by row,   O = P V.
+ * The library never forms S or P in memory: the forward walks K/V tile by
+ * tile with a running row max and row sum ("Tiling"), and the backward
+ * rebuilds S and P from Q, K, V and the stored statistic ("Recomputation").
+ * The stored statistic is the natural-log logsumexp lse_i = m_i + ln l_i.
+ *
+ * Conventions shared by every call
+ *   Tensors      bf16, contiguous [B, H, N, d] (each (b, h) slice is the
+ *                pages' N x d matrix); lse and D are fp32 [B, H, N].
+ *   Pointers     device pointers.  q, k, v, o, dO, dq, dk, dv and the
+ *                workspace must be 16-byte aligned (TMA / vector access);
+ *                lse 4-byte aligned.  Misalignment -> FA_ERR_MISALIGNED.
+ *   Sizes        B, H, N >= 1; d in {64, 128} (else FA_ERR_UNSUPPORTED);
+ *                B*H*N*d < 2^31.  scale finite and > 0.
+ *   Masks        causal != 0 keeps key j for query i iff j <= i.  Block
+ *                masks are uint8 [mask_heads, nT, nT] in device memory,
+ *                nT = ceil(N / 128); a nonzero byte keeps that 128 x 128
+ *                tile; mask_heads is 1 (shared by all heads) or H.
+ *                A query row with no kept key gets O = 0, lse = -inf and
+ *                zero gradients.
+ *   Ownership    the caller allocates every buffer, including workspaces;
+ *                the library allocates no device memory and keeps no state
+ *                between calls except one status word per device.
+ *   Streams      work is enqueued on `stream` and the call returns without
+ *                waiting.  The return value reports argument and launch
+ *                errors; no kernel is launched when it is not FA_OK.
+ *                A device-side wait that exceeds its time limit records
+ *                FA_ERR_TIMEOUT, read with fa_get_device_status().
+ */
+#ifndef FA_GB300_H
+#define FA_GB300_H
+
+#include <cuda_runtime_api.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum fa_status {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1, /* null pointer, non-positive size, bad scale   */
+  FA_ERR_UNSUPPORTED = 2, /* head dim not in {64, 128}, sizes too large    */
+  FA_ERR_MISALIGNED = 3,  /* pointer alignment below the stated minimum    */
+  FA_ERR_WORKSPACE = 4,   /* workspace smaller than the *_workspace_size   */
+  FA_ERR_CUDA = 5,        /* a CUDA runtime or driver call failed          */
+  FA_ERR_TIMEOUT = 6      /* a device-side wait ran past its limit         */
+} fa_status;
+
+/* Short English description of a status code (static storage). */
+const char* fa_status_string(fa_status s);
+
+/*
+ * Forward pass ("Tiling"; "Kernel Fusion": one kernel does
+ * matmul -> mask -> softmax -> matmul).
+ *   in : q, k, v   bf16 [B, H, N, d]
+ *   out: o         bf16 [B, H, N, d]   O = softmax(scale*QK^T + mask) V
+ *        lse       fp32 [B, H, N]      natural-log logsumexp of each row
+ * The extra memory is O(N) per head ("Theorem 1"): only o and lse.
+ */
+fa_status fa_forward(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                     int N, int d, float scale, int causal, cudaStream_t stream);
+
+/* Bytes of workspace fa_backward needs: D (fp32 [B,H,N]) and the fp32 dQ
+ * accumulator ([B,H,N,d]), each 256-byte aligned.  O(B*H*N*d), never
+ * O(N^2). */
+size_t fa_backward_workspace_size(int B, int H, int N, int d);
+
+/*
+ * Backward pass by recomputation ("Recomputation": the forward kept only O
+ * and the softmax statistics; S and P are rebuilt block by block).
+ *   in : q, k, v, o, dO   bf16 [B, H, N, d];  lse fp32 [B, H, N] from
+ *        fa_forward with the same q, k, v, scale and causal
+ *   out: dq, dk, dv       bf16 [B, H, N, d], gradients of sum(O o dO)
+ *   workspace / workspace_bytes: caller-owned device scratch of at least
+ *        fa_backward_workspace_size(B, H, N, d) bytes; its contents on
+ *        entry do not matter.
+ * Enqueues three kernels: fa_backward_preprocess, fa_backward_main,
+ * fa_backward_dq_convert (also exported separately, below).  dq is summed
+ * with fp32 atomics, so it is not bit-reproducible from run to run.
+ */
+fa_status fa_backward(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                      const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                      float scale, int causal, void* workspace, size_t workspace_bytes,
+                      cudaStream_t stream);
+
+/* Backward step 1: D_i = <dO_i, O_i> (fp32) into the workspace and zero the
+ * workspace's dQ accumulator. */
+fa_status fa_backward_preprocess(const void* o, const void* dO, int B, int H, int N, int d,
+                                 void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Backward step 2: the fused recompute kernel.  Reads D from the workspace,
+ * writes dk and dv, and adds unscaled dS K into the workspace's dQ
+ * accumulator. */
+fa_status fa_backward_main(const void* q, const void* k, const void* v, const void* dO,
+                           const float* lse, void* dk, void* dv, int B, int H, int N, int d,
+                           float scale, int causal, void* workspace, size_t workspace_bytes,
+                           cudaStream_t stream);
+
+/* Backward step 3: dq = bf16(scale * dQ accumulator). */
+fa_status fa_backward_dq_convert(void* dq, int B, int H, int N, int d, float scale,
+                                 void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Bytes of workspace the block-sparse calls need: the CSR and CSC tile
+ * lists of the mask (4 * mask_heads * (2*(nT+1) + 2*nT*nT) bytes) followed
+ * by the fa_backward workspace.  The forward uses only the list part. */
+size_t fa_blocksparse_workspace_size(int B, int H, int N, int d, int mask_heads);
+
+/*
+ * Block-sparse tile lists ("Block-sparse FlashAttention": only the nonzero
+ * blocks of the block mask are read and computed).  Writes into the
+ * workspace, at offset 0:
+ *   row_ptr int32 [mask_heads, nT+1]   head-local CSR offsets
+ *   col_ptr int32 [mask_heads, nT+1]   head-local CSC offsets
+ *   col_idx int32 [mask_heads, nT*nT]  ascending key tiles of each query tile
+ *   row_idx int32 [mask_heads, nT*nT]  ascending query tiles of each key tile
+ * Integer work, bit-exact.  nT must be <= 8192.
+ */
+fa_status fa_blocksparse_build_lists(const uint8_t* block_mask, int mask_heads, int N,
+                                     void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Block-sparse forward: builds the lists into the workspace, then runs the
+ * forward over kept tiles only; skipped tiles contribute exactly zero.
+ * causal may be combined with the mask (intersection). */
+fa_status fa_blocksparse_forward(const void* q, const void* k, const void* v, void* o, float* lse,
+                                 int B, int H, int N, int d, float scale, int causal,
+                                 const uint8_t* block_mask, int mask_heads, void* workspace,
+                                 size_t workspace_bytes, cudaStream_t stream);
+
+/* Block-sparse backward: lists, preprocess, recompute kernel over kept
+ * tiles, dq conversion.  workspace as fa_blocksparse_workspace_size. */
+fa_status fa_blocksparse_backward(const void* q, const void* k, const void* v, const void* o,
+                                  const void* dO, const float* lse, void* dq, void* dk, void* dv,
+                                  int B, int H, int N, int d, float scale, int causal,
+                                  const uint8_t* block_mask, int mask_heads, void* workspace,
+                                  size_t workspace_bytes, cudaStream_t stream);
+
+/* Synchronises `stream`, then reads and clears the status word of the
+ * current device.  FA_OK, FA_ERR_TIMEOUT (a device wait gave up; outputs of
+ * the calls since the last check are undefined) or FA_ERR_CUDA. */
+fa_status fa_get_device_status(cudaStream_t stream);
+
+/* Time limit of every device-side wait, in nanoseconds (default 2e9, also
+ * settable with the FA_WAIT_LIMIT_NS environment variable).  0 restores the
+ * default.  Applies to calls made after it returns. */
+fa_status fa_set_wait_limit_ns(unsigned long long ns);
+
+/* ---------------------------------------------------------------- tests */
+
+/* Launches one CTA that waits on an mbarrier nothing completes; the bounded
+ * wait gives up after limit_ns and records FA_ERR_TIMEOUT in the status
+ * word.  Exercises the timeout path without faulting or hanging. */
+fa_status fa_debug_wait_timeout(unsigned long long limit_ns, cudaStream_t stream);
+
+/*
+ * Exports the tile schedules the kernels walk (integer, bit-exact):
+ *   fwd_counts int32 [heads, nT], fwd_lists int32 [heads, nT, nT]:
+ *       for each query tile, the key tiles the forward visits, in order;
+ *   bwd_counts int32 [heads, nT], bwd_lists int32 [heads, nT, nT]:
+ *       for each key tile, the query tiles the backward visits, in order.
+ * heads = mask_heads with a block mask (the lists are built into the
+ * workspace first), else 1.  All outputs are device memory.
+ */
+fa_status fa_debug_schedule(int N, int causal, const uint8_t* block_mask, int mask_heads,
+                            void* workspace, size_t workspace_bytes, int* fwd_counts,
+                            int* bwd_counts, int* fwd_lists, int* bwd_lists, cudaStream_t stream);
+
+/*
+ * One-tile tcgen05 check of the operand layouts the kernels use.
+ *   mode 0: c[128x128] = a b^T, a and b bf16 [128 x 128]
+ *   mode 1: c[128xn]   = a b,   a bf16 [128 x 128], b bf16 [128 x n]
+ *   mode 2: c[128xn]   = a^T b, a bf16 [128 x 128], b bf16 [128 x n]
+ * n in {64, 128}; c fp32 row-major; all device pointers, 16-byte aligned.
+ */
+fa_status fa_debug_mma_probe(const void* a, const void* b, float* c, int mode, int n,
+                             cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_H */

@@ -1,0 +1,456 @@
+// Host side of the C ABI: argument checks, TMA descriptors, workspace
+// layout, launches and the per-device status word.
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "../../include/fa.h"
+#include "fa_internal.h"
+
+namespace fa {
+int* status_word_address();  // fa_aux.cu
+}
+
+namespace {
+
+using fa::kTile;
+
+constexpr unsigned long long kDefaultWaitNs = 2000000000ull;
+std::atomic<unsigned long long> g_wait_ns{0};
+
+unsigned long long wait_limit_ns() {
+  unsigned long long v = g_wait_ns.load();
+  if (v == 0) {
+    v = kDefaultWaitNs;
+    if (const char* e = getenv("FA_WAIT_LIMIT_NS")) {
+      const unsigned long long x = strtoull(e, nullptr, 10);
+      if (x > 0) v = x;
+    }
+    g_wait_ns.store(v);
+  }
+  return v;
+}
+
+// status word address per device, looked up once per device
+constexpr int kMaxDevices = 64;
+std::atomic<int*> g_status[kMaxDevices];
+std::mutex g_status_mu;
+
+int* status_word(fa_status* st) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    *st = FA_ERR_CUDA;
+    return nullptr;
+  }
+  int* p = g_status[dev].load();
+  if (p) return p;
+  std::lock_guard<std::mutex> lk(g_status_mu);
+  p = g_status[dev].load();
+  if (!p) {
+    p = fa::status_word_address();
+    if (!p) {
+      *st = FA_ERR_CUDA;
+      return nullptr;
+    }
+    g_status[dev].store(p);
+  }
+  return p;
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = []() -> EncodeTiledFn {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return reinterpret_cast<EncodeTiledFn>(p);
+  }();
+  return fn;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+fa_status check_shape(int B, int H, int N, int d, float scale) {
+  if (B < 1 || H < 1 || N < 1) return FA_ERR_INVALID_ARG;
+  if (!(isfinite(scale) && scale > 0.f)) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  const long long total = static_cast<long long>(B) * H * N * d;
+  if (total >= (1LL << 31)) return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
+
+fa_status check_ptr16(const void* p) {
+  if (!p) return FA_ERR_INVALID_ARG;
+  if (!aligned(p, 16)) return FA_ERR_MISALIGNED;
+  return FA_OK;
+}
+
+fa_status check_ptr4(const void* p) {
+  if (!p) return FA_ERR_INVALID_ARG;
+  if (!aligned(p, 4)) return FA_ERR_MISALIGNED;
+  return FA_OK;
+}
+
+#define FA_TRY(x)                    \
+  do {                               \
+    const fa_status _s = (x);        \
+    if (_s != FA_OK) return _s;      \
+  } while (0)
+
+#define FA_CUDA(x)                                \
+  do {                                            \
+    if ((x) != cudaSuccess) return FA_ERR_CUDA;   \
+  } while (0)
+
+struct BwdWorkspace {
+  float* delta;
+  float* dq_acc;
+};
+
+size_t bwd_ws_bytes(int B, int H, int N, int d) {
+  const size_t rows = static_cast<size_t>(B) * H * N;
+  return align256(rows * sizeof(float)) + align256(rows * d * sizeof(float));
+}
+
+BwdWorkspace bwd_ws(void* ws, int B, int H, int N) {
+  const size_t rows = static_cast<size_t>(B) * H * N;
+  BwdWorkspace w;
+  w.delta = static_cast<float*>(ws);
+  w.dq_acc = reinterpret_cast<float*>(static_cast<char*>(ws) + align256(rows * sizeof(float)));
+  return w;
+}
+
+int num_tiles(int N) { return (N + kTile - 1) / kTile; }
+
+size_t lists_bytes(int N, int mask_heads) {
+  const size_t nT = static_cast<size_t>(num_tiles(N));
+  return align256(sizeof(int) * mask_heads * (2 * (nT + 1) + 2 * nT * nT));
+}
+
+fa::TileLists lists_in(void* ws, int N, int mask_heads) {
+  const size_t nT = static_cast<size_t>(num_tiles(N));
+  int* base = static_cast<int*>(ws);
+  fa::TileLists L;
+  L.row_ptr = base;
+  L.col_ptr = base + mask_heads * (nT + 1);
+  L.col_idx = base + 2 * mask_heads * (nT + 1);
+  L.row_idx = L.col_idx + mask_heads * nT * nT;
+  L.mask_heads = mask_heads;
+  L.nT = static_cast<int>(nT);
+  return L;
+}
+
+fa_status build_lists(const uint8_t* mask, int mask_heads, int N, void* ws, cudaStream_t stream) {
+  fa::TileLists L = lists_in(ws, N, mask_heads);
+  FA_CUDA(fa::launch_build_lists(mask, mask_heads, L.nT, const_cast<int*>(L.row_ptr),
+                                 const_cast<int*>(L.col_idx), const_cast<int*>(L.col_ptr),
+                                 const_cast<int*>(L.row_idx), stream));
+  return FA_OK;
+}
+
+fa_status check_mask(const uint8_t* mask, int mask_heads, int H, int N) {
+  if (!mask) return FA_ERR_INVALID_ARG;
+  if (mask_heads != 1 && mask_heads != H) return FA_ERR_INVALID_ARG;
+  if (num_tiles(N) > 8192) return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
+
+fa_status forward_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                       int H, int N, int d, float scale, int causal, const fa::TileLists* lists,
+                       cudaStream_t stream) {
+  fa_status st = FA_OK;
+  int* err = status_word(&st);
+  if (!err) return st;
+  CUtensorMap tq, tk, tv;
+  if (!fa::make_tile_map(&tq, q, B * H, N, d) || !fa::make_tile_map(&tk, k, B * H, N, d) ||
+      !fa::make_tile_map(&tv, v, B * H, N, d))
+    return FA_ERR_CUDA;
+  fa::FwdParams p;
+  p.o = o;
+  p.lse = lse;
+  p.B = B;
+  p.H = H;
+  p.N = N;
+  p.d = d;
+  p.scale = scale;
+  p.causal = causal ? 1 : 0;
+  if (lists) p.lists = *lists;
+  p.err = err;
+  p.wait_ns = wait_limit_ns();
+  FA_CUDA(fa::launch_forward(p, tq, tk, tv, stream));
+  return FA_OK;
+}
+
+fa_status backward_main_impl(const void* q, const void* k, const void* v, const void* dO,
+                             const float* lse, void* dk, void* dv, int B, int H, int N, int d,
+                             float scale, int causal, const BwdWorkspace& w,
+                             const fa::TileLists* lists, cudaStream_t stream) {
+  fa_status st = FA_OK;
+  int* err = status_word(&st);
+  if (!err) return st;
+  CUtensorMap tq, tk, tv, tdo;
+  if (!fa::make_tile_map(&tq, q, B * H, N, d) || !fa::make_tile_map(&tk, k, B * H, N, d) ||
+      !fa::make_tile_map(&tv, v, B * H, N, d) || !fa::make_tile_map(&tdo, dO, B * H, N, d))
+    return FA_ERR_CUDA;
+  fa::BwdParams p;
+  p.lse = lse;
+  p.delta = w.delta;
+  p.dq_acc = w.dq_acc;
+  p.dk = dk;
+  p.dv = dv;
+  p.B = B;
+  p.H = H;
+  p.N = N;
+  p.d = d;
+  p.scale = scale;
+  p.causal = causal ? 1 : 0;
+  if (lists) p.lists = *lists;
+  p.err = err;
+  p.wait_ns = wait_limit_ns();
+  FA_CUDA(fa::launch_backward_main(p, tq, tk, tv, tdo, stream));
+  return FA_OK;
+}
+
+fa_status check_fwd_args(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                         int H, int N, int d, float scale) {
+  FA_TRY(check_shape(B, H, N, d, scale));
+  FA_TRY(check_ptr16(q));
+  FA_TRY(check_ptr16(k));
+  FA_TRY(check_ptr16(v));
+  FA_TRY(check_ptr16(o));
+  FA_TRY(check_ptr4(lse));
+  return FA_OK;
+}
+
+fa_status check_bwd_args(const void* q, const void* k, const void* v, const void* o,
+                         const void* dO, const float* lse, void* dq, void* dk, void* dv, int B,
+                         int H, int N, int d, float scale) {
+  FA_TRY(check_shape(B, H, N, d, scale));
+  for (const void* p : {q, k, v, o, dO, static_cast<const void*>(dq), static_cast<const void*>(dk),
+                        static_cast<const void*>(dv)})
+    FA_TRY(check_ptr16(p));
+  FA_TRY(check_ptr4(lse));
+  return FA_OK;
+}
+
+fa_status check_ws(void* ws, size_t have, size_t need) {
+  if (!ws) return FA_ERR_INVALID_ARG;
+  if (!aligned(ws, 256)) return FA_ERR_MISALIGNED;
+  if (have < need) return FA_ERR_WORKSPACE;
+  return FA_OK;
+}
+
+}  // namespace
+
+namespace fa {
+bool make_tile_map(CUtensorMap* map, const void* base, int BH, int N, int d) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                              static_cast<cuuint64_t>(BH)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
+                                 static_cast<cuuint64_t>(N) * d * 2};
+  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(kTile), 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+}  // namespace fa
+
+extern "C" {
+
+const char* fa_status_string(fa_status s) {
+  switch (s) {
+    case FA_OK: return "ok";
+    case FA_ERR_INVALID_ARG: return "invalid argument";
+    case FA_ERR_UNSUPPORTED: return "unsupported size or head dimension";
+    case FA_ERR_MISALIGNED: return "misaligned pointer";
+    case FA_ERR_WORKSPACE: return "workspace too small";
+    case FA_ERR_CUDA: return "CUDA error";
+    case FA_ERR_TIMEOUT: return "device wait timed out";
+  }
+  return "unknown status";
+}
+
+fa_status fa_forward(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                     int N, int d, float scale, int causal, cudaStream_t stream) {
+  FA_TRY(check_fwd_args(q, k, v, o, lse, B, H, N, d, scale));
+  return forward_impl(q, k, v, o, lse, B, H, N, d, scale, causal, nullptr, stream);
+}
+
+size_t fa_backward_workspace_size(int B, int H, int N, int d) {
+  if (B < 1 || H < 1 || N < 1 || d < 1) return 0;
+  return bwd_ws_bytes(B, H, N, d);
+}
+
+fa_status fa_backward_preprocess(const void* o, const void* dO, int B, int H, int N, int d,
+                                 void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  FA_TRY(check_shape(B, H, N, d, 1.f));
+  FA_TRY(check_ptr16(o));
+  FA_TRY(check_ptr16(dO));
+  FA_TRY(check_ws(workspace, workspace_bytes, bwd_ws_bytes(B, H, N, d)));
+  const BwdWorkspace w = bwd_ws(workspace, B, H, N);
+  FA_CUDA(fa::launch_bwd_preprocess(o, dO, w.delta, w.dq_acc, static_cast<long long>(B) * H * N, d,
+                                    stream));
+  return FA_OK;
+}
+
+fa_status fa_backward_main(const void* q, const void* k, const void* v, const void* dO,
+                           const float* lse, void* dk, void* dv, int B, int H, int N, int d,
+                           float scale, int causal, void* workspace, size_t workspace_bytes,
+                           cudaStream_t stream) {
+  FA_TRY(check_shape(B, H, N, d, scale));
+  for (const void* p : {q, k, v, dO, static_cast<const void*>(dk), static_cast<const void*>(dv)})
+    FA_TRY(check_ptr16(p));
+  FA_TRY(check_ptr4(lse));
+  FA_TRY(check_ws(workspace, workspace_bytes, bwd_ws_bytes(B, H, N, d)));
+  return backward_main_impl(q, k, v, dO, lse, dk, dv, B, H, N, d, scale, causal,
+                            bwd_ws(workspace, B, H, N), nullptr, stream);
+}
+
+fa_status fa_backward_dq_convert(void* dq, int B, int H, int N, int d, float scale,
+                                 void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  FA_TRY(check_shape(B, H, N, d, scale));
+  FA_TRY(check_ptr16(dq));
+  FA_TRY(check_ws(workspace, workspace_bytes, bwd_ws_bytes(B, H, N, d)));
+  const BwdWorkspace w = bwd_ws(workspace, B, H, N);
+  FA_CUDA(fa::launch_dq_convert(w.dq_acc, dq, static_cast<long long>(B) * H * N * d, scale, stream));
+  return FA_OK;
+}
+
+fa_status fa_backward(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                      const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                      float scale, int causal, void* workspace, size_t workspace_bytes,
+                      cudaStream_t stream) {
+  FA_TRY(check_bwd_args(q, k, v, o, dO, lse, dq, dk, dv, B, H, N, d, scale));
+  FA_TRY(check_ws(workspace, workspace_bytes, bwd_ws_bytes(B, H, N, d)));
+  FA_TRY(fa_backward_preprocess(o, dO, B, H, N, d, workspace, workspace_bytes, stream));
+  FA_TRY(fa_backward_main(q, k, v, dO, lse, dk, dv, B, H, N, d, scale, causal, workspace,
+                          workspace_bytes, stream));
+  return fa_backward_dq_convert(dq, B, H, N, d, scale, workspace, workspace_bytes, stream);
+}
+
+size_t fa_blocksparse_workspace_size(int B, int H, int N, int d, int mask_heads) {
+  if (B < 1 || H < 1 || N < 1 || d < 1 || mask_heads < 1) return 0;
+  return lists_bytes(N, mask_heads) + bwd_ws_bytes(B, H, N, d);
+}
+
+fa_status fa_blocksparse_build_lists(const uint8_t* block_mask, int mask_heads, int N,
+                                     void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (N < 1 || mask_heads < 1 || !block_mask) return FA_ERR_INVALID_ARG;
+  if (num_tiles(N) > 8192) return FA_ERR_UNSUPPORTED;
+  FA_TRY(check_ws(workspace, workspace_bytes, lists_bytes(N, mask_heads)));
+  return build_lists(block_mask, mask_heads, N, workspace, stream);
+}
+
+fa_status fa_blocksparse_forward(const void* q, const void* k, const void* v, void* o, float* lse,
+                                 int B, int H, int N, int d, float scale, int causal,
+                                 const uint8_t* block_mask, int mask_heads, void* workspace,
+                                 size_t workspace_bytes, cudaStream_t stream) {
+  FA_TRY(check_fwd_args(q, k, v, o, lse, B, H, N, d, scale));
+  FA_TRY(check_mask(block_mask, mask_heads, H, N));
+  FA_TRY(check_ws(workspace, workspace_bytes, lists_bytes(N, mask_heads)));
+  FA_TRY(build_lists(block_mask, mask_heads, N, workspace, stream));
+  const fa::TileLists L = lists_in(workspace, N, mask_heads);
+  return forward_impl(q, k, v, o, lse, B, H, N, d, scale, causal, &L, stream);
+}
+
+fa_status fa_blocksparse_backward(const void* q, const void* k, const void* v, const void* o,
+                                  const void* dO, const float* lse, void* dq, void* dk, void* dv,
+                                  int B, int H, int N, int d, float scale, int causal,
+                                  const uint8_t* block_mask, int mask_heads, void* workspace,
+                                  size_t workspace_bytes, cudaStream_t stream) {
+  FA_TRY(check_bwd_args(q, k, v, o, dO, lse, dq, dk, dv, B, H, N, d, scale));
+  FA_TRY(check_mask(block_mask, mask_heads, H, N));
+  const size_t lb = lists_bytes(N, mask_heads);
+  FA_TRY(check_ws(workspace, workspace_bytes, lb + bwd_ws_bytes(B, H, N, d)));
+  FA_TRY(build_lists(block_mask, mask_heads, N, workspace, stream));
+  const fa::TileLists L = lists_in(workspace, N, mask_heads);
+  void* bws = static_cast<char*>(workspace) + lb;
+  const size_t bws_bytes = workspace_bytes - lb;
+  FA_TRY(fa_backward_preprocess(o, dO, B, H, N, d, bws, bws_bytes, stream));
+  FA_TRY(backward_main_impl(q, k, v, dO, lse, dk, dv, B, H, N, d, scale, causal,
+                            bwd_ws(bws, B, H, N), &L, stream));
+  return fa_backward_dq_convert(dq, B, H, N, d, scale, bws, bws_bytes, stream);
+}
+
+fa_status fa_get_device_status(cudaStream_t stream) {
+  fa_status st = FA_OK;
+  int* w = status_word(&st);
+  if (!w) return st;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return FA_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpyAsync(&v, w, sizeof(int), cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+    return FA_ERR_CUDA;
+  if (cudaMemsetAsync(w, 0, sizeof(int), stream) != cudaSuccess) return FA_ERR_CUDA;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return FA_ERR_CUDA;
+  if (v == 0) return FA_OK;
+  return v == FA_ERR_TIMEOUT ? FA_ERR_TIMEOUT : FA_ERR_CUDA;
+}
+
+fa_status fa_set_wait_limit_ns(unsigned long long ns) {
+  g_wait_ns.store(ns == 0 ? kDefaultWaitNs : ns);
+  return FA_OK;
+}
+
+fa_status fa_debug_wait_timeout(unsigned long long limit_ns, cudaStream_t stream) {
+  if (limit_ns == 0 || limit_ns > 10000000000ull) return FA_ERR_INVALID_ARG;
+  fa_status st = FA_OK;
+  int* err = status_word(&st);
+  if (!err) return st;
+  FA_CUDA(fa::launch_wait_probe(err, limit_ns, stream));
+  return FA_OK;
+}
+
+fa_status fa_debug_schedule(int N, int causal, const uint8_t* block_mask, int mask_heads,
+                            void* workspace, size_t workspace_bytes, int* fwd_counts,
+                            int* bwd_counts, int* fwd_lists, int* bwd_lists, cudaStream_t stream) {
+  if (N < 1 || !fwd_counts || !bwd_counts || !fwd_lists || !bwd_lists) return FA_ERR_INVALID_ARG;
+  if (num_tiles(N) > 8192) return FA_ERR_UNSUPPORTED;
+  fa::TileLists L;
+  int heads = 1;
+  if (block_mask) {
+    if (mask_heads < 1) return FA_ERR_INVALID_ARG;
+    FA_TRY(check_ws(workspace, workspace_bytes, lists_bytes(N, mask_heads)));
+    FA_TRY(build_lists(block_mask, mask_heads, N, workspace, stream));
+    L = lists_in(workspace, N, mask_heads);
+    heads = mask_heads;
+  }
+  FA_CUDA(fa::launch_schedule_export(N, causal, L, heads, fwd_counts, bwd_counts, fwd_lists,
+                                     bwd_lists, stream));
+  return FA_OK;
+}
+
+fa_status fa_debug_mma_probe(const void* a, const void* b, float* c, int mode, int n,
+                             cudaStream_t stream) {
+  if (mode < 0 || mode > 2) return FA_ERR_INVALID_ARG;
+  if (mode == 0) n = 128;
+  if (n != 64 && n != 128) return FA_ERR_UNSUPPORTED;
+  FA_TRY(check_ptr16(a));
+  FA_TRY(check_ptr16(b));
+  FA_TRY(check_ptr16(c));
+  fa_status st = FA_OK;
+  int* err = status_word(&st);
+  if (!err) return st;
+  CUtensorMap ta, tb;
+  if (!fa::make_tile_map(&ta, a, 1, 128, 128) || !fa::make_tile_map(&tb, b, 1, 128, n))
+    return FA_ERR_CUDA;
+  FA_CUDA(fa::launch_mma_probe(ta, tb, a, c, mode, n, err, wait_limit_ns(), stream));
+  return FA_OK;
+}
+
+}  // extern "C"

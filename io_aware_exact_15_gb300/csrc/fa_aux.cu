@@ -1,0 +1,352 @@
+// Small kernels around the two attention kernels: the block-mask -> tile
+// list builder, the backward preprocess (D = rowsum(dO o O), zero dQ
+// accumulator) and dQ conversion, the schedule export used by the tests,
+// a one-tile tcgen05 probe, and the bounded-wait probe.
+#include <math.h>
+#include <stdint.h>
+
+#include "fa_internal.h"
+#include "fa_ptx.cuh"
+#include "fa_sched.cuh"
+
+namespace fa {
+
+// ------------------------------------------------------------------ lists
+// One CTA per mask head.  CSR: for each query tile the ascending key tiles
+// whose mask byte is nonzero; CSC: for each key tile the ascending query
+// tiles ("Block-sparse FlashAttention": only nonzero blocks are visited).
+__global__ void __launch_bounds__(1024) fa_lists_kernel(const uint8_t* __restrict__ mask, int nT,
+                                                        int* row_ptr, int* col_idx, int* col_ptr,
+                                                        int* row_idx) {
+  extern __shared__ int cnt[];  // [nT + 1]
+  const int h = blockIdx.x;
+  const uint8_t* m = mask + static_cast<size_t>(h) * nT * nT;
+  int* rp = row_ptr + static_cast<size_t>(h) * (nT + 1);
+  int* cp = col_ptr + static_cast<size_t>(h) * (nT + 1);
+  int* ci = col_idx + static_cast<size_t>(h) * nT * nT;
+  int* ri = row_idx + static_cast<size_t>(h) * nT * nT;
+  for (int pass = 0; pass < 2; ++pass) {
+    // pass 0: rows (CSR), pass 1: columns (CSC)
+    for (int a = threadIdx.x; a < nT; a += blockDim.x) {
+      int c = 0;
+      for (int b = 0; b < nT; ++b) {
+        const size_t e = pass == 0 ? static_cast<size_t>(a) * nT + b : static_cast<size_t>(b) * nT + a;
+        c += m[e] != 0;
+      }
+      cnt[a] = c;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      int run = 0;
+      for (int a = 0; a < nT; ++a) {
+        const int c = cnt[a];
+        cnt[a] = run;
+        run += c;
+      }
+      cnt[nT] = run;
+    }
+    __syncthreads();
+    int* ptr = pass == 0 ? rp : cp;
+    int* idx = pass == 0 ? ci : ri;
+    for (int a = threadIdx.x; a <= nT; a += blockDim.x) ptr[a] = cnt[a];
+    for (int a = threadIdx.x; a < nT; a += blockDim.x) {
+      int pos = cnt[a];
+      for (int b = 0; b < nT; ++b) {
+        const size_t e = pass == 0 ? static_cast<size_t>(a) * nT + b : static_cast<size_t>(b) * nT + a;
+        if (m[e] != 0) idx[pos++] = b;
+      }
+    }
+    __syncthreads();
+  }
+}
+
+cudaError_t launch_build_lists(const uint8_t* mask, int mask_heads, int nT, int* row_ptr,
+                               int* col_idx, int* col_ptr, int* row_idx, cudaStream_t stream) {
+  const int smem = (nT + 1) * static_cast<int>(sizeof(int));
+  if (smem > 48 * 1024) {
+    cudaError_t e =
+        cudaFuncSetAttribute(fa_lists_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+  }
+  fa_lists_kernel<<<mask_heads, 1024, smem, stream>>>(mask, nT, row_ptr, col_idx, col_ptr, row_idx);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ backward helpers
+// D_i = sum_c dO_ic O_ic in fp32 (one warp per row) and dQ_acc = 0.
+template <int D>
+__global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const uint16_t* __restrict__ o,
+                                                         const uint16_t* __restrict__ dO,
+                                                         float* __restrict__ delta,
+                                                         float* __restrict__ dq_acc,
+                                                         long long rows) {
+  constexpr int PER = D / 32;  // elements per lane: 2 or 4
+  const int lane = threadIdx.x & 31;
+  const long long warps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
+  for (long long row = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+       row < rows; row += warps) {
+    const size_t base = static_cast<size_t>(row) * D + lane * PER;
+    float acc = 0.f;
+    if (PER == 2) {
+      const uint32_t a = *reinterpret_cast<const uint32_t*>(o + base);
+      const uint32_t b = *reinterpret_cast<const uint32_t*>(dO + base);
+      acc = __uint_as_float(a << 16) * __uint_as_float(b << 16) +
+            __uint_as_float(a & 0xFFFF0000u) * __uint_as_float(b & 0xFFFF0000u);
+      *reinterpret_cast<float2*>(dq_acc + base) = make_float2(0.f, 0.f);
+    } else {
+      const uint2 a = *reinterpret_cast<const uint2*>(o + base);
+      const uint2 b = *reinterpret_cast<const uint2*>(dO + base);
+      acc = __uint_as_float(a.x << 16) * __uint_as_float(b.x << 16) +
+            __uint_as_float(a.x & 0xFFFF0000u) * __uint_as_float(b.x & 0xFFFF0000u) +
+            __uint_as_float(a.y << 16) * __uint_as_float(b.y << 16) +
+            __uint_as_float(a.y & 0xFFFF0000u) * __uint_as_float(b.y & 0xFFFF0000u);
+      *reinterpret_cast<float4*>(dq_acc + base) = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (lane == 0) delta[row] = acc;
+  }
+}
+
+cudaError_t launch_bwd_preprocess(const void* o, const void* dO, float* delta, float* dq_acc,
+                                  long long rows, int d, cudaStream_t stream) {
+  const long long want = (rows + 7) / 8;
+  const int blocks = static_cast<int>(want < 152LL * 16 ? want : 152LL * 16);
+  if (d == 64)
+    fa_bwd_pre_kernel<64><<<blocks, 256, 0, stream>>>(static_cast<const uint16_t*>(o),
+                                                      static_cast<const uint16_t*>(dO), delta,
+                                                      dq_acc, rows);
+  else
+    fa_bwd_pre_kernel<128><<<blocks, 256, 0, stream>>>(static_cast<const uint16_t*>(o),
+                                                       static_cast<const uint16_t*>(dO), delta,
+                                                       dq_acc, rows);
+  return cudaGetLastError();
+}
+
+// dq = bf16(scale * dq_acc), 8 elements per thread
+__global__ void __launch_bounds__(256) fa_dq_convert_kernel(const float4* __restrict__ acc,
+                                                            uint4* __restrict__ dq, long long n8,
+                                                            float scale) {
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
+       i += stride) {
+    const float4 a = acc[2 * i], b = acc[2 * i + 1];
+    uint4 w;
+    w.x = pack_bf16(a.x * scale, a.y * scale);
+    w.y = pack_bf16(a.z * scale, a.w * scale);
+    w.z = pack_bf16(b.x * scale, b.y * scale);
+    w.w = pack_bf16(b.z * scale, b.w * scale);
+    dq[i] = w;
+  }
+}
+
+cudaError_t launch_dq_convert(const float* dq_acc, void* dq, long long n, float scale,
+                              cudaStream_t stream) {
+  const long long n8 = n / 8;
+  const long long want = (n8 + 255) / 256;
+  const int blocks = static_cast<int>(want < 152LL * 16 ? want : 152LL * 16);
+  fa_dq_convert_kernel<<<blocks, 256, 0, stream>>>(reinterpret_cast<const float4*>(dq_acc),
+                                                   static_cast<uint4*>(dq), n8, scale);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ schedule export
+// Runs the kernels' own schedule code and writes, per head layout, the key
+// tiles each query tile visits in the forward and the query tiles each key
+// tile visits in the backward.  lists are [heads][nT][nT], counts [heads][nT].
+__global__ void fa_schedule_kernel(int N, int causal, TileLists L, int heads, int* fc, int* bc,
+                                   int* fl, int* bl) {
+  const int nT = (N + kTile - 1) / kTile, npairs = (nT + 1) / 2;
+  const long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const long long nf = static_cast<long long>(heads) * npairs;
+  const long long nb = static_cast<long long>(heads) * nT;
+  if (t < nf) {
+    const int head = static_cast<int>(t / npairs), pair = static_cast<int>(t % npairs);
+    FwdSchedule s;
+    s.init(pair, nT, causal != 0, L, head);
+    int c0 = 0, c1 = 0, kt, mem;
+    int* l0 = fl + (static_cast<size_t>(head) * nT + s.qt[0]) * nT;
+    int* l1 = fl + (static_cast<size_t>(head) * nT + (s.act[1] ? s.qt[1] : s.qt[0])) * nT;
+    while (s.next(kt, mem)) {
+      if (mem & 1) l0[c0++] = kt;
+      if (mem & 2) l1[c1++] = kt;
+    }
+    fc[static_cast<size_t>(head) * nT + s.qt[0]] = c0;
+    if (s.act[1]) fc[static_cast<size_t>(head) * nT + s.qt[1]] = c1;
+  } else if (t < nf + nb) {
+    const long long u = t - nf;
+    const int head = static_cast<int>(u / nT), kt = static_cast<int>(u % nT);
+    BwdSchedule s;
+    s.init(kt, nT, causal != 0, L, head);
+    int c = 0, qt;
+    int* lo = bl + (static_cast<size_t>(head) * nT + kt) * nT;
+    while (s.next(qt)) lo[c++] = qt;
+    bc[static_cast<size_t>(head) * nT + kt] = c;
+  }
+}
+
+cudaError_t launch_schedule_export(int N, int causal, const TileLists& lists, int heads,
+                                   int* fwd_counts, int* bwd_counts, int* fwd_lists,
+                                   int* bwd_lists, cudaStream_t stream) {
+  const int nT = (N + kTile - 1) / kTile, npairs = (nT + 1) / 2;
+  const long long total = static_cast<long long>(heads) * (npairs + nT);
+  const int blocks = static_cast<int>((total + 127) / 128);
+  fa_schedule_kernel<<<blocks, 128, 0, stream>>>(N, causal, lists, heads, fwd_counts, bwd_counts,
+                                                 fwd_lists, bwd_lists);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ tcgen05 probe
+// One CTA, one 128-row tile, the operand forms the attention kernels use:
+//   mode 0: C[128x128] = A B^T, A and B [128 x 128] K-major through TMA
+//           (the S = Q K^T form)
+//   mode 1: C[128xn] = A B, A [128 x 128] written by threads in the 128-byte
+//           swizzle, B [128 x n] MN-major through TMA (the O += P V form)
+//   mode 2: C[128xn] = A^T B, A [128 x 128] and B [128 x n] both MN-major
+//           through TMA (the dV += P^T dO and dK += dS^T Q forms)
+__global__ void __launch_bounds__(128, 1)
+    fa_mma_probe_kernel(const __grid_constant__ CUtensorMap ta,
+                        const __grid_constant__ CUtensorMap tb, const uint16_t* a_raw, float* c,
+                        int mode, int n, int* err, uint64_t wait_ns) {
+  constexpr int CHUNK = 16384;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sb = smem_u32(smem);
+  const uint32_t A = sb, B = sb + 2 * CHUNK, bar_ld = sb + 4 * CHUNK, bar_mma = bar_ld + 8;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + 4 * CHUNK + 16);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + 4 * CHUNK + 20);
+  const int warp = threadIdx.x >> 5, t = threadIdx.x;
+  if (t == 0) {
+    mbar_init(bar_ld, 1);
+    mbar_init(bar_mma, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_u32(tmem_slot), 128);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const WaitCtl wc{abort_flag, err, wait_ns};
+  const int nb_chunks = (mode == 0) ? 2 : n / 64;
+  if (t == 0) {
+    const int a_chunks = (mode == 1) ? 0 : 2;
+    mbar_arrive_expect_tx(bar_ld, (a_chunks + nb_chunks) * CHUNK);
+    for (int cc = 0; cc < a_chunks; ++cc) tma_load_3d(A + cc * CHUNK, &ta, bar_ld, 64 * cc, 0, 0);
+    for (int cc = 0; cc < nb_chunks; ++cc) tma_load_3d(B + cc * CHUNK, &tb, bar_ld, 64 * cc, 0, 0);
+  }
+  if (mode == 1) {
+    // thread t writes row t of A (128 bf16) in the 128-byte swizzle
+    const uint4* src = reinterpret_cast<const uint4*>(a_raw + t * 128);
+    for (int cc = 0; cc < 16; ++cc) {
+      const uint4 w = src[cc];
+      st_shared_v4(A + (cc >> 3) * CHUNK + sw128_offset(t, cc & 7), w.x, w.y, w.z, w.w);
+    }
+    fence_async_smem();
+  }
+  __syncthreads();
+  bool ok = true;
+  if (t == 0) {
+    ok = wait_bar(bar_ld, 0, wc);
+    if (ok) {
+      tc_fence_after();
+      if (mode == 0) {
+        const uint32_t id = idesc_bf16(128, 128, false, false);
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t off = (kk >> 2) * CHUNK + (kk & 3) * 32;
+          mma_bf16_ss(tmem, desc_sw128(A + off, 16, 1024), desc_sw128(B + off, 16, 1024), id,
+                      kk > 0);
+        }
+      } else if (mode == 1) {
+        const uint32_t id = idesc_bf16(128, n, false, true);
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t aoff = (kk >> 2) * CHUNK + (kk & 3) * 32;
+          mma_bf16_ss(tmem, desc_sw128(A + aoff, 16, 1024), desc_sw128(B + kk * 2048, CHUNK, 1024),
+                      id, kk > 0);
+        }
+      } else {
+        const uint32_t id = idesc_bf16(128, n, true, true);
+        for (int kk = 0; kk < 8; ++kk)
+          mma_bf16_ss(tmem, desc_sw128(A + kk * 2048, CHUNK, 1024),
+                      desc_sw128(B + kk * 2048, CHUNK, 1024), id, kk > 0);
+      }
+    }
+    mma_commit(bar_mma);
+    drain_bar(bar_mma, 0, wait_ns);
+    if (!ok) drain_bar(bar_ld, 0, wait_ns);
+  }
+  __syncthreads();
+  ok = !*abort_flag;
+  tc_fence_after();
+  const int ncols = (mode == 0) ? 128 : n;
+  if (ok) {
+    for (int cc = 0; cc < ncols / 32; ++cc) {
+      uint32_t r[32];
+      tmem_ld32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + 32 * cc, r);
+      tmem_ld_wait();
+      reg_fence(r);
+      for (int j = 0; j < 32; ++j) c[t * ncols + 32 * cc + j] = __uint_as_float(r[j]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 128);
+  }
+}
+
+cudaError_t launch_mma_probe(const CUtensorMap& ta, const CUtensorMap& tb, const void* a_raw,
+                             float* c, int mode, int n, int* err, uint64_t wait_ns,
+                             cudaStream_t stream) {
+  const int smem = 4 * 16384 + 64 + 1024;
+  cudaError_t e = cudaFuncSetAttribute(fa_mma_probe_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  fa_mma_probe_kernel<<<1, 128, smem, stream>>>(ta, tb, static_cast<const uint16_t*>(a_raw), c,
+                                                mode, n, err, wait_ns);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ wait probe
+// Waits on an mbarrier that nothing will ever complete.  The bounded wait
+// gives up after wait_ns, records the timeout in the status word and the
+// kernel returns normally.
+__global__ void fa_wait_probe_kernel(int* err, uint64_t wait_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(smem_u32(&bar), 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const WaitCtl wc{&abort_flag, err, wait_ns};
+    (void)wait_bar(smem_u32(&bar), 0, wc);
+  }
+  __syncthreads();
+}
+
+cudaError_t launch_wait_probe(int* err, uint64_t wait_ns, cudaStream_t stream) {
+  fa_wait_probe_kernel<<<1, 32, 0, stream>>>(err, wait_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace fa
+
+// ------------------------------------------------------------------ status word
+// One per device (each device that loads the module gets its own copy).
+__device__ int g_fa_status_word = 0;
+
+namespace fa {
+int* status_word_address() {
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_fa_status_word) != cudaSuccess) return nullptr;
+  return static_cast<int*>(p);
+}
+}  // namespace fa

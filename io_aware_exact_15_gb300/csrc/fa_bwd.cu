@@ -1,0 +1,434 @@
+// Backward pass of exact attention by recomputation (FlashAttention hackmd
+// summary, "Recomputation": the forward keeps only O and the softmax
+// statistics; the backward rebuilds S and P block by block instead of
+// reading an N x N matrix).  With lse from the forward and
+// D_i = <dO_i, O_i> from the preprocess kernel, for each key tile j and every
+// query tile i that reaches it:
+//   S = Q_i K_j^T,  P = exp(scale*S - lse_i),  dP = dO_i V_j^T,
+//   dS = P o (dP - D_i),
+//   dV_j += P^T dO_i,  dK_j += dS^T Q_i,  dQ_i += dS K_j  (dQ, dK scaled later).
+//
+// GB300 design (one CTA = one head x one 128-key tile; K_j, V_j stay in
+// shared memory while the CTA walks the query tiles):
+//   warp 0      TMA producer: K_j, V_j once; Q_i through an NQ-slot ring and
+//               dO_i through an NDO-slot ring (128-byte swizzle)
+//   warp 1      allocates 512 TMEM columns; lane 0 issues the five MMAs
+//   warps 2-5   one thread per query row: P from S and lse (ex2 with the
+//               scale folded in), dS from dP and D, both written to shared
+//               memory as bf16 for the MMAs that read them
+//   warps 6-9   one thread per query row: read dQ_i from TMEM and add it into
+//               the fp32 dQ accumulator with vector reductions
+// At the end warps 2-5 write dV_j and warps 6-9 write scale * dK_j.
+// TMEM: S [0,128) dP [128,256) dV [256,256+d) dK [256+d,256+2d);
+//       dQ at [384,448) for d = 64 and over the dP columns for d = 128.
+#include <math.h>
+
+#include "fa_internal.h"
+#include "fa_ptx.cuh"
+#include "fa_sched.cuh"
+
+namespace fa {
+namespace {
+
+template <int D>
+struct BwdSmem {
+  static constexpr int CH = D / 64;
+  static constexpr int CHUNK = kTile * 128;
+  static constexpr int TILE = CH * CHUNK;
+  static constexpr int NQ = (D == 64) ? 3 : 2;
+  static constexpr int NDO = (D == 64) ? 3 : 1;
+  static constexpr int PT = 2 * CHUNK;  // 128 x 128 bf16
+  static constexpr int K = 0;
+  static constexpr int V = K + TILE;
+  static constexpr int QR = V + TILE;
+  static constexpr int DOR = QR + NQ * TILE;
+  static constexpr int P = DOR + NDO * TILE;
+  static constexpr int DS = P + PT;
+  static constexpr int BAR = DS + PT;
+  static constexpr int B_KV = 0, B_QF = 1, B_QE = B_QF + NQ, B_DOF = B_QE + NQ,
+                       B_DOE = B_DOF + NDO, B_SF = B_DOE + NDO, B_DPF = B_SF + 1,
+                       B_PR = B_DPF + 1, B_DSR = B_PR + 1, B_DQF = B_DSR + 1, B_DQE = B_DQF + 1,
+                       B_FIN = B_DQE + 1, NBAR = B_FIN + 1;
+  static constexpr int MISC = BAR + NBAR * 8;
+  static constexpr int ALLOC = MISC + 16 + 1024;
+  static_assert(ALLOC <= 232448, "shared memory budget");
+  // TMEM columns
+  static constexpr int T_S = 0, T_DP = 128, T_DV = 256, T_DK = 256 + D;
+  static constexpr int T_DQ = (D == 64) ? 384 : T_DP;
+};
+
+constexpr int kBwdThreads = 320;
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int D>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    fa_bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                  const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
+                  const BwdParams p) {
+  using L = BwdSmem<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sb = smem_u32(smem);
+  auto bar = [&](int i) { return sb + L::BAR + 8 * i; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::MISC + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int N = p.N;
+  const int nT = (N + kTile - 1) / kTile;
+  const int BH = p.B * p.H;
+  int bh, kt;
+  bwd_cta_coords(blockIdx.x, BH, nT, p.causal != 0, bh, kt);
+  const int head = bh % p.H;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(L::B_KV), 1);
+    for (int s = 0; s < L::NQ; ++s) {
+      mbar_init(bar(L::B_QF + s), 1);
+      mbar_init(bar(L::B_QE + s), 1);
+    }
+    for (int s = 0; s < L::NDO; ++s) {
+      mbar_init(bar(L::B_DOF + s), 1);
+      mbar_init(bar(L::B_DOE + s), 1);
+    }
+    mbar_init(bar(L::B_SF), 1);
+    mbar_init(bar(L::B_DPF), 1);
+    mbar_init(bar(L::B_PR), 128);
+    mbar_init(bar(L::B_DSR), 128);
+    mbar_init(bar(L::B_DQF), 1);
+    mbar_init(bar(L::B_DQE), 128);
+    mbar_init(bar(L::B_FIN), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const WaitCtl wc{abort_flag, p.err, p.wait_ns};
+
+  BwdSchedule sch;
+  sch.init(kt, nT, p.causal != 0, p.lists, head);
+
+  if (warp == 0) {
+    // ------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      prefetch_tmap(&tq);
+      prefetch_tmap(&tk);
+      prefetch_tmap(&tv);
+      prefetch_tmap(&tdo);
+      mbar_arrive_expect_tx(bar(L::B_KV), 2 * L::TILE);
+#pragma unroll
+      for (int c = 0; c < L::CH; ++c) {
+        tma_load_3d(sb + L::K + c * L::CHUNK, &tk, bar(L::B_KV), 64 * c, kt * kTile, bh);
+        tma_load_3d(sb + L::V + c * L::CHUNK, &tv, bar(L::B_KV), 64 * c, kt * kTile, bh);
+      }
+      uint32_t nq = 0, nd = 0;  // Q / dO copies issued
+      bool ok = true;
+      int qt;
+      while (ok && sch.next(qt)) {
+        const int qpos = nq % L::NQ, dpos = nd % L::NDO;
+        const uint32_t qround = nq / L::NQ, dround = nd / L::NDO;
+        if (qround > 0 && !wait_bar(bar(L::B_QE + qpos), (qround - 1) & 1, wc)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(bar(L::B_QF + qpos), L::TILE);
+#pragma unroll
+        for (int c = 0; c < L::CH; ++c)
+          tma_load_3d(sb + L::QR + qpos * L::TILE + c * L::CHUNK, &tq, bar(L::B_QF + qpos), 64 * c,
+                      qt * kTile, bh);
+        ++nq;
+        if (dround > 0 && !wait_bar(bar(L::B_DOE + dpos), (dround - 1) & 1, wc)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(bar(L::B_DOF + dpos), L::TILE);
+#pragma unroll
+        for (int c = 0; c < L::CH; ++c)
+          tma_load_3d(sb + L::DOR + dpos * L::TILE + c * L::CHUNK, &tdo, bar(L::B_DOF + dpos),
+                      64 * c, qt * kTile, bh);
+        ++nd;
+      }
+      // let copies still in flight land before the CTA can exit
+      drain_bar(bar(L::B_KV), 0, p.wait_ns);
+      if (!ok) {
+        const uint32_t fq = nq > static_cast<uint32_t>(L::NQ) ? nq - L::NQ : 0;
+        for (uint32_t j = fq; j < nq; ++j)
+          drain_bar(bar(L::B_QF + j % L::NQ), (j / L::NQ) & 1, p.wait_ns);
+        const uint32_t fd = nd > static_cast<uint32_t>(L::NDO) ? nd - L::NDO : 0;
+        for (uint32_t j = fd; j < nd; ++j)
+          drain_bar(bar(L::B_DOF + j % L::NDO), (j / L::NDO) & 1, p.wait_ns);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idSS = idesc_bf16(128, 128, false, false);  // S, dP
+      constexpr uint32_t idTT = idesc_bf16(128, D, true, true);      // dV, dK
+      constexpr uint32_t idDQ = idesc_bf16(128, D, false, true);     // dQ
+      // X[128 q x 128 k] = A[128 x D] B[128 x D]^T, both K-major
+      auto issue_qk = [&](uint32_t dst, uint32_t a, uint32_t b) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * L::CHUNK + (kk & 3) * 32;
+          mma_bf16_ss(dst, desc_sw128(a + off, 16, 1024), desc_sw128(b + off, 16, 1024), idSS,
+                      kk > 0);
+        }
+      };
+      // Y[128 k x D] += X^T[128 k x 128 q] Z[128 q x D]; X stored [q][k]
+      auto issue_tt = [&](uint32_t dst, uint32_t x, uint32_t z, bool acc) {
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          mma_bf16_ss(dst, desc_sw128(x + kk * 2048, L::CHUNK, 1024),
+                      desc_sw128(z + kk * 2048, L::CHUNK, 1024), idTT, (acc || kk > 0) ? 1u : 0u);
+      };
+      // dQ[128 q x D] = dS[128 q x 128 k] K[128 k x D]
+      auto issue_dq = [&](uint32_t dst) {
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk) {
+          const uint32_t aoff = (kk >> 2) * L::CHUNK + (kk & 3) * 32;
+          mma_bf16_ss(dst, desc_sw128(sb + L::DS + aoff, 16, 1024),
+                      desc_sw128(sb + L::K + kk * 2048, L::CHUNK, 1024), idDQ, kk > 0);
+        }
+      };
+      const uint32_t tS = tmem + L::T_S, tDP = tmem + L::T_DP, tDV = tmem + L::T_DV,
+                     tDK = tmem + L::T_DK, tDQ = tmem + L::T_DQ;
+      int qt, qt_n;
+      bool ok = wait_bar(bar(L::B_KV), 0, wc);
+      bool have = sch.next(qt);
+      uint32_t n = 0;
+      if (ok && have) {
+        ok = wait_bar(bar(L::B_QF + 0), 0, wc);
+        if (ok) {
+          tc_fence_after();
+          issue_qk(tS, sb + L::QR, sb + L::K);
+          mma_commit(bar(L::B_SF));
+          ok = wait_bar(bar(L::B_DOF + 0), 0, wc);
+        }
+        if (ok) {
+          tc_fence_after();
+          issue_qk(tDP, sb + L::DOR, sb + L::V);
+          mma_commit(bar(L::B_DPF));
+        }
+      }
+      while (ok && have) {
+        const bool have_n = sch.next(qt_n);
+        const uint32_t qpos = n % L::NQ, dpos = n % L::NDO;
+        const uint32_t n1 = n + 1;
+        // dV += P^T dO_i once P is in shared memory
+        if (!(ok = wait_bar(bar(L::B_PR), n & 1, wc))) break;
+        tc_fence_after();
+        issue_tt(tDV, sb + L::P, sb + L::DOR + dpos * L::TILE, n > 0);
+        mma_commit(bar(L::B_DOE + dpos));
+        // next S as soon as its Q tile is in (the S columns were read)
+        if (have_n) {
+          if (!(ok = wait_bar(bar(L::B_QF + n1 % L::NQ), (n1 / L::NQ) & 1, wc))) break;
+          tc_fence_after();
+          issue_qk(tS, sb + L::QR + (n1 % L::NQ) * L::TILE, sb + L::K);
+          mma_commit(bar(L::B_SF));
+        }
+        // dK += dS^T Q_i, dQ_i = dS K once dS is in shared memory
+        if (!(ok = wait_bar(bar(L::B_DSR), n & 1, wc))) break;
+        tc_fence_after();
+        issue_tt(tDK, sb + L::DS, sb + L::QR + qpos * L::TILE, n > 0);
+        mma_commit(bar(L::B_QE + qpos));
+        if (D == 64 && n > 0) {
+          if (!(ok = wait_bar(bar(L::B_DQE), (n - 1) & 1, wc))) break;
+          tc_fence_after();
+        }
+        issue_dq(tDQ);
+        mma_commit(bar(L::B_DQF));
+        if (have_n) {
+          if (D != 64) {  // dQ_i shares the dP columns: wait until it is read out
+            if (!(ok = wait_bar(bar(L::B_DQE), n & 1, wc))) break;
+            tc_fence_after();
+          }
+          if (!(ok = wait_bar(bar(L::B_DOF + n1 % L::NDO), (n1 / L::NDO) & 1, wc))) break;
+          tc_fence_after();
+          issue_qk(tDP, sb + L::DOR + (n1 % L::NDO) * L::TILE, sb + L::V);
+          mma_commit(bar(L::B_DPF));
+        }
+        qt = qt_n;
+        have = have_n;
+        n = n1;
+      }
+      mma_commit(bar(L::B_FIN));
+      drain_bar(bar(L::B_FIN), 0, p.wait_ns);
+    }
+  } else {
+    const bool compute = warp < 6;  // warps 2-5: P / dS;  warps 6-9: dQ read-out
+    const int q4 = warp & 3;
+    const int r = q4 * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
+    const float sl2 = p.scale * kLog2e;
+    const int kbase = kt * kTile;
+    bool ok = true;
+    uint32_t n = 0;
+    int qt;
+    while (ok && sch.next(qt)) {
+      const int qrow = qt * kTile + r;
+      const bool row_ok = qrow < N;
+      if (compute) {
+        const size_t ridx = static_cast<size_t>(bh) * N + (row_ok ? qrow : 0);
+        const float lse = p.lse[ridx];
+        const float dlt = p.delta[ridx];
+        const bool live = row_ok && lse != -INFINITY;
+        const float lse2 = live ? lse * kLog2e : 0.f;
+        ok = __all_sync(0xffffffffu, wait_bar(bar(L::B_SF), n & 1, wc));
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t pr[4][32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld32(tmem + lane_off + L::T_S + 32 * c, pr[c]);
+        tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < 4; ++c) reg_fence(pr[c]);
+        const bool need_mask = (kbase + kTile > N) || (p.causal && kbase + kTile - 1 > qt * kTile);
+        // P = exp2(S * scale * log2e - lse * log2e), masked entries 0
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            float pv = ex2(fmaf(__uint_as_float(pr[c][j]), sl2, -lse2));
+            if (need_mask) {
+              const int key = kbase + 32 * c + j;
+              if (key >= N || (p.causal && key > qrow)) pv = 0.f;
+            }
+            pr[c][j] = __float_as_uint(live ? pv : 0.f);
+          }
+#pragma unroll
+        for (int cc = 0; cc < 16; ++cc) {
+          const uint32_t* e = &pr[cc >> 2][(cc & 3) * 8];
+          st_shared_v4(sb + L::P + (cc >> 3) * L::CHUNK + sw128_offset(r, cc & 7),
+                       pack_bf16(__uint_as_float(e[0]), __uint_as_float(e[1])),
+                       pack_bf16(__uint_as_float(e[2]), __uint_as_float(e[3])),
+                       pack_bf16(__uint_as_float(e[4]), __uint_as_float(e[5])),
+                       pack_bf16(__uint_as_float(e[6]), __uint_as_float(e[7])));
+        }
+        fence_async_smem();
+        tc_fence_before();
+        mbar_arrive(bar(L::B_PR));
+        // dS = P o (dP - D_i)
+        ok = __all_sync(0xffffffffu, wait_bar(bar(L::B_DPF), n & 1, wc));
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t dp[32];
+          tmem_ld32(tmem + lane_off + L::T_DP + 32 * c, dp);
+          tmem_ld_wait();
+          reg_fence(dp);
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            float x[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              x[j] = __uint_as_float(pr[c][8 * g + j]) * (__uint_as_float(dp[8 * g + j]) - dlt);
+            const int cc = 4 * c + g;
+            st_shared_v4(sb + L::DS + (cc >> 3) * L::CHUNK + sw128_offset(r, cc & 7),
+                         pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]), pack_bf16(x[4], x[5]),
+                         pack_bf16(x[6], x[7]));
+          }
+        }
+        fence_async_smem();
+        tc_fence_before();
+        mbar_arrive(bar(L::B_DSR));
+      } else {
+        ok = __all_sync(0xffffffffu, wait_bar(bar(L::B_DQF), n & 1, wc));
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t dq[D / 32][32];
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) tmem_ld32(tmem + lane_off + L::T_DQ + 32 * c, dq[c]);
+        tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) reg_fence(dq[c]);
+        tc_fence_before();
+        mbar_arrive(bar(L::B_DQE));
+        if (row_ok) {
+          float* dst = p.dq_acc + (static_cast<size_t>(bh) * N + qrow) * D;
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c)
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              red_add_v4(dst + 32 * c + 4 * v, __uint_as_float(dq[c][4 * v + 0]),
+                         __uint_as_float(dq[c][4 * v + 1]), __uint_as_float(dq[c][4 * v + 2]),
+                         __uint_as_float(dq[c][4 * v + 3]));
+        }
+      }
+      ++n;
+    }
+    // ---------------------------------------------------- epilogue: dV, dK
+    if (ok) ok = __all_sync(0xffffffffu, wait_bar(bar(L::B_FIN), 0, wc));
+    tc_fence_after();
+    const int key = kbase + r;
+    if (ok) {  // warp-uniform: every lane takes part in the TMEM reads
+      const uint32_t tcol = compute ? L::T_DV : L::T_DK;
+      const float mul = compute ? 1.f : p.scale;
+      uint8_t* dst = static_cast<uint8_t*>(compute ? p.dv : p.dk) +
+                     (static_cast<size_t>(bh) * N + (key < N ? key : 0)) * static_cast<size_t>(D) * 2;
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t a[32];
+        if (n > 0) {
+          tmem_ld32(tmem + lane_off + tcol + 32 * c, a);
+          tmem_ld_wait();
+          reg_fence(a);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) a[j] = 0u;
+        }
+        if (key < N) {
+          uint4* o4 = reinterpret_cast<uint4*>(dst + c * 64);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            uint4 w;
+            w.x = pack_bf16(__uint_as_float(a[8 * v + 0]) * mul, __uint_as_float(a[8 * v + 1]) * mul);
+            w.y = pack_bf16(__uint_as_float(a[8 * v + 2]) * mul, __uint_as_float(a[8 * v + 3]) * mul);
+            w.z = pack_bf16(__uint_as_float(a[8 * v + 4]) * mul, __uint_as_float(a[8 * v + 5]) * mul);
+            w.w = pack_bf16(__uint_as_float(a[8 * v + 6]) * mul, __uint_as_float(a[8 * v + 7]) * mul);
+            o4[v] = w;
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D>
+cudaError_t launch_bwd_d(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
+                         const CUtensorMap& tv, const CUtensorMap& tdo, cudaStream_t stream) {
+  using L = BwdSmem<D>;
+  cudaError_t e = cudaFuncSetAttribute(fa_bwd_kernel<D>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
+  if (e != cudaSuccess) return e;
+  const int nT = (p.N + kTile - 1) / kTile;
+  const long long ctas = static_cast<long long>(nT) * p.B * p.H;
+  fa_bwd_kernel<D><<<static_cast<unsigned>(ctas), kBwdThreads, L::ALLOC, stream>>>(tq, tk, tv, tdo,
+                                                                                   p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_backward_main(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
+                                 const CUtensorMap& tv, const CUtensorMap& tdo,
+                                 cudaStream_t stream) {
+  if (p.d == 64) return launch_bwd_d<64>(p, tq, tk, tv, tdo, stream);
+  if (p.d == 128) return launch_bwd_d<128>(p, tq, tk, tv, tdo, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace fa

@@ -1,0 +1,384 @@
+// Forward pass of exact attention, tile by tile with an online softmax
+// (FlashAttention hackmd summary, "Tiling" and "Kernel Fusion": Q, K, V are
+// split into blocks that are brought on chip, the row max m and the row sum
+// l of exponentials are carried from block to block, and O is rescaled so
+// the final result equals the full softmax; one kernel does
+// matmul -> mask -> softmax -> matmul and only O and the statistics reach
+// HBM).  The statistic written is lse = m + ln l.
+//
+// GB300 design (one CTA = one head x two 128-row query tiles):
+//   warp 0      TMA producer: both Q tiles once, then K_j, V_j through an
+//               NS-deep ring of 128 x d tiles (128-byte swizzle)
+//   warp 1      allocates 512 TMEM columns; lane 0 issues every tcgen05.mma:
+//               S_s = Q_s K_j^T (fp32 in TMEM) and O_s += P_s V_j
+//   warps 2-5   softmax for query tile 0, warps 6-9 for query tile 1: one
+//               thread per query row reads its 128 scores from TMEM, applies
+//               the causal / ragged-length mask, updates (m, l) in the log2
+//               domain with the scale folded into one FMA before ex2, writes
+//               P (bf16) into shared memory for the PV MMA, and rescales its
+//               O row in TMEM only when the running max grew by more than
+//               2^8 (the final O / l uses the same m, so this stays exact).
+// While one warpgroup does its softmax the tensor core runs the other tile's
+// MMAs.  TMEM columns: S0 [0,128) S1 [128,256) O0 [256,256+d) O1 [.., +d).
+#include <math.h>
+
+#include "fa_internal.h"
+#include "fa_ptx.cuh"
+#include "fa_sched.cuh"
+
+namespace fa {
+namespace {
+
+template <int D>
+struct FwdSmem {
+  static constexpr int CH = D / 64;             // 128-byte column chunks per row
+  static constexpr int CHUNK = kTile * 128;     // [128 rows x 128 B] = 16 KB
+  static constexpr int TILE = CH * CHUNK;       // one 128 x D bf16 tile
+  static constexpr int NS = (D == 64) ? 6 : 3;  // K/V ring slots (one tile each)
+  static constexpr int PT = 2 * CHUNK;          // one 128 x 128 bf16 P tile
+  static constexpr int Q = 0;
+  static constexpr int P = Q + 2 * TILE;
+  static constexpr int KV = P + 2 * PT;
+  static constexpr int BAR = KV + NS * TILE;
+  static constexpr int B_Q = 0, B_KVF = 1, B_KVE = 1 + NS, B_SF = 1 + 2 * NS, B_PF = B_SF + 2,
+                       B_OF = B_PF + 2, NBAR = B_OF + 1;
+  static constexpr int MISC = BAR + NBAR * 8;
+  static constexpr int ALLOC = MISC + 16 + 1024;  // + slack for 1024-byte alignment
+  static_assert(ALLOC <= 232448, "shared memory budget");
+};
+
+constexpr int kFwdThreads = 320;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleLog2 = 8.0f;  // lazy rescale threshold (factor 256)
+
+template <int D>
+__global__ void __launch_bounds__(kFwdThreads, 1)
+    fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                  const __grid_constant__ CUtensorMap tv, const FwdParams p) {
+  using L = FwdSmem<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sb = smem_u32(smem);
+  auto bar = [&](int i) { return sb + L::BAR + 8 * i; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::MISC + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int N = p.N;
+  const int nT = (N + kTile - 1) / kTile, npairs = (nT + 1) / 2;
+  const int BH = p.B * p.H;
+  int bh, pair;
+  fwd_cta_coords(blockIdx.x, BH, npairs, p.causal != 0, bh, pair);
+  const int head = bh % p.H;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(L::B_Q), 1);
+    for (int s = 0; s < L::NS; ++s) {
+      mbar_init(bar(L::B_KVF + s), 1);
+      mbar_init(bar(L::B_KVE + s), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(L::B_SF + s), 1);
+      mbar_init(bar(L::B_PF + s), 128);
+    }
+    mbar_init(bar(L::B_OF), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const WaitCtl wc{abort_flag, p.err, p.wait_ns};
+
+  FwdSchedule sch;
+  sch.init(pair, nT, p.causal != 0, p.lists, head);
+
+  if (warp == 0) {
+    // ------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      prefetch_tmap(&tq);
+      prefetch_tmap(&tk);
+      prefetch_tmap(&tv);
+      const int y0 = sch.qt[0] * kTile;
+      const int y1 = (sch.act[1] ? sch.qt[1] : sch.qt[0]) * kTile;
+      mbar_arrive_expect_tx(bar(L::B_Q), 2 * L::TILE);
+#pragma unroll
+      for (int c = 0; c < L::CH; ++c) {
+        tma_load_3d(sb + L::Q + c * L::CHUNK, &tq, bar(L::B_Q), 64 * c, y0, bh);
+        tma_load_3d(sb + L::Q + L::TILE + c * L::CHUNK, &tq, bar(L::B_Q), 64 * c, y1, bh);
+      }
+      uint32_t idx = 0;
+      bool ok = true;
+      int kt, mem;
+      while (ok && sch.next(kt, mem)) {
+        for (int t = 0; t < 2; ++t) {
+          const int pos = idx % L::NS;
+          const uint32_t round = idx / L::NS;
+          if (round > 0 && !wait_bar(bar(L::B_KVE + pos), (round - 1) & 1, wc)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(bar(L::B_KVF + pos), L::TILE);
+#pragma unroll
+          for (int c = 0; c < L::CH; ++c)
+            tma_load_3d(sb + L::KV + pos * L::TILE + c * L::CHUNK, t == 0 ? &tk : &tv,
+                        bar(L::B_KVF + pos), 64 * c, kt * kTile, bh);
+          ++idx;
+        }
+      }
+      // let copies still in flight land before the CTA can exit
+      drain_bar(bar(L::B_Q), 0, p.wait_ns);
+      if (!ok) {
+        const uint32_t first = idx > static_cast<uint32_t>(L::NS) ? idx - L::NS : 0;
+        for (uint32_t j = first; j < idx; ++j)
+          drain_bar(bar(L::B_KVF + j % L::NS), (j / L::NS) & 1, p.wait_ns);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idS = idesc_bf16(128, 128, false, false);
+      constexpr uint32_t idO = idesc_bf16(128, D, false, true);
+      auto issue_s = [&](int s, int kpos) {
+        const uint32_t qa = sb + L::Q + s * L::TILE;
+        const uint32_t kb = sb + L::KV + kpos * L::TILE;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * L::CHUNK + (kk & 3) * 32;
+          mma_bf16_ss(tmem + s * 128, desc_sw128(qa + off, 16, 1024),
+                      desc_sw128(kb + off, 16, 1024), idS, kk > 0);
+        }
+      };
+      auto issue_pv = [&](int s, int vpos, bool acc) {
+        const uint32_t pa = sb + L::P + s * L::PT;
+        const uint32_t vb = sb + L::KV + vpos * L::TILE;
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk) {
+          const uint32_t aoff = (kk >> 2) * L::CHUNK + (kk & 3) * 32;
+          mma_bf16_ss(tmem + 256 + s * D, desc_sw128(pa + aoff, 16, 1024),
+                      desc_sw128(vb + kk * 2048, L::CHUNK, 1024), idO, (acc || kk > 0) ? 1u : 0u);
+        }
+      };
+      int kt, mem, kt_n = 0, mem_n = 0;
+      uint32_t idx = 0;
+      int cnt[2] = {0, 0};
+      bool ok = wait_bar(bar(L::B_Q), 0, wc);
+      bool have = sch.next(kt, mem);
+      if (ok && have) {
+        const int kpos = idx % L::NS;
+        ok = wait_bar(bar(L::B_KVF + kpos), (idx / L::NS) & 1, wc);
+        if (ok) {
+          tc_fence_after();
+          for (int s = 0; s < 2; ++s)
+            if (mem & (1 << s)) {
+              issue_s(s, kpos);
+              mma_commit(bar(L::B_SF + s));
+            }
+          mma_commit(bar(L::B_KVE + kpos));
+          ++idx;
+        }
+      }
+      while (ok && have) {
+        const bool have_n = sch.next(kt_n, mem_n);
+        const int vpos = idx % L::NS;
+        ok = wait_bar(bar(L::B_KVF + vpos), (idx / L::NS) & 1, wc);
+        ++idx;
+        if (!ok) break;
+        tc_fence_after();
+        int kpos = -1;
+        for (int s = 0; s < 2 && ok; ++s) {
+          if (mem & (1 << s)) {
+            ok = wait_bar(bar(L::B_PF + s), cnt[s] & 1, wc);
+            if (!ok) break;
+            tc_fence_after();
+            issue_pv(s, vpos, cnt[s] > 0);
+            ++cnt[s];
+          }
+          if (have_n && (mem_n & (1 << s))) {
+            if (kpos < 0) {
+              kpos = idx % L::NS;
+              ok = wait_bar(bar(L::B_KVF + kpos), (idx / L::NS) & 1, wc);
+              if (!ok) break;
+              tc_fence_after();
+            }
+            issue_s(s, kpos);
+            mma_commit(bar(L::B_SF + s));
+          }
+        }
+        if (!ok) break;
+        mma_commit(bar(L::B_KVE + vpos));
+        if (kpos >= 0) {
+          mma_commit(bar(L::B_KVE + kpos));
+          ++idx;
+        }
+        kt = kt_n;
+        mem = mem_n;
+        have = have_n;
+      }
+      // every MMA issued above completes before o_full fires
+      mma_commit(bar(L::B_OF));
+      drain_bar(bar(L::B_OF), 0, p.wait_ns);
+    }
+  } else {
+    // ------------------------------------------------------ softmax warps
+    const int s = (warp - 2) >> 2;
+    const int q4 = warp & 3;  // TMEM lane quarter this warp may access
+    const int r = q4 * 32 + lane;
+    const int qt = sch.qt[s];
+    const bool active = sch.act[s];
+    const int qrow = qt * kTile + r;
+    const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
+    const uint32_t tS = tmem + lane_off + s * 128;
+    const uint32_t tO = tmem + lane_off + 256 + s * D;
+    const uint32_t pbuf = sb + L::P + s * L::PT;
+    const float sl2 = p.scale * kLog2e;
+    float m = -INFINITY, l = 0.f;
+    int cnt = 0;
+    bool ok = true;
+    int kt, mem;
+    while (ok && sch.next(kt, mem)) {
+      if (!(mem & (1 << s))) continue;
+      ok = __all_sync(0xffffffffu, wait_bar(bar(L::B_SF + s), cnt & 1, wc));
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t sr[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32 * c, sr[c]);
+      tmem_ld_wait();
+#pragma unroll
+      for (int c = 0; c < 4; ++c) reg_fence(sr[c]);
+      const int kbase = kt * kTile;
+      const bool need_mask = (kbase + kTile > N) || (p.causal && kbase + kTile - 1 > qt * kTile);
+      if (need_mask) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int key = kbase + 32 * c + j;
+            if (key >= N || (p.causal && key > qrow)) sr[c][j] = __float_as_uint(-INFINITY);
+          }
+      }
+      float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        mx0 = fmaxf(mx0, __uint_as_float(sr[0][j]));
+        mx1 = fmaxf(mx1, __uint_as_float(sr[1][j]));
+        mx2 = fmaxf(mx2, __uint_as_float(sr[2][j]));
+        mx3 = fmaxf(mx3, __uint_as_float(sr[3][j]));
+      }
+      const float m_new = fmaxf(m, fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2);
+      const bool resc = m_new > m + kRescaleLog2;
+      const float alpha = resc ? ex2(m - m_new) : 1.f;
+      if (resc) {
+        l *= alpha;
+        m = m_new;
+      }
+      if (cnt > 0 && __any_sync(0xffffffffu, resc)) {
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tO + 32 * c, o);
+          tmem_ld_wait();
+          reg_fence(o);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
+          tmem_st32(tO + 32 * c, o);
+        }
+        tmem_st_wait();
+      }
+      const float mu = (m == -INFINITY) ? 0.f : m;
+      float ls0 = 0.f, ls1 = 0.f;
+#pragma unroll
+      for (int cc = 0; cc < 16; ++cc) {
+        float e[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          e[j] = ex2(fmaf(__uint_as_float(sr[cc >> 2][(cc & 3) * 8 + j]), sl2, -mu));
+        const uint32_t w0 = pack_bf16(e[0], e[1]), w1 = pack_bf16(e[2], e[3]);
+        const uint32_t w2 = pack_bf16(e[4], e[5]), w3 = pack_bf16(e[6], e[7]);
+        // l sums the same bf16-rounded weights the PV MMA consumes, so a
+        // dominant key's rounding cancels in O / l
+        ls0 += (bf16_lo(w0) + bf16_hi(w0)) + (bf16_lo(w1) + bf16_hi(w1));
+        ls1 += (bf16_lo(w2) + bf16_hi(w2)) + (bf16_lo(w3) + bf16_hi(w3));
+        st_shared_v4(pbuf + (cc >> 3) * L::CHUNK + sw128_offset(r, cc & 7), w0, w1, w2, w3);
+      }
+      l += ls0 + ls1;
+      fence_async_smem();
+      tc_fence_before();
+      mbar_arrive(bar(L::B_PF + s));
+      ++cnt;
+    }
+    // ---------------------------------------------------- epilogue
+    if (ok) ok = __all_sync(0xffffffffu, wait_bar(bar(L::B_OF), 0, wc));
+    tc_fence_after();
+    if (ok && active) {
+      uint8_t* orow = static_cast<uint8_t*>(p.o) +
+                      (static_cast<size_t>(bh) * N + qrow) * static_cast<size_t>(D) * 2;
+      const bool store = qrow < N;
+      const bool has = cnt > 0 && l > 0.f;
+      const float inv = has ? 1.f / l : 0.f;
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        if (cnt > 0) {
+          tmem_ld32(tO + 32 * c, o);
+          tmem_ld_wait();
+          reg_fence(o);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) o[j] = 0u;
+        }
+        if (store) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + c * 64);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            uint4 w;
+            w.x = pack_bf16(__uint_as_float(o[8 * v + 0]) * inv, __uint_as_float(o[8 * v + 1]) * inv);
+            w.y = pack_bf16(__uint_as_float(o[8 * v + 2]) * inv, __uint_as_float(o[8 * v + 3]) * inv);
+            w.z = pack_bf16(__uint_as_float(o[8 * v + 4]) * inv, __uint_as_float(o[8 * v + 5]) * inv);
+            w.w = pack_bf16(__uint_as_float(o[8 * v + 6]) * inv, __uint_as_float(o[8 * v + 7]) * inv);
+            dst[v] = w;
+          }
+        }
+      }
+      if (store) p.lse[static_cast<size_t>(bh) * N + qrow] = has ? (m + lg2(l)) * kLn2 : -INFINITY;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D>
+cudaError_t launch_fwd_d(const FwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
+                         const CUtensorMap& tv, cudaStream_t stream) {
+  using L = FwdSmem<D>;
+  cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<D>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
+  if (e != cudaSuccess) return e;
+  const int nT = (p.N + kTile - 1) / kTile, npairs = (nT + 1) / 2;
+  const long long ctas = static_cast<long long>(npairs) * p.B * p.H;
+  fa_fwd_kernel<D><<<static_cast<unsigned>(ctas), kFwdThreads, L::ALLOC, stream>>>(tq, tk, tv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_forward(const FwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
+                           const CUtensorMap& tv, cudaStream_t stream) {
+  if (p.d == 64) return launch_fwd_d<64>(p, tq, tk, tv, stream);
+  if (p.d == 128) return launch_fwd_d<128>(p, tq, tk, tv, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace fa

@@ -1,0 +1,75 @@
+// Declarations shared by the library's translation units (host side).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime_api.h>
+#include <stdint.h>
+
+namespace fa {
+
+constexpr int kTile = 128;  // query rows and keys per tile (Br = Bc = 128)
+
+// Block-sparse tile lists for one mask head layout:
+//   csr: row_ptr [mask_heads][nT+1] (head-local offsets),
+//        col_idx [mask_heads][nT*nT] (ascending key tiles of each query tile)
+//   csc: col_ptr / row_idx, the same for each key tile (ascending query tiles)
+struct TileLists {
+  const int* row_ptr = nullptr;
+  const int* col_idx = nullptr;
+  const int* col_ptr = nullptr;
+  const int* row_idx = nullptr;
+  int mask_heads = 0;
+  int nT = 0;
+};
+
+struct FwdParams {
+  void* o = nullptr;      // bf16 [BH, N, d]
+  float* lse = nullptr;   // fp32 [BH, N]
+  int B = 0, H = 0, N = 0, d = 0;
+  float scale = 0.f;
+  int causal = 0;
+  TileLists lists;        // sparse when lists.row_ptr != nullptr
+  int* err = nullptr;     // device status word
+  uint64_t wait_ns = 0;
+};
+
+struct BwdParams {
+  const float* lse = nullptr;   // fp32 [BH, N]
+  const float* delta = nullptr; // fp32 [BH, N]  D_i = <dO_i, O_i>
+  float* dq_acc = nullptr;      // fp32 [BH, N, d] (unscaled sum of dS K)
+  void* dk = nullptr;           // bf16 [BH, N, d]
+  void* dv = nullptr;           // bf16 [BH, N, d]
+  int B = 0, H = 0, N = 0, d = 0;
+  float scale = 0.f;
+  int causal = 0;
+  TileLists lists;              // sparse when lists.col_ptr != nullptr
+  int* err = nullptr;
+  uint64_t wait_ns = 0;
+};
+
+// 3-D bf16 view {d, N, B*H} of a [B, H, N, d] tensor, 128-row x 64-column
+// boxes with 128-byte swizzle.
+bool make_tile_map(CUtensorMap* map, const void* base, int BH, int N, int d);
+
+cudaError_t launch_forward(const FwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
+                           const CUtensorMap& tv, cudaStream_t stream);
+cudaError_t launch_backward_main(const BwdParams& p, const CUtensorMap& tq,
+                                 const CUtensorMap& tk, const CUtensorMap& tv,
+                                 const CUtensorMap& tdo, cudaStream_t stream);
+cudaError_t launch_bwd_preprocess(const void* o, const void* dO, float* delta, float* dq_acc,
+                                  long long rows, int d, cudaStream_t stream);
+cudaError_t launch_dq_convert(const float* dq_acc, void* dq, long long n, float scale,
+                              cudaStream_t stream);
+cudaError_t launch_build_lists(const uint8_t* mask, int mask_heads, int nT, int* row_ptr,
+                               int* col_idx, int* col_ptr, int* row_idx, cudaStream_t stream);
+// schedule export (tests): per query tile the key tiles the forward visits
+// and per key tile the query tiles the backward visits
+cudaError_t launch_schedule_export(int N, int causal, const TileLists& lists, int heads,
+                                   int* fwd_counts, int* bwd_counts, int* fwd_lists,
+                                   int* bwd_lists, cudaStream_t stream);
+cudaError_t launch_mma_probe(const CUtensorMap& ta, const CUtensorMap& tb, const void* a_raw,
+                             float* c, int mode, int n, int* err, uint64_t wait_ns,
+                             cudaStream_t stream);
+cudaError_t launch_wait_probe(int* err, uint64_t wait_ns, cudaStream_t stream);
+
+}  // namespace fa

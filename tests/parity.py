@@ -1,0 +1,67 @@
+"""Shared helpers for the GPU parity tests: run the CUDA path through the
+C ABI and the fp64 oracle on the same seeded bf16 inputs, and compare.
+
+Tolerances (bf16 inputs, fp32 accumulation; written once here):
+  O      max |diff| <= 2e-2 and mean |diff| <= 2e-3
+  lse    max |diff| <= 1e-2
+  dQ, dK, dV   max |diff| / max |ref| <= 5e-2 per tensor
+"""
+from __future__ import annotations
+
+import numpy as np
+
+import oracle
+
+O_MAX, O_MEAN, LSE_MAX, GRAD_REL = 2e-2, 2e-3, 1e-2, 5e-2
+
+
+def f64(t):
+    return t.detach().float().cpu().double().numpy()
+
+
+def check_forward(o_gpu, lse_gpu, o_ref, lse_ref, what=""):
+    o = f64(o_gpu)
+    lse = lse_gpu.detach().cpu().double().numpy()
+    assert np.all(np.isfinite(o)), f"{what}: non-finite O"
+    err = np.abs(o - o_ref)
+    assert err.max() <= O_MAX, f"{what}: O max err {err.max():.3e}"
+    assert err.mean() <= O_MEAN, f"{what}: O mean err {err.mean():.3e}"
+    fin = np.isfinite(lse_ref)
+    assert np.array_equal(np.isfinite(lse), fin), f"{what}: lse finiteness differs"
+    if fin.any():
+        le = np.abs(lse[fin] - lse_ref[fin]).max()
+        assert le <= LSE_MAX, f"{what}: lse max err {le:.3e}"
+    return float(err.max()), float(err.mean())
+
+
+def check_grad(g_gpu, g_ref, name, what=""):
+    g = f64(g_gpu) if not isinstance(g_gpu, np.ndarray) else g_gpu
+    assert np.all(np.isfinite(g)), f"{what}: non-finite {name}"
+    scale = max(np.abs(g_ref).max(), 1e-30)
+    rel = np.abs(g - g_ref).max() / scale
+    assert rel <= GRAD_REL, f"{what}: {name} rel err {rel:.3e}"
+    return float(rel)
+
+
+def oracle_forward(q, k, v, scale, causal=False, mask=None, rows=None):
+    return oracle.forward(f64(q), f64(k), f64(v), scale, causal=causal, block_mask=mask,
+                          rows=rows)
+
+
+def oracle_backward(q, k, v, do, scale, causal=False, mask=None, qrows=None, krows=None,
+                    heads=None):
+    """Oracle gradients; `heads` restricts the evaluation to a list of
+    (b, h) pairs (returns arrays over those heads only)."""
+    qa, ka, va, da = f64(q), f64(k), f64(v), f64(do)
+    if heads is None:
+        return oracle.backward(qa, ka, va, da, scale, causal=causal, block_mask=mask,
+                               qrows=qrows, krows=krows)
+    outs = []
+    for (b, h) in heads:
+        sl = (slice(b, b + 1), slice(h, h + 1))
+        m = None
+        if mask is not None:
+            m = mask if mask.shape[0] == 1 else mask[h:h + 1]
+        outs.append(oracle.backward(qa[sl], ka[sl], va[sl], da[sl], scale, causal=causal,
+                                    block_mask=m, qrows=qrows, krows=krows))
+    return tuple(np.concatenate([o[i] for o in outs], axis=1) for i in range(3))

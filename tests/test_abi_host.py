@@ -1,0 +1,120 @@
+"""Host-side checks of the C ABI (no GPU needed): the library builds and
+loads, exports every entry point include/fa.h declares, sizes its
+workspaces as documented, and rejects bad arguments before launching
+anything (every case below returns before the first CUDA call)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import io_aware_exact_15_gb300 as fa
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "fa.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_library_exports_every_declared_symbol():
+    lib = fa.load()
+    names = _declared()
+    assert "fa_forward" in names and "fa_backward" in names and "fa_blocksparse_forward" in names
+    for n in names:
+        assert hasattr(lib, n), n
+    assert sorted(fa.EXPORTS) == names
+
+
+def test_status_strings():
+    for s in range(7):
+        assert fa.fa_status_string(s)
+    assert fa.fa_status_string(99) == "unknown status"
+
+
+def test_workspace_sizes():
+    B, H, N, d = 2, 3, 300, 64
+    rows = B * H * N
+    a256 = lambda x: (x + 255) // 256 * 256
+    assert fa.fa_backward_workspace_size(B, H, N, d) == a256(4 * rows) + a256(4 * rows * d)
+    nT = (N + 127) // 128
+    lists = a256(4 * 1 * (2 * (nT + 1) + 2 * nT * nT))
+    assert fa.fa_blocksparse_workspace_size(B, H, N, d, 1) == lists + \
+        fa.fa_backward_workspace_size(B, H, N, d)
+    assert fa.fa_backward_workspace_size(0, 1, 1, 64) == 0
+    # Theorem 1: extra memory linear in N (no N^2 term outside the tile lists)
+    w1 = fa.fa_backward_workspace_size(1, 1, 4096, 128)
+    w2 = fa.fa_backward_workspace_size(1, 1, 8192, 128)
+    assert abs(w2 - 2 * w1) <= 512
+
+
+ALIGNED = 1 << 20          # fake, never dereferenced: every case fails validation first
+MIS = ALIGNED + 8
+
+
+@pytest.mark.parametrize("B,H,N,d,scale,expect", [
+    (0, 1, 128, 64, 0.125, fa.FA_ERR_INVALID_ARG),
+    (1, 0, 128, 64, 0.125, fa.FA_ERR_INVALID_ARG),
+    (1, 1, 0, 64, 0.125, fa.FA_ERR_INVALID_ARG),
+    (1, 1, 128, 64, 0.0, fa.FA_ERR_INVALID_ARG),
+    (1, 1, 128, 64, -1.0, fa.FA_ERR_INVALID_ARG),
+    (1, 1, 128, 64, float("inf"), fa.FA_ERR_INVALID_ARG),
+    (1, 1, 128, 64, float("nan"), fa.FA_ERR_INVALID_ARG),
+    (1, 1, 128, 96, 0.125, fa.FA_ERR_UNSUPPORTED),
+    (1, 1, 128, 256, 0.125, fa.FA_ERR_UNSUPPORTED),
+    (1024, 1024, 4096, 128, 0.125, fa.FA_ERR_UNSUPPORTED),
+])
+def test_forward_rejects_bad_shapes(B, H, N, d, scale, expect):
+    assert fa.fa_forward(ALIGNED, ALIGNED, ALIGNED, ALIGNED, ALIGNED, B, H, N, d, scale, 0, 0) \
+        == expect
+
+
+def test_forward_rejects_null_and_misaligned():
+    A = ALIGNED
+    assert fa.fa_forward(None, A, A, A, A, 1, 1, 128, 64, 0.1, 0, 0) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_forward(A, A, A, A, None, 1, 1, 128, 64, 0.1, 0, 0) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_forward(MIS, A, A, A, A, 1, 1, 128, 64, 0.1, 0, 0) == fa.FA_ERR_MISALIGNED
+    assert fa.fa_forward(A, A, MIS, A, A, 1, 1, 128, 64, 0.1, 0, 0) == fa.FA_ERR_MISALIGNED
+    assert fa.fa_forward(A, A, A, MIS, A, 1, 1, 128, 64, 0.1, 0, 0) == fa.FA_ERR_MISALIGNED
+    assert fa.fa_forward(A, A, A, A, A + 2, 1, 1, 128, 64, 0.1, 0, 0) == fa.FA_ERR_MISALIGNED
+
+
+def test_backward_rejects_bad_workspace():
+    A = ALIGNED
+    need = fa.fa_backward_workspace_size(1, 1, 128, 64)
+    args = (A, A, A, A, A, A, A, A, A, 1, 1, 128, 64, 0.1, 0)
+    assert fa.fa_backward(*args, A, need - 1, 0) == fa.FA_ERR_WORKSPACE
+    assert fa.fa_backward(*args, None, need, 0) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_backward(*args, A + 16, need, 0) == fa.FA_ERR_MISALIGNED
+    assert fa.fa_backward(A, A, A, A, A, A, MIS, A, A, 1, 1, 128, 64, 0.1, 0, A, need, 0) \
+        == fa.FA_ERR_MISALIGNED
+
+
+def test_blocksparse_rejects_bad_mask_args():
+    A = ALIGNED
+    ws = fa.fa_blocksparse_workspace_size(1, 4, 256, 64, 1)
+    base = (A, A, A, A, A, 1, 4, 256, 64, 0.1, 0)
+    assert fa.fa_blocksparse_forward(*base, None, 1, A, ws, 0) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_blocksparse_forward(*base, A, 2, A, ws, 0) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_blocksparse_forward(*base, A, 1, A, 0, 0) == fa.FA_ERR_WORKSPACE
+    assert fa.fa_blocksparse_build_lists(A, 1, 256, A, 0, 0) == fa.FA_ERR_WORKSPACE
+    assert fa.fa_blocksparse_build_lists(None, 1, 256, A, 1 << 20, 0) == fa.FA_ERR_INVALID_ARG
+
+
+def test_debug_entry_points_validate():
+    assert fa.fa_debug_wait_timeout(0, 0) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_debug_mma_probe(ALIGNED, ALIGNED, ALIGNED, 3, 64, 0) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_debug_mma_probe(ALIGNED, ALIGNED, ALIGNED, 1, 96, 0) == fa.FA_ERR_UNSUPPORTED
+    assert fa.fa_set_wait_limit_ns(0) == fa.FA_OK
+
+
+def test_product_package_does_not_reference_oracle():
+    pkg = os.path.join(ROOT, "io_aware_exact_15_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "import oracle" not in text and "from oracle" not in text, f
+                assert "liboracle" not in text and "fa_oracle" not in text, f

@@ -1,0 +1,83 @@
+"""Backward parity: dQ, dK, dV of sum(O * dO) vs the fp64 oracle."""
+import numpy as np
+import pytest
+
+from gpu_common import device, status_ok, torch
+import parity
+
+import fa_workloads as W
+import io_aware_exact_15_gb300 as fa
+
+pytestmark = pytest.mark.gpu
+
+
+def run_fwd_bwd(q, k, v, do, scale, causal, dev):
+    B, H, N, d = q.shape
+    qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
+    o = torch.empty_like(qd)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    assert fa.fa_forward(qd, kd, vd, o, lse, B, H, N, d, scale, causal) == fa.FA_OK
+    dq, dk, dv = (torch.full_like(qd, float("nan")) for _ in range(3))
+    nbytes = fa.fa_backward_workspace_size(B, H, N, d)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    ws.fill_(0xFF)  # contents on entry must not matter
+    assert fa.fa_backward(qd, kd, vd, o, dod, lse, dq, dk, dv, B, H, N, d, scale, causal, ws,
+                          nbytes) == fa.FA_OK
+    status_ok()
+    return o.cpu(), lse.cpu(), dq.cpu(), dk.cpu(), dv.cpu()
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("N", [1, 7, 100, 128, 129, 255, 300, 513])
+def test_backward_small_full(N, d, causal):
+    dev = device()
+    q, k, v, do = W.make_qkv(2, 2, N, d, seed=N * 11 + d + causal)
+    scale = 1.0 / d ** 0.5
+    o, lse, dq, dk, dv = run_fwd_bwd(q, k, v, do, scale, causal, dev)
+    what = f"N={N} d={d} causal={causal}"
+    o_ref, lse_ref = parity.oracle_forward(q, k, v, scale, causal)
+    parity.check_forward(o, lse, o_ref, lse_ref, what)
+    dq_r, dk_r, dv_r = parity.oracle_backward(q, k, v, do, scale, causal)
+    parity.check_grad(dq, dq_r, "dQ", what)
+    parity.check_grad(dk, dk_r, "dK", what)
+    parity.check_grad(dv, dv_r, "dV", what)
+
+
+def test_backward_is_repeatable_to_tolerance():
+    # dQ is summed with fp32 atomics: two runs agree to rounding, not bits
+    dev = device()
+    q, k, v, do = W.make_qkv(1, 2, 640, 64, seed=3)
+    a = run_fwd_bwd(q, k, v, do, 0.125, True, dev)
+    b = run_fwd_bwd(q, k, v, do, 0.125, True, dev)
+    assert torch.equal(a[3], b[3]) and torch.equal(a[4], b[4])  # dK, dV: no atomics
+    assert (a[2].float() - b[2].float()).abs().max().item() < 1e-2
+
+
+@pytest.mark.parametrize("name", ["bert_large", "gpt2_causal"])
+def test_backward_named_workload_full(name):
+    dev = device()
+    w = W.WORKLOADS[name]
+    q, k, v, do, _ = W.make_inputs(w)
+    o, lse, dq, dk, dv = run_fwd_bwd(q, k, v, do, w.scale, w.causal, dev)
+    dq_r, dk_r, dv_r = parity.oracle_backward(q, k, v, do, w.scale, w.causal)
+    parity.check_grad(dq, dq_r, "dQ", name)
+    parity.check_grad(dk, dk_r, "dK", name)
+    parity.check_grad(dv, dv_r, "dV", name)
+
+
+@pytest.mark.parametrize("name", ["longseq_causal_n2048_d128", "longseq_causal_n16384_d64",
+                                  "longseq_dense_n4096_d128"])
+def test_backward_long_sequences_sampled_rows(name):
+    dev = device()
+    w = W.WORKLOADS[name]
+    q, k, v, do, _ = W.make_inputs(w)
+    o, lse, dq, dk, dv = run_fwd_bwd(q, k, v, do, w.scale, w.causal, dev)
+    rows = W.sample_rows(w.N, 256, seed=w.seed + 23)
+    heads = [(0, 0), (w.B - 1, w.H - 1)]  # two heads keep the oracle's cost bounded
+    dq_r, dk_r, dv_r = parity.oracle_backward(q, k, v, do, w.scale, w.causal, qrows=rows,
+                                              krows=rows, heads=heads)
+    sel = lambda t: torch.stack([t[b, h] for (b, h) in heads])[None][:, :, rows]
+    parity.check_grad(sel(dq), dq_r, "dQ", name)
+    parity.check_grad(sel(dk), dk_r, "dK", name)
+    parity.check_grad(sel(dv), dv_r, "dV", name)

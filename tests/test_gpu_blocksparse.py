@@ -1,0 +1,168 @@
+"""Block-sparse parity and the bit-exact integer work (tile lists, schedules)."""
+import numpy as np
+import pytest
+
+from gpu_common import device, status_ok, torch
+import parity
+
+import fa_workloads as W
+import io_aware_exact_15_gb300 as fa
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+
+def run_sparse(q, k, v, do, scale, causal, mask, dev):
+    B, H, N, d = q.shape
+    mh = mask.shape[0]
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    md = torch.from_numpy(np.ascontiguousarray(mask)).to(dev)
+    o = torch.full_like(qd, float("nan"))
+    lse = torch.full((B, H, N), float("nan"), dtype=torch.float32, device=dev)
+    nbytes = fa.fa_blocksparse_workspace_size(B, H, N, d, mh)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    assert fa.fa_blocksparse_forward(qd, kd, vd, o, lse, B, H, N, d, scale, causal, md, mh, ws,
+                                     nbytes) == fa.FA_OK
+    out = [o, lse]
+    if do is not None:
+        dod = do.to(dev)
+        dq, dk, dv = (torch.full_like(qd, float("nan")) for _ in range(3))
+        assert fa.fa_blocksparse_backward(qd, kd, vd, o, dod, lse, dq, dk, dv, B, H, N, d, scale,
+                                          causal, md, mh, ws, nbytes) == fa.FA_OK
+        out += [dq, dk, dv]
+    status_ok()
+    return [t.cpu() for t in out]
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("N,mh", [(300, 1), (640, 2), (1000, 1)])
+def test_blocksparse_small_full(N, mh, d, causal):
+    dev = device()
+    B, H = 1, 2
+    nT = (N + 127) // 128
+    q, k, v, do = W.make_qkv(B, H, N, d, seed=N + d + causal)
+    mask = W.random_block_mask(mh, nT, seed=N + 1, density=0.45)
+    mask[0, 1, :] = 0  # a query tile with no kept key tile
+    mask[-1, :, 0] = 1
+    scale = 1.0 / d ** 0.5
+    o, lse, dq, dk, dv = run_sparse(q, k, v, do, scale, causal, mask, dev)
+    what = f"N={N} mh={mh} d={d} causal={causal}"
+    o_ref, lse_ref = parity.oracle_forward(q, k, v, scale, causal, mask=mask)
+    parity.check_forward(o, lse, o_ref, lse_ref, what)
+    dq_r, dk_r, dv_r = parity.oracle_backward(q, k, v, do, scale, causal, mask=mask)
+    parity.check_grad(dq, dq_r, "dQ", what)
+    parity.check_grad(dk, dk_r, "dK", what)
+    parity.check_grad(dv, dv_r, "dV", what)
+
+
+def test_blocksparse_all_ones_equals_dense():
+    dev = device()
+    q, k, v, _ = W.make_qkv(1, 2, 384, 64, seed=9, with_do=False)
+    mask = np.ones((1, 3, 3), dtype=np.uint8)
+    o_s, lse_s = run_sparse(q, k, v, None, 0.125, False, mask, dev)
+    o_d = torch.empty_like(q.to(dev))
+    lse_d = torch.empty((1, 2, 384), dtype=torch.float32, device=dev)
+    assert fa.fa_forward(q.to(dev), k.to(dev), v.to(dev), o_d, lse_d, 1, 2, 384, 64, 0.125,
+                         0) == fa.FA_OK
+    status_ok()
+    assert torch.equal(o_s, o_d.cpu()) and torch.equal(lse_s, lse_d.cpu())
+
+
+def test_blocksparse_64k_sampled_rows():
+    dev = device()
+    w = W.WORKLOADS["blocksparse_64k"]
+    q, k, v, do, mask = W.make_inputs(w)
+    o, lse, dq, dk, dv = run_sparse(q, k, v, do, w.scale, w.causal, mask, dev)
+    rows = W.sample_rows(w.N, 256, seed=w.seed + 29)
+    o_ref, lse_ref = parity.oracle_forward(q, k, v, w.scale, w.causal, mask=mask, rows=rows)
+    parity.check_forward(o[:, :, rows], lse[:, :, rows], o_ref, lse_ref, "blocksparse_64k")
+    heads = [(0, 0), (0, w.H - 1)]
+    dq_r, dk_r, dv_r = parity.oracle_backward(q, k, v, do, w.scale, w.causal, mask=mask,
+                                              qrows=rows, krows=rows, heads=heads)
+    sel = lambda t: torch.stack([t[b, h] for (b, h) in heads])[None][:, :, rows]
+    parity.check_grad(sel(dq), dq_r, "dQ", "blocksparse_64k")
+    parity.check_grad(sel(dk), dk_r, "dK", "blocksparse_64k")
+    parity.check_grad(sel(dv), dv_r, "dV", "blocksparse_64k")
+
+
+# ---------------------------------------------------------------- integer work
+
+def _lists_on_gpu(mask, N, dev):
+    mh, nT, _ = mask.shape
+    nbytes = fa.fa_blocksparse_workspace_size(1, mh, N, 64, mh)
+    ws = torch.full((nbytes,), 0x7F, dtype=torch.uint8, device=dev)
+    md = torch.from_numpy(np.ascontiguousarray(mask)).to(dev)
+    assert fa.fa_blocksparse_build_lists(md, mh, N, ws, nbytes) == fa.FA_OK
+    status_ok()
+    words = ws.view(torch.int32).cpu().numpy()
+    rp = words[:mh * (nT + 1)].reshape(mh, nT + 1)
+    cp = words[mh * (nT + 1):2 * mh * (nT + 1)].reshape(mh, nT + 1)
+    base = 2 * mh * (nT + 1)
+    ci = words[base:base + mh * nT * nT].reshape(mh, nT * nT)
+    ri = words[base + mh * nT * nT:base + 2 * mh * nT * nT].reshape(mh, nT * nT)
+    return rp, ci, cp, ri
+
+
+@pytest.mark.parametrize("N,mh,density", [(128, 1, 1.0), (1000, 2, 0.3), (65536, 1, None)])
+def test_tile_lists_bit_exact(N, mh, density):
+    dev = device()
+    nT = (N + 127) // 128
+    if density is None:
+        mask = W.band_random_block_mask(N, seed=2005, density=0.05)
+    else:
+        mask = W.random_block_mask(mh, nT, seed=N, density=density)
+    rp, ci, cp, ri = _lists_on_gpu(mask, N, dev)
+    rp_o, ci_o, cp_o, ri_o = oracle.mask_lists(mask)
+    assert np.array_equal(rp, rp_o) and np.array_equal(cp, cp_o)
+    for h in range(mask.shape[0]):
+        assert np.array_equal(ci[h, :rp[h, -1]], ci_o[h])
+        assert np.array_equal(ri[h, :cp[h, -1]], ri_o[h])
+
+
+def _schedule(N, causal, mask, dev):
+    nT = (N + 127) // 128
+    heads = 1 if mask is None else mask.shape[0]
+    fc = torch.full((heads, nT), -1, dtype=torch.int32, device=dev)
+    bc = torch.full((heads, nT), -1, dtype=torch.int32, device=dev)
+    fl = torch.full((heads, nT, nT), -1, dtype=torch.int32, device=dev)
+    bl = torch.full((heads, nT, nT), -1, dtype=torch.int32, device=dev)
+    md, ws, nbytes = None, None, 0
+    if mask is not None:
+        md = torch.from_numpy(np.ascontiguousarray(mask)).to(dev)
+        nbytes = fa.fa_blocksparse_workspace_size(1, heads, N, 64, heads)
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    assert fa.fa_debug_schedule(N, causal, md, heads, ws, nbytes, fc, bc, fl, bl) == fa.FA_OK
+    status_ok()
+    return fc.cpu().numpy(), bc.cpu().numpy(), fl.cpu().numpy(), bl.cpu().numpy()
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N,mask_kind", [(1, None), (1024, None), (16384, None), (1000, "rand"),
+                                         (65536, "band")])
+def test_schedules_bit_exact(N, mask_kind, causal):
+    dev = device()
+    nT = (N + 127) // 128
+    mask = None
+    if mask_kind == "rand":
+        mask = W.random_block_mask(2, nT, seed=11, density=0.4)
+    elif mask_kind == "band":
+        mask = W.band_random_block_mask(N, seed=2005, density=0.05)
+    fc, bc, fl, bl = _schedule(N, causal, mask, dev)
+    counts = oracle.tile_counts(N, 128, causal, mask)
+    assert np.array_equal(fc, counts)  # forward: tiles holding an allowed element
+    if mask is None and causal:
+        assert int(fc.sum()) == nT * (nT + 1) // 2
+    heads = fc.shape[0]
+    if mask is not None:
+        rp, ci, cp, ri = oracle.mask_lists(mask)
+    for h in range(heads):
+        for a in range(nT):
+            if mask is None:
+                fexp = list(range(a + 1)) if causal else list(range(nT))
+                bexp = list(range(a, nT)) if causal else list(range(nT))
+            else:
+                fexp = [int(x) for x in ci[h][rp[h, a]:rp[h, a + 1]] if not causal or x <= a]
+                bexp = [int(x) for x in ri[h][cp[h, a]:cp[h, a + 1]] if not causal or x >= a]
+            assert fl[h, a, :fc[h, a]].tolist() == fexp
+            assert bc[h, a] == len(bexp) and bl[h, a, :bc[h, a]].tolist() == bexp
