@@ -1,0 +1,448 @@
+"""Benchmark: attention TFLOP/s (forward + backward) on one GB300.
+
+One step = the whole hot path over one batch: fa_forward (tile schedule,
+TMA loads, S = QK^T, mask, online softmax, O += PV, epilogue) then the
+backward (preprocess, recompute kernel, dQ conversion), all through the C
+ABI.  Default workload: BERT-large-shaped self-attention, B=8 H=16 N=512
+d=64, non-causal, bf16 inputs drawn N(0,1) from a seeded generator.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py --impl reference ...   # the fp64 CPU oracle, timed
+
+Inputs of this workload (~34 MB) fit in L2, so L2 is flushed (a 256 MiB
+device write) before every timed step; the flush is outside the per-step
+CUDA events.  Under torchrun every rank runs its own replica (weak
+scaling); the reported time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attention TFLOP/s fwd and fwd+bwd (bf16, 1×GB300) and % of dense BF16 peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS, source="fallback")
+
+
+def kernel_source_hash(files):
+    h = hashlib.sha1()
+    for f in files:
+        with open(os.path.join(ROOT, "io_aware_exact_15_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:12]
+
+
+def ncu_traffic(kernel_key, src_hash):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f).get(kernel_key)
+    except (OSError, ValueError):
+        return None
+    if not rec or rec.get("source_hash") != src_hash:
+        return None
+    return rec.get("bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled while the timed loop runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index, period_ms=100):
+        self.gpu = gpu_index
+        self.period = period_ms
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", f"-lms={self.period}"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            threading.Thread(target=self._read, daemon=True).start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------- GPU arm
+def run_gpu(args, rank, world, dist):
+    import numpy as np
+    import torch
+
+    import fa_workloads as W
+    import io_aware_exact_15_gb300 as fa
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    peaks = load_peaks()
+    w = W.WORKLOADS[args.workload]
+    B, H, N, d = w.B, w.H, w.N, w.d
+    q, k, v, do, mask = W.make_inputs(w, with_do=True)
+    stream = torch.cuda.Stream(device=dev)
+    K = args.steps
+    s_ptr = stream.cuda_stream
+    sparse = mask is not None
+    mh = mask.shape[0] if sparse else 1
+    with torch.cuda.stream(stream):
+        qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
+        md = torch.from_numpy(np.ascontiguousarray(mask)).to(dev) if sparse else None
+        o = torch.empty_like(qd)
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+        dq, dk, dv = (torch.empty_like(qd) for _ in range(3))
+        nbytes = (fa.fa_blocksparse_workspace_size(B, H, N, d, mh) if sparse
+                  else fa.fa_backward_workspace_size(B, H, N, d))
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    lists_bytes = nbytes - fa.fa_backward_workspace_size(B, H, N, d) if sparse else 0
+
+    def check(st, what):
+        if st != fa.FA_OK:
+            raise RuntimeError(f"{what}: {fa.fa_status_string(st)}")
+
+    bws = ws[lists_bytes:] if sparse else ws
+    bwb = nbytes - lists_bytes
+
+    # one step; `ev` (5 events) splits it into its kernels
+    def step(ev=None):
+        rec = (lambda i: ev[i].record(stream)) if ev else (lambda i: None)
+        rec(0)
+        if sparse:
+            check(fa.fa_blocksparse_forward(qd, kd, vd, o, lse, B, H, N, d, w.scale, w.causal, md,
+                                            mh, ws, nbytes, s_ptr), "forward")
+            rec(1)
+            rec(2)
+            check(fa.fa_blocksparse_backward(qd, kd, vd, o, dod, lse, dq, dk, dv, B, H, N, d,
+                                             w.scale, w.causal, md, mh, ws, nbytes, s_ptr),
+                  "backward")
+            rec(3)
+            rec(4)
+            return
+        check(fa.fa_forward(qd, kd, vd, o, lse, B, H, N, d, w.scale, w.causal, s_ptr), "forward")
+        rec(1)
+        check(fa.fa_backward_preprocess(o, dod, B, H, N, d, bws, bwb, s_ptr), "preprocess")
+        rec(2)
+        check(fa.fa_backward_main(qd, kd, vd, dod, lse, dk, dv, B, H, N, d, w.scale, w.causal,
+                                  bws, bwb, s_ptr), "backward")
+        rec(3)
+        check(fa.fa_backward_dq_convert(dq, B, H, N, d, w.scale, bws, bwb, s_ptr), "convert")
+        rec(4)
+
+    launches_per_step = (2 + 4) if sparse else 4
+    ff = W.fwd_flops(w, mask)
+    fb = W.fwd_bwd_flops(w, mask)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    st = fa.fa_get_device_status(s_ptr)
+    if st != fa.FA_OK:
+        raise RuntimeError(f"device status after warm-up: {fa.fa_status_string(st)}")
+
+    def timed_loop(K, split):
+        """K steps, each after an L2 flush; returns per-step event lists."""
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5 if split else 2)]
+               for _ in range(K)]
+        with torch.cuda.stream(stream):
+            torch.cuda._sleep(40_000_000)  # head start so launches queue ahead of the GPU
+        for i in range(K):
+            with torch.cuda.stream(stream):
+                flush.fill_(i & 0xFF)
+            if split:
+                step(evs[i])
+            else:
+                evs[i][0].record(stream)
+                step()
+                evs[i][1].record(stream)
+        return evs
+
+    K = args.steps
+    clocks = ClockSampler(local)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    time.sleep(0.3)
+    t0 = time.perf_counter()
+    evs = timed_loop(K, split=False)
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - t0
+    if dist is not None:
+        dist.barrier()
+    clk = clocks.stop()
+    step_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    ms = statistics.fmean(step_ms)
+    # per-kernel split on a shorter loop of the same steps
+    Ks = max(10, min(K, 300))
+    sev = timed_loop(Ks, split=True)
+    torch.cuda.synchronize(dev)
+    st = fa.fa_get_device_status(s_ptr)
+    if st != fa.FA_OK:
+        raise RuntimeError(f"device status after timing: {fa.fa_status_string(st)}")
+    per = [[e[j].elapsed_time(e[j + 1]) for j in range(4)] for e in sev]
+    fwd_ms = statistics.fmean(p[0] for p in per)
+    pre_ms = statistics.fmean(p[1] for p in per)
+    main_ms = statistics.fmean(p[2] for p in per)
+    conv_ms = statistics.fmean(p[3] for p in per)
+    ms_max = ms
+    if dist is not None:
+        t = torch.tensor([ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_max = float(t.item())
+    value = world * fb / (ms_max * 1e-3) / 1e12
+
+    # end to end through the public API with host buffers (pinned)
+    hq, hk, hv, hdo = (t.pin_memory() for t in (q, k, v, do))
+    ho = torch.empty_like(q).pin_memory()
+    hl = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
+    hdq, hdk, hdv = (torch.empty_like(q).pin_memory() for _ in range(3))
+    hm = torch.from_numpy(np.ascontiguousarray(mask)).pin_memory() if sparse else None
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo))
+    d2h = sum(t.numel() * t.element_size() for t in (ho, hl, hdq, hdk, hdv))
+    if sparse:
+        h2d += hm.numel()
+
+    def e2e_step():
+        with torch.cuda.stream(stream):
+            for dst, src in ((qd, hq), (kd, hk), (vd, hv), (dod, hdo)):
+                dst.copy_(src, non_blocking=True)
+            if sparse:
+                md.copy_(hm, non_blocking=True)
+        step()
+        with torch.cuda.stream(stream):
+            for dst, src in ((ho, o), (hl, lse), (hdq, dq), (hdk, dk), (hdv, dv)):
+                dst.copy_(src, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    Ke = max(3, min(K, 200))
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(Ke):
+        e2e_step()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    ems = a.elapsed_time(b) / Ke
+    if dist is not None:
+        t = torch.tensor([ems], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ems = float(t.item())
+    e2e = {"value": round(world * fb / (ems * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+           "ms_per_step": round(ems, 4), "h2d_bytes_per_step": int(h2d),
+           "d2h_bytes_per_step": int(d2h),
+           "path": "pinned host -> device copies, forward + backward via the C ABI, "
+                   "device -> host copies of o, lse, dq, dk, dv"}
+
+    src_hash = kernel_source_hash(["fa_bwd.cu", "fa_ptx.cuh", "fa_sched.cuh"])
+    main_flops = 2.5 * ff
+    achieved = main_flops / (main_ms * 1e-3) / 1e12
+    peak = peaks["bf16_tflops"]
+    roofline = {"kernel": "fa_bwd_kernel (recompute: S, dP, dV, dK, dQ MMAs)", "bound": "tensor",
+                "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+                "frac": round(achieved / peak, 4),
+                "peak_source": f"{peaks['source']} bf16 burst",
+                "traffic": ncu_traffic(f"fa_bwd_kernel:{args.workload}", src_hash),
+                "algorithmic_flops_per_launch": main_flops,
+                "avg_launch_ms": round(main_ms, 5)}
+    fwd_tf = ff / (fwd_ms * 1e-3) / 1e12
+    result = {
+        "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_max, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16)",
+        "config": {"workload": f"{w.name}: {w.note}", "B": B, "H": H, "N": N, "d": d,
+                   "causal": w.causal, "sparse": sparse,
+                   "l2": "flushed before every timed step (256 MiB device write, outside events)",
+                   "parallelism": f"replicas x{world} (independent heads per GPU)"},
+        "fwd": {"ms": round(fwd_ms, 5), "tflops": round(fwd_tf, 2),
+                "frac_of_peak": round(fwd_tf / peak, 4)},
+        "fwd_bwd": {"ms": round(ms, 5), "tflops": round(fb / (ms * 1e-3) / 1e12, 2),
+                    "frac_of_peak": round(fb / (ms * 1e-3) / 1e12 / peak, 4)},
+        "kernels_ms": {"fa_fwd_kernel": round(fwd_ms, 5), "fa_bwd_pre_kernel": round(pre_ms, 5),
+                       "fa_bwd_kernel": round(main_ms, 5),
+                       "fa_dq_convert_kernel": round(conv_ms, 5)},
+        "roofline": roofline, "e2e": e2e, "gpu_launches": launches_per_step * K,
+        "split_steps": Ks,
+        "clocks": clk, "wall_s_timed": round(wall, 3),
+        "peaks": {k_: peaks[k_] for k_ in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained")},
+    }
+    return result
+
+
+# ---------------------------------------------------------------------------- CPU oracle
+def oracle_sample(w, heads, q, k, v, do, mask, nthreads):
+    """fp64 oracle forward + backward on the first `heads` (batch, head)
+    slices of the workload."""
+    import oracle
+    B, H, N, d = q.shape
+    f = lambda t: t.reshape(1, B * H, N, d)[:, :heads].float().double().numpy()
+    oracle.forward(f(q), f(k), f(v), w.scale, causal=w.causal, block_mask=mask,
+                   nthreads=nthreads)
+    oracle.backward(f(q), f(k), f(v), f(do), w.scale, causal=w.causal, block_mask=mask,
+                    nthreads=nthreads)
+
+
+def calibrate_heads(w, q, k, v, do, mask, nthreads, budget_s):
+    """Heads whose oracle forward + backward take about budget_s seconds."""
+    total = w.B * w.H
+    n = 1
+    while True:
+        t0 = time.perf_counter()
+        oracle_sample(w, n, q, k, v, do, mask, nthreads)
+        dt = time.perf_counter() - t0
+        if n >= total or dt >= 0.2 * budget_s:
+            break
+        n = min(total, n * 4)
+    return max(1, min(total, int(n * budget_s / max(dt, 1e-3))))
+
+
+def cpu_baseline(w, budget_s=12.0):
+    import fa_workloads as W
+    q, k, v, do, mask = W.make_inputs(w, with_do=True)
+    nthreads = os.cpu_count() or 1
+    heads = calibrate_heads(w, q, k, v, do, mask, nthreads, budget_s)
+    t0 = time.perf_counter()
+    oracle_sample(w, heads, q, k, v, do, mask, nthreads)
+    dt = time.perf_counter() - t0
+    per_head = W.fwd_bwd_flops(w, mask) / (w.B * w.H)
+    return {"value": round(per_head * heads / dt / 1e12, 9), "unit": "TFLOP/s",
+            "cores": nthreads, "kind": "oracle",
+            "sample": f"fp64 C oracle forward+backward on {heads} of {w.B * w.H} (batch, head) "
+                      f"slices of {w.name}, {dt:.2f} s wall"}
+
+
+def run_reference(args, rank, world):
+    """The reference arm: the fp64 CPU oracle timed on the host cores, on a
+    bounded sample of the same workload each step (rank 0 only)."""
+    import fa_workloads as W
+    if rank != 0:
+        return None
+    w = W.WORKLOADS[args.workload]
+    q, k, v, do, mask = W.make_inputs(w, with_do=True)
+    nthreads = os.cpu_count() or 1
+    per_step_budget = max(1.0, 150.0 / max(1, args.steps + args.warmup))
+    heads = calibrate_heads(w, q, k, v, do, mask, nthreads, per_step_budget)
+    for _ in range(args.warmup):
+        oracle_sample(w, heads, q, k, v, do, mask, nthreads)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle_sample(w, heads, q, k, v, do, mask, nthreads)
+        times.append(time.perf_counter() - t0)
+    ms = 1e3 * statistics.fmean(times)
+    per_head = W.fwd_bwd_flops(w, mask) / (w.B * w.H)
+    value = per_head * heads / (ms * 1e-3) / 1e12
+    sample = (f"fp64 C oracle forward+backward on {heads} of {w.B * w.H} heads per step "
+              f"({w.name})")
+    return {"metric": METRIC, "value": round(value, 9), "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded N(0,1) bf16, upcast to fp64)",
+            "config": {"workload": f"{w.name}: {w.note}", "B": w.B, "H": w.H, "N": w.N,
+                       "d": w.d, "causal": w.causal},
+            "impl": "reference",
+            "cpu_baseline": {"value": round(value, 9), "unit": "TFLOP/s", "cores": nthreads,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 9), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default="bert_large")
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        return
+    dist = None
+    if world > 1:
+        import torch
+        import torch.distributed as tdist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        tdist.init_process_group("nccl")
+        dist = tdist
+    # the oracle pool starts before the first GPU call (threads, no fork)
+    res = run_gpu(args, rank, world, dist)
+    if rank == 0:
+        import fa_workloads as W
+        if not args.no_cpu_baseline and world >= 1:
+            res["cpu_baseline"] = cpu_baseline(W.WORKLOADS[args.workload])
+        print(json.dumps(res), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

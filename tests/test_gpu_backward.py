@@ -44,6 +44,16 @@ def test_backward_small_full(N, d, causal):
     parity.check_grad(dv, dv_r, "dV", what)
 
 
+def test_backward_single_key_closed_form():
+    # N = 1: O = V, dV = dO and dQ = dK = 0 exactly
+    dev = device()
+    q, k, v, do = W.make_qkv(3, 2, 1, 128, seed=77)
+    o, lse, dq, dk, dv = run_fwd_bwd(q, k, v, do, 0.09, False, dev)
+    assert torch.equal(o, v)
+    assert torch.equal(dv, do)
+    assert dq.float().abs().max().item() < 1e-4 and dk.float().abs().max().item() < 1e-4
+
+
 def test_backward_is_repeatable_to_tolerance():
     # dQ is summed with fp32 atomics: two runs agree to rounding, not bits
     dev = device()
