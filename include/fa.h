@@ -108,6 +108,31 @@ fa_status fa_backward_main(const void* q, const void* k, const void* v, const vo
 fa_status fa_backward_dq_convert(void* dq, int B, int H, int N, int d, float scale,
                                  void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/*
+ * fa_backward without a workspace argument, for callers that cannot
+ * allocate device memory: a host framework that hands a plugin no workspace,
+ * or code that must not call cudaMalloc once running (it can synchronise the
+ * device and can fail under memory pressure mid-job).  The paper has no
+ * counterpart; this is a packaging variant of fa_backward, same arguments
+ * and results minus the workspace.
+ *   Scratch: one file-scope device array of 32 MiB (2^25 bytes) per GPU,
+ *            held from library load until process exit.  Problems whose
+ *            fa_backward_workspace_size(B, H, N, d) exceeds 2^25 bytes return
+ *            FA_ERR_WORKSPACE with nothing launched (d = 64: about 129k rows
+ *            B*H*N; d = 128: about 65k rows).
+ *   Sharing: every call on a device uses the same array, which keeps the last
+ *            call's contents; each call clears what must start at zero (the
+ *            dQ accumulator) itself.  Calls whose kernels overlap on the GPU
+ *            race on the array: order them on one stream.
+ *   Set-up:  the first call on each device looks up the array's device
+ *            address (cudaGetSymbolAddress, that device current) and caches
+ *            it; make that first call before any stream capture.
+ * Allocates nothing: no cudaMalloc / cudaFree, no allocating library call.
+ */
+fa_status fa_backward_noalloc(const void* q, const void* k, const void* v, const void* o,
+                              const void* dO, const float* lse, void* dq, void* dk, void* dv, int B,
+                              int H, int N, int d, float scale, int causal, cudaStream_t stream);
+
 /* Bytes of workspace the block-sparse calls need: the CSR and CSC tile
  * lists of the mask (4 * mask_heads * (2*(nT+1) + 2*nT*nT) bytes) followed
  * by the fa_backward workspace.  The forward uses only the list part. */

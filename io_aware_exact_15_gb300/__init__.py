@@ -27,7 +27,7 @@ FA_ERR_TIMEOUT = 6
 
 EXPORTS = (
     "fa_status_string", "fa_forward", "fa_backward_workspace_size", "fa_backward",
-    "fa_backward_preprocess", "fa_backward_main", "fa_backward_dq_convert",
+    "fa_backward_preprocess", "fa_backward_main", "fa_backward_dq_convert", "fa_backward_noalloc",
     "fa_blocksparse_workspace_size", "fa_blocksparse_build_lists", "fa_blocksparse_forward",
     "fa_blocksparse_backward", "fa_get_device_status", "fa_set_wait_limit_ns",
     "fa_debug_wait_timeout", "fa_debug_schedule", "fa_debug_mma_probe",
@@ -72,6 +72,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
             "fa_backward_preprocess": ([P, P, I, I, I, I, P, Z, P], I),
             "fa_backward_main": ([P, P, P, P, P, P, P, I, I, I, I, F, I, P, Z, P], I),
             "fa_backward_dq_convert": ([P, I, I, I, I, F, P, Z, P], I),
+            "fa_backward_noalloc": ([P, P, P, P, P, P, P, P, P, I, I, I, I, F, I, P], I),
             "fa_blocksparse_workspace_size": ([I, I, I, I, I], Z),
             "fa_blocksparse_build_lists": ([P, I, I, P, Z, P], I),
             "fa_blocksparse_forward": ([P, P, P, P, P, I, I, I, I, F, I, P, I, P, Z, P], I),
@@ -149,6 +150,15 @@ def fa_backward_main(q, k, v, dO, lse, dk, dv, B, H, N, d, scale, causal, worksp
 def fa_backward_dq_convert(dq, B, H, N, d, scale, workspace, workspace_bytes, stream=None) -> int:
     return load().fa_backward_dq_convert(_p(dq), B, H, N, d, float(scale), _p(workspace),
                                          int(workspace_bytes), _s(stream))
+
+
+def fa_backward_noalloc(q, k, v, o, dO, lse, dq, dk, dv, B, H, N, d, scale, causal,
+                        stream=None) -> int:
+    """fa_backward with the library's fixed 32 MiB per-device scratch array
+    instead of a caller workspace (for callers that cannot allocate)."""
+    return load().fa_backward_noalloc(_p(q), _p(k), _p(v), _p(o), _p(dO), _p(lse), _p(dq), _p(dk),
+                                      _p(dv), B, H, N, d, float(scale), int(bool(causal)),
+                                      _s(stream))
 
 
 def fa_blocksparse_workspace_size(B, H, N, d, mask_heads) -> int:
