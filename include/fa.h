@@ -202,6 +202,7 @@ fa_status fa_debug_schedule(int N, int causal, const uint8_t* block_mask, int ma
  *   mode 0: c[128x128] = a b^T, a and b bf16 [128 x 128]
  *   mode 1: c[128xn]   = a b,   a bf16 [128 x 128], b bf16 [128 x n]
  *   mode 2: c[128xn]   = a^T b, a bf16 [128 x 128], b bf16 [128 x n]
+ *   mode 3: c[128xn]   = a b,   as mode 1 with a held in tensor memory
  * n in {64, 128}; c fp32 row-major; all device pointers, 16-byte aligned.
  */
 fa_status fa_debug_mma_probe(const void* a, const void* b, float* c, int mode, int n,

@@ -201,9 +201,10 @@ fa_status backward_main_impl(const void* q, const void* k, const void* v, const 
   fa_status st = FA_OK;
   int* err = status_word(&st);
   if (!err) return st;
-  CUtensorMap tq, tk, tv, tdo;
+  CUtensorMap tq, tk, tv, tdo, tdq;
   if (!fa::make_tile_map(&tq, q, B * H, N, d) || !fa::make_tile_map(&tk, k, B * H, N, d) ||
-      !fa::make_tile_map(&tv, v, B * H, N, d) || !fa::make_tile_map(&tdo, dO, B * H, N, d))
+      !fa::make_tile_map(&tv, v, B * H, N, d) || !fa::make_tile_map(&tdo, dO, B * H, N, d) ||
+      !fa::make_acc_map(&tdq, w.dq_acc, B * H, N, d))
     return FA_ERR_CUDA;
   fa::BwdParams p;
   p.lse = lse;
@@ -220,7 +221,7 @@ fa_status backward_main_impl(const void* q, const void* k, const void* v, const 
   if (lists) p.lists = *lists;
   p.err = err;
   p.wait_ns = wait_limit_ns();
-  FA_CUDA(fa::launch_backward_main(p, tq, tk, tv, tdo, stream));
+  FA_CUDA(fa::launch_backward_main(p, tq, tk, tv, tdo, tdq, stream));
   return FA_OK;
 }
 
@@ -266,6 +267,19 @@ bool make_tile_map(CUtensorMap* map, const void* base, int BH, int N, int d) {
   const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(kTile), 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+bool make_acc_map(CUtensorMap* map, const void* base, int BH, int N, int d) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                              static_cast<cuuint64_t>(BH)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 4,
+                                 static_cast<cuuint64_t>(N) * d * 4};
+  const cuuint32_t box[3] = {32, 32, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides, box,
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -437,7 +451,7 @@ fa_status fa_debug_schedule(int N, int causal, const uint8_t* block_mask, int ma
 
 fa_status fa_debug_mma_probe(const void* a, const void* b, float* c, int mode, int n,
                              cudaStream_t stream) {
-  if (mode < 0 || mode > 2) return FA_ERR_INVALID_ARG;
+  if (mode < 0 || mode > 3) return FA_ERR_INVALID_ARG;
   if (mode == 0) n = 128;
   if (n != 64 && n != 128) return FA_ERR_UNSUPPORTED;
   FA_TRY(check_ptr16(a));

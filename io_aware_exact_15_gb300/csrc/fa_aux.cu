@@ -204,6 +204,9 @@ cudaError_t launch_schedule_export(int N, int causal, const TileLists& lists, in
 //           swizzle, B [128 x n] MN-major through TMA (the O += P V form)
 //   mode 2: C[128xn] = A^T B, A [128 x 128] and B [128 x n] both MN-major
 //           through TMA (the dV += P^T dO and dK += dS^T Q forms)
+//   mode 3: C[128xn] = A B, A [128 x 128] written by threads into TMEM (two
+//           bf16 per column), B [128 x n] MN-major through TMA (O += P V with
+//           P held in tensor memory)
 __global__ void __launch_bounds__(128, 1)
     fa_mma_probe_kernel(const __grid_constant__ CUtensorMap ta,
                         const __grid_constant__ CUtensorMap tb, const uint16_t* a_raw, float* c,
@@ -224,7 +227,7 @@ __global__ void __launch_bounds__(128, 1)
     fence_mbar_init();
   }
   if (warp == 0) {
-    tmem_alloc(smem_u32(tmem_slot), 128);
+    tmem_alloc(smem_u32(tmem_slot), 256);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -234,7 +237,7 @@ __global__ void __launch_bounds__(128, 1)
   const WaitCtl wc{abort_flag, err, wait_ns};
   const int nb_chunks = (mode == 0) ? 2 : n / 64;
   if (t == 0) {
-    const int a_chunks = (mode == 1) ? 0 : 2;
+    const int a_chunks = (mode == 1 || mode == 3) ? 0 : 2;
     mbar_arrive_expect_tx(bar_ld, (a_chunks + nb_chunks) * CHUNK);
     for (int cc = 0; cc < a_chunks; ++cc) tma_load_3d(A + cc * CHUNK, &ta, bar_ld, 64 * cc, 0, 0);
     for (int cc = 0; cc < nb_chunks; ++cc) tma_load_3d(B + cc * CHUNK, &tb, bar_ld, 64 * cc, 0, 0);
@@ -247,6 +250,23 @@ __global__ void __launch_bounds__(128, 1)
       st_shared_v4(A + (cc >> 3) * CHUNK + sw128_offset(t, cc & 7), w.x, w.y, w.z, w.w);
     }
     fence_async_smem();
+  }
+  if (mode == 3) {
+    // thread t writes row t of A into TMEM lane t, columns 128..191
+    const uint4* src = reinterpret_cast<const uint4*>(a_raw + t * 128);
+    for (int half = 0; half < 2; ++half) {
+      uint32_t w[32];
+      for (int cc = 0; cc < 8; ++cc) {
+        const uint4 x = src[8 * half + cc];
+        w[4 * cc + 0] = x.x;
+        w[4 * cc + 1] = x.y;
+        w[4 * cc + 2] = x.z;
+        w[4 * cc + 3] = x.w;
+      }
+      tmem_st32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + 128 + 32 * half, w);
+    }
+    tmem_st_wait();
+    tc_fence_before();
   }
   __syncthreads();
   bool ok = true;
@@ -268,11 +288,16 @@ __global__ void __launch_bounds__(128, 1)
           mma_bf16_ss(tmem, desc_sw128(A + aoff, 16, 1024), desc_sw128(B + kk * 2048, CHUNK, 1024),
                       id, kk > 0);
         }
-      } else {
+      } else if (mode == 2) {
         const uint32_t id = idesc_bf16(128, n, true, true);
         for (int kk = 0; kk < 8; ++kk)
           mma_bf16_ss(tmem, desc_sw128(A + kk * 2048, CHUNK, 1024),
                       desc_sw128(B + kk * 2048, CHUNK, 1024), id, kk > 0);
+      } else {
+        const uint32_t id = idesc_bf16(128, n, false, true);
+        for (int kk = 0; kk < 8; ++kk)
+          mma_bf16_ts(tmem, tmem + 128 + kk * 8, desc_sw128(B + kk * 2048, CHUNK, 1024), id,
+                      kk > 0);
       }
     }
     mma_commit(bar_mma);
@@ -296,7 +321,7 @@ __global__ void __launch_bounds__(128, 1)
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
-    tmem_dealloc(tmem, 128);
+    tmem_dealloc(tmem, 256);
   }
 }
 

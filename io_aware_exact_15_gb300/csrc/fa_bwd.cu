@@ -13,12 +13,16 @@
 //   warp 0      TMA producer: K_j, V_j once; Q_i through an NQ-slot ring and
 //               dO_i through an NDO-slot ring (128-byte swizzle)
 //   warp 1      allocates 512 TMEM columns; lane 0 issues the five MMAs
-//   warps 2-5   one thread per query row: P from S and lse (ex2 with the
-//               scale folded in), dS from dP and D, both written to shared
-//               memory as bf16 for the MMAs that read them
-//   warps 6-9   one thread per query row: read dQ_i from TMEM and add it into
-//               the fp32 dQ accumulator with vector reductions
-// At the end warps 2-5 write dV_j and warps 6-9 write scale * dK_j.
+//   warps 4-11  one thread per query row and half of the key columns (warps
+//               4-7: keys 0-63, warps 8-11: keys 64-127): P from S and lse
+//               (ex2 with the scale folded in) and dS from dP and D, both
+//               written to shared memory as bf16 for the MMAs that read them;
+//               between the two, the previous tile's dQ is read out of TMEM,
+//               staged in the (then idle) dS buffer and added into the fp32
+//               dQ accumulator by TMA reduce-add while the tensor core runs
+//               the next MMAs
+//   warps 2-3   idle
+// At the end warps 4-7 write dV_j and warps 8-11 write scale * dK_j.
 // TMEM: S [0,128) dP [128,256) dV [256,256+d) dK [256+d,256+2d);
 //       dQ at [384,448) for d = 64 and over the dP columns for d = 128.
 #include <math.h>
@@ -57,14 +61,14 @@ struct BwdSmem {
   static constexpr int T_DQ = (D == 64) ? 384 : T_DP;
 };
 
-constexpr int kBwdThreads = 320;
+constexpr int kBwdThreads = 384;
 constexpr float kLog2e = 1.4426950408889634f;
 
 template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     fa_bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
-                  const BwdParams p) {
+                  const __grid_constant__ CUtensorMap tdq, const BwdParams p) {
   using L = BwdSmem<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -94,10 +98,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     mbar_init(bar(L::B_SF), 1);
     mbar_init(bar(L::B_DPF), 1);
-    mbar_init(bar(L::B_PR), 128);
-    mbar_init(bar(L::B_DSR), 128);
+    mbar_init(bar(L::B_PR), 256);
+    mbar_init(bar(L::B_DSR), 256);
     mbar_init(bar(L::B_DQF), 1);
-    mbar_init(bar(L::B_DQE), 128);
+    mbar_init(bar(L::B_DQE), 256);
     mbar_init(bar(L::B_FIN), 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -122,6 +126,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       prefetch_tmap(&tk);
       prefetch_tmap(&tv);
       prefetch_tmap(&tdo);
+      prefetch_tmap(&tdq);
       mbar_arrive_expect_tx(bar(L::B_KV), 2 * L::TILE);
 #pragma unroll
       for (int c = 0; c < L::CH; ++c) {
@@ -261,117 +266,168 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mma_commit(bar(L::B_FIN));
       drain_bar(bar(L::B_FIN), 0, p.wait_ns);
     }
-  } else {
-    const bool compute = warp < 6;  // warps 2-5: P / dS;  warps 6-9: dQ read-out
+  } else if (warp >= 4) {
+    // ------------------------------------------------------ P, dS, dQ warps
+    // Warps 4-7 own key columns [0, 64) of the tile and warps 8-11 own
+    // [64, 128); each thread owns one query row (its TMEM lane).  Per query
+    // tile: P from S and lse into shared memory, then the previous tile's dQ
+    // out of TMEM into the fp32 accumulator (its MMA ran meanwhile), then dS
+    // from dP and D into shared memory.  P stays in registers as packed bf16
+    // for the dS step.
+    const int half = (warp - 4) >> 2;
     const int q4 = warp & 3;
     const int r = q4 * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
+    const uint32_t tS = tmem + lane_off + L::T_S + 64 * half;
+    const uint32_t tDP = tmem + lane_off + L::T_DP + 64 * half;
+    const uint32_t tDQ = tmem + lane_off + L::T_DQ + (D / 2) * half;
+    const uint32_t pbuf = sb + L::P + half * L::CHUNK;
+    const uint32_t dsbuf = sb + L::DS + half * L::CHUNK;
     const float sl2 = p.scale * kLog2e;
     const int kbase = kt * kTile;
+    const int kcol0 = kbase + 64 * half;  // first key of this thread's columns
     bool ok = true;
     uint32_t n = 0;
-    int qt;
-    while (ok && sch.next(qt)) {
-      const int qrow = qt * kTile + r;
-      const bool row_ok = qrow < N;
-      if (compute) {
-        const size_t ridx = static_cast<size_t>(bh) * N + (row_ok ? qrow : 0);
-        const float lse = p.lse[ridx];
-        const float dlt = p.delta[ridx];
-        const bool live = row_ok && lse != -INFINITY;
-        const float lse2 = live ? lse * kLog2e : 0.f;
-        ok = __all_sync(0xffffffffu, wait_bar(bar(L::B_SF), n & 1, wc));
-        if (!ok) break;
-        tc_fence_after();
-        uint32_t pr[4][32];
+    int qt = 0, qt_prev = 0;
+    bool have = sch.next(qt);
+    auto load_stats = [&](int t, float& l_, float& d_) {
+      const int row = t * kTile + r;
+      const size_t idx = static_cast<size_t>(bh) * N + (row < N ? row : 0);
+      l_ = p.lse[idx];
+      d_ = p.delta[idx];
+    };
+    float lse_c = 0.f, dlt_c = 0.f;
+    if (have) load_stats(qt, lse_c, dlt_c);
+    // dQ of query tile t (step m): TMEM -> registers, release the columns,
+    // then add this thread's D/2 columns into the fp32 accumulator
+    auto drain_dq = [&](uint32_t m, int t) -> bool {
+      if (!__all_sync(0xffffffffu, wait_bar(bar(L::B_DQF), m & 1, wc))) return false;
+      tc_fence_after();
+      uint32_t dq[D / 64][32];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld32(tmem + lane_off + L::T_S + 32 * c, pr[c]);
-        tmem_ld_wait();
+      for (int c = 0; c < D / 64; ++c) tmem_ld32(tDQ + 32 * c, dq[c]);
+      tmem_ld_wait();
 #pragma unroll
-        for (int c = 0; c < 4; ++c) reg_fence(pr[c]);
-        const bool need_mask = (kbase + kTile > N) || (p.causal && kbase + kTile - 1 > qt * kTile);
-        // P = exp2(S * scale * log2e - lse * log2e), masked entries 0
+      for (int c = 0; c < D / 64; ++c) reg_fence(dq[c]);
+      tc_fence_before();
+      mbar_arrive(bar(L::B_DQE));
+      // Reduce-add through the TMA engine: the warp stages its 32 rows x 32
+      // columns (4 KB, 128-byte swizzle) in its own rows of the dS buffer,
+      // which no MMA reads between dQ's completion and the next dS, and lane 0
+      // adds the box into the fp32 accumulator (rows past N are clipped).
+      const uint32_t stage = dsbuf + q4 * 4096;
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            float pv = ex2(fmaf(__uint_as_float(pr[c][j]), sl2, -lse2));
-            if (need_mask) {
-              const int key = kbase + 32 * c + j;
-              if (key >= N || (p.causal && key > qrow)) pv = 0.f;
-            }
-            pr[c][j] = __float_as_uint(live ? pv : 0.f);
-          }
-#pragma unroll
-        for (int cc = 0; cc < 16; ++cc) {
-          const uint32_t* e = &pr[cc >> 2][(cc & 3) * 8];
-          st_shared_v4(sb + L::P + (cc >> 3) * L::CHUNK + sw128_offset(r, cc & 7),
-                       pack_bf16(__uint_as_float(e[0]), __uint_as_float(e[1])),
-                       pack_bf16(__uint_as_float(e[2]), __uint_as_float(e[3])),
-                       pack_bf16(__uint_as_float(e[4]), __uint_as_float(e[5])),
-                       pack_bf16(__uint_as_float(e[6]), __uint_as_float(e[7])));
+      for (int c = 0; c < D / 64; ++c) {
+        if (c > 0) {
+          if (lane == 0) bulk_wait_read_all();
+          __syncwarp();
         }
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          st_shared_v4(stage + sw128_offset(lane, u), dq[c][4 * u], dq[c][4 * u + 1],
+                       dq[c][4 * u + 2], dq[c][4 * u + 3]);
         fence_async_smem();
-        tc_fence_before();
-        mbar_arrive(bar(L::B_PR));
-        // dS = P o (dP - D_i)
-        ok = __all_sync(0xffffffffu, wait_bar(bar(L::B_DPF), n & 1, wc));
-        if (!ok) break;
-        tc_fence_after();
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t dp[32];
-          tmem_ld32(tmem + lane_off + L::T_DP + 32 * c, dp);
-          tmem_ld_wait();
-          reg_fence(dp);
-#pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            float x[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-              x[j] = __uint_as_float(pr[c][8 * g + j]) * (__uint_as_float(dp[8 * g + j]) - dlt);
-            const int cc = 4 * c + g;
-            st_shared_v4(sb + L::DS + (cc >> 3) * L::CHUNK + sw128_offset(r, cc & 7),
-                         pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]), pack_bf16(x[4], x[5]),
-                         pack_bf16(x[6], x[7]));
-          }
-        }
-        fence_async_smem();
-        tc_fence_before();
-        mbar_arrive(bar(L::B_DSR));
-      } else {
-        ok = __all_sync(0xffffffffu, wait_bar(bar(L::B_DQF), n & 1, wc));
-        if (!ok) break;
-        tc_fence_after();
-        uint32_t dq[D / 32][32];
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) tmem_ld32(tmem + lane_off + L::T_DQ + 32 * c, dq[c]);
-        tmem_ld_wait();
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) reg_fence(dq[c]);
-        tc_fence_before();
-        mbar_arrive(bar(L::B_DQE));
-        if (row_ok) {
-          float* dst = p.dq_acc + (static_cast<size_t>(bh) * N + qrow) * D;
-#pragma unroll
-          for (int c = 0; c < D / 32; ++c)
-#pragma unroll
-            for (int v = 0; v < 8; ++v)
-              red_add_v4(dst + 32 * c + 4 * v, __uint_as_float(dq[c][4 * v + 0]),
-                         __uint_as_float(dq[c][4 * v + 1]), __uint_as_float(dq[c][4 * v + 2]),
-                         __uint_as_float(dq[c][4 * v + 3]));
+        __syncwarp();
+        if (lane == 0) {
+          tma_reduce_add_3d(&tdq, stage, (D / 2) * half + 32 * c, t * kTile + 32 * q4, bh);
+          bulk_commit();
         }
       }
+      // the staging rows are this warp's dS rows: their reads must be done
+      if (lane == 0) bulk_wait_read_all();
+      __syncwarp();
+      return true;
+    };
+    while (ok && have) {
+      int qt_n = 0;
+      const bool have_n = sch.next(qt_n);
+      float lse_n = 0.f, dlt_n = 0.f;
+      if (have_n) load_stats(qt_n, lse_n, dlt_n);  // prefetch the next tile's statistics
+      const int qrow = qt * kTile + r;
+      const bool live = qrow < N && lse_c != -INFINITY;
+      const float lse2 = live ? lse_c * kLog2e : 0.f;
+      // P = exp2(S * scale * log2e - lse * log2e); masked entries 0
+      ok = __all_sync(0xffffffffu, wait_bar(bar(L::B_SF), n & 1, wc));
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t sv[2][32];
+      tmem_ld32(tS, sv[0]);
+      tmem_ld32(tS + 32, sv[1]);
+      tmem_ld_wait();
+      reg_fence(sv[0]);
+      reg_fence(sv[1]);
+      const bool need_mask = (kcol0 + 64 > N) || (p.causal && kcol0 + 63 > qt * kTile);
+      // keys kcol0 + i with i >= lim are masked (past N, or after this row
+      // when causal)
+      int lim = N - kcol0;
+      if (p.causal && qrow - kcol0 + 1 < lim) lim = qrow - kcol0 + 1;
+      uint32_t pw[32];  // pw[i]: keys 2i, 2i+1 of this thread's 64 columns
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        float a = ex2(fmaf(__uint_as_float(sv[i >> 4][(2 * i) & 31]), sl2, -lse2));
+        float b = ex2(fmaf(__uint_as_float(sv[i >> 4][(2 * i + 1) & 31]), sl2, -lse2));
+        if (need_mask) {
+          if (2 * i >= lim) a = 0.f;
+          if (2 * i + 1 >= lim) b = 0.f;
+        }
+        pw[i] = live ? pack_bf16(a, b) : 0u;
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        st_shared_v4(pbuf + sw128_offset(r, u), pw[4 * u], pw[4 * u + 1], pw[4 * u + 2],
+                     pw[4 * u + 3]);
+      fence_async_smem();
+      tc_fence_before();
+      mbar_arrive(bar(L::B_PR));
+      if (n > 0 && !drain_dq(n - 1, qt_prev)) {
+        ok = false;
+        break;
+      }
+      // dS = P o (dP - D_i)
+      ok = __all_sync(0xffffffffu, wait_bar(bar(L::B_DPF), n & 1, wc));
+      if (!ok) break;
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t dp[32];
+        tmem_ld32(tDP + 32 * c, dp);
+        tmem_ld_wait();
+        reg_fence(dp);
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          uint32_t w[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint32_t pp = pw[16 * c + 4 * g + j];
+            const float x0 = bf16_lo(pp) * (__uint_as_float(dp[8 * g + 2 * j]) - dlt_c);
+            const float x1 = bf16_hi(pp) * (__uint_as_float(dp[8 * g + 2 * j + 1]) - dlt_c);
+            w[j] = pack_bf16(x0, x1);
+          }
+          st_shared_v4(dsbuf + sw128_offset(r, 4 * c + g), w[0], w[1], w[2], w[3]);
+        }
+      }
+      fence_async_smem();
+      tc_fence_before();
+      mbar_arrive(bar(L::B_DSR));
+      qt_prev = qt;
+      qt = qt_n;
+      have = have_n;
+      lse_c = lse_n;
+      dlt_c = dlt_n;
       ++n;
     }
+    if (ok && n > 0) ok = drain_dq(n - 1, qt_prev);
+    if (lane == 0) bulk_wait_all();  // every dQ reduce of this warp has landed
     // ---------------------------------------------------- epilogue: dV, dK
+    // warps 4-7 write dV_j, warps 8-11 write scale * dK_j (thread = key row)
     if (ok) ok = __all_sync(0xffffffffu, wait_bar(bar(L::B_FIN), 0, wc));
     tc_fence_after();
     const int key = kbase + r;
     if (ok) {  // warp-uniform: every lane takes part in the TMEM reads
-      const uint32_t tcol = compute ? L::T_DV : L::T_DK;
-      const float mul = compute ? 1.f : p.scale;
-      uint8_t* dst = static_cast<uint8_t*>(compute ? p.dv : p.dk) +
+      const bool dv_side = half == 0;
+      const uint32_t tcol = dv_side ? L::T_DV : L::T_DK;
+      const float mul = dv_side ? 1.f : p.scale;
+      uint8_t* dst = static_cast<uint8_t*>(dv_side ? p.dv : p.dk) +
                      (static_cast<size_t>(bh) * N + (key < N ? key : 0)) * static_cast<size_t>(D) * 2;
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
@@ -409,7 +465,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
 template <int D>
 cudaError_t launch_bwd_d(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
-                         const CUtensorMap& tv, const CUtensorMap& tdo, cudaStream_t stream) {
+                         const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq,
+                         cudaStream_t stream) {
   using L = BwdSmem<D>;
   cudaError_t e = cudaFuncSetAttribute(fa_bwd_kernel<D>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
@@ -417,7 +474,7 @@ cudaError_t launch_bwd_d(const BwdParams& p, const CUtensorMap& tq, const CUtens
   const int nT = (p.N + kTile - 1) / kTile;
   const long long ctas = static_cast<long long>(nT) * p.B * p.H;
   fa_bwd_kernel<D><<<static_cast<unsigned>(ctas), kBwdThreads, L::ALLOC, stream>>>(tq, tk, tv, tdo,
-                                                                                   p);
+                                                                                   tdq, p);
   return cudaGetLastError();
 }
 
@@ -425,9 +482,9 @@ cudaError_t launch_bwd_d(const BwdParams& p, const CUtensorMap& tq, const CUtens
 
 cudaError_t launch_backward_main(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                                  const CUtensorMap& tv, const CUtensorMap& tdo,
-                                 cudaStream_t stream) {
-  if (p.d == 64) return launch_bwd_d<64>(p, tq, tk, tv, tdo, stream);
-  if (p.d == 128) return launch_bwd_d<128>(p, tq, tk, tv, tdo, stream);
+                                 const CUtensorMap& tdq, cudaStream_t stream) {
+  if (p.d == 64) return launch_bwd_d<64>(p, tq, tk, tv, tdo, tdq, stream);
+  if (p.d == 128) return launch_bwd_d<128>(p, tq, tk, tv, tdo, tdq, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -15,11 +15,15 @@
 //               thread per query row reads its 128 scores from TMEM, applies
 //               the causal / ragged-length mask, updates (m, l) in the log2
 //               domain with the scale folded into one FMA before ex2, writes
-//               P (bf16) into shared memory for the PV MMA, and rescales its
+//               P (bf16) back into TMEM over the scores it has read (the PV
+//               MMA takes its A operand from TMEM), and rescales its
 //               O row in TMEM only when the running max grew by more than
 //               2^8 (the final O / l uses the same m, so this stays exact).
 // While one warpgroup does its softmax the tensor core runs the other tile's
-// MMAs.  TMEM columns: S0 [0,128) S1 [128,256) O0 [256,256+d) O1 [.., +d).
+// MMAs.  TMEM columns: S0 [0,128) S1 [128,256) O0 [256,256+d) O1 [.., +d);
+// P_s takes the first 64 columns of S_s.  The MMA issuer puts PV_s(j) before
+// S_s(j+1) in its stream, so the tensor core reads P_s before the next scores
+// overwrite those columns.  The K/V ring is 5 (d = 128) or 8 (d = 64) tiles.
 #include <math.h>
 
 #include "fa_internal.h"
@@ -34,11 +38,9 @@ struct FwdSmem {
   static constexpr int CH = D / 64;             // 128-byte column chunks per row
   static constexpr int CHUNK = kTile * 128;     // [128 rows x 128 B] = 16 KB
   static constexpr int TILE = CH * CHUNK;       // one 128 x D bf16 tile
-  static constexpr int NS = (D == 64) ? 6 : 3;  // K/V ring slots (one tile each)
-  static constexpr int PT = 2 * CHUNK;          // one 128 x 128 bf16 P tile
+  static constexpr int NS = (D == 64) ? 8 : 5;  // K/V ring slots (one tile each)
   static constexpr int Q = 0;
-  static constexpr int P = Q + 2 * TILE;
-  static constexpr int KV = P + 2 * PT;
+  static constexpr int KV = Q + 2 * TILE;
   static constexpr int BAR = KV + NS * TILE;
   static constexpr int B_Q = 0, B_KVF = 1, B_KVE = 1 + NS, B_SF = 1 + 2 * NS, B_PF = B_SF + 2,
                        B_OF = B_PF + 2, NBAR = B_OF + 1;
@@ -156,19 +158,18 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                       desc_sw128(kb + off, 16, 1024), idS, kk > 0);
         }
       };
+      // O_s += P_s V: P_s sits in TMEM (columns 128 s .. 128 s + 63, two bf16
+      // per column), V is MN-major in shared memory
       auto issue_pv = [&](int s, int vpos, bool acc) {
-        const uint32_t pa = sb + L::P + s * L::PT;
         const uint32_t vb = sb + L::KV + vpos * L::TILE;
 #pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk) {
-          const uint32_t aoff = (kk >> 2) * L::CHUNK + (kk & 3) * 32;
-          mma_bf16_ss(tmem + 256 + s * D, desc_sw128(pa + aoff, 16, 1024),
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          mma_bf16_ts(tmem + 256 + s * D, tmem + s * 128 + kk * 8,
                       desc_sw128(vb + kk * 2048, L::CHUNK, 1024), idO, (acc || kk > 0) ? 1u : 0u);
-        }
       };
       int kt, mem, kt_n = 0, mem_n = 0;
       uint32_t idx = 0;
-      int cnt[2] = {0, 0};
+      uint32_t cnt01 = 0;  // participations of slot 0 (low 16 bits) and slot 1 (high)
       bool ok = wait_bar(bar(L::B_Q), 0, wc);
       bool have = sch.next(kt, mem);
       if (ok && have) {
@@ -195,11 +196,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         int kpos = -1;
         for (int s = 0; s < 2 && ok; ++s) {
           if (mem & (1 << s)) {
-            ok = wait_bar(bar(L::B_PF + s), cnt[s] & 1, wc);
+            const uint32_t cs = (cnt01 >> (16 * s)) & 0xFFFFu;
+            ok = wait_bar(bar(L::B_PF + s), cs & 1, wc);
             if (!ok) break;
             tc_fence_after();
-            issue_pv(s, vpos, cnt[s] > 0);
-            ++cnt[s];
+            issue_pv(s, vpos, cs > 0);
+            cnt01 += 1u << (16 * s);
           }
           if (have_n && (mem_n & (1 << s))) {
             if (kpos < 0) {
@@ -237,7 +239,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
     const uint32_t tS = tmem + lane_off + s * 128;
     const uint32_t tO = tmem + lane_off + 256 + s * D;
-    const uint32_t pbuf = sb + L::P + s * L::PT;
     const float sl2 = p.scale * kLog2e;
     float m = -INFINITY, l = 0.f;
     int cnt = 0;
@@ -257,13 +258,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       const int kbase = kt * kTile;
       const bool need_mask = (kbase + kTile > N) || (p.causal && kbase + kTile - 1 > qt * kTile);
       if (need_mask) {
+        // keys kbase + i with i >= lim are masked (past N, or after this row
+        // when causal)
+        int lim = N - kbase;
+        if (p.causal && qrow - kbase + 1 < lim) lim = qrow - kbase + 1;
 #pragma unroll
         for (int c = 0; c < 4; ++c)
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int key = kbase + 32 * c + j;
-            if (key >= N || (p.causal && key > qrow)) sr[c][j] = __float_as_uint(-INFINITY);
-          }
+          for (int j = 0; j < 32; ++j)
+            if (32 * c + j >= lim) sr[c][j] = __float_as_uint(-INFINITY);
       }
       float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
@@ -280,7 +283,33 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         l *= alpha;
         m = m_new;
       }
-      if (cnt > 0 && __any_sync(0xffffffffu, resc)) {
+      const bool rescale_o = cnt > 0 && __any_sync(0xffffffffu, resc);
+      const float mu = (m == -INFINITY) ? 0.f : m;
+      float ls0 = 0.f, ls1 = 0.f;
+      // P (bf16, two per 32-bit column) overwrites the first 64 columns of
+      // this tile's S, which are already in registers
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {  // 32 keys -> 16 columns per store
+        // packed words overwrite the scores already consumed: group c4 reads
+        // sr[q][8 c4 .. 8 c4 + 7] and writes sr[q][4 c4 .. 4 c4 + 3]
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4) {
+          float e[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) e[j] = ex2(fmaf(__uint_as_float(sr[q][8 * c4 + j]), sl2, -mu));
+#pragma unroll
+          for (int j = 0; j < 4; ++j) sr[q][4 * c4 + j] = pack_bf16(e[2 * j], e[2 * j + 1]);
+          // l sums the same bf16-rounded weights the PV MMA consumes, so a
+          // dominant key's rounding cancels in O / l
+          ls0 += (bf16_lo(sr[q][4 * c4]) + bf16_hi(sr[q][4 * c4])) +
+                 (bf16_lo(sr[q][4 * c4 + 1]) + bf16_hi(sr[q][4 * c4 + 1]));
+          ls1 += (bf16_lo(sr[q][4 * c4 + 2]) + bf16_hi(sr[q][4 * c4 + 2])) +
+                 (bf16_lo(sr[q][4 * c4 + 3]) + bf16_hi(sr[q][4 * c4 + 3]));
+        }
+        tmem_st16(tS + 16 * q, *reinterpret_cast<const uint32_t(*)[16]>(&sr[q][0]));
+      }
+      // rescale O only after P is out of the registers (lower register pressure)
+      if (rescale_o) {
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
           uint32_t o[32];
@@ -293,24 +322,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         }
         tmem_st_wait();
       }
-      const float mu = (m == -INFINITY) ? 0.f : m;
-      float ls0 = 0.f, ls1 = 0.f;
-#pragma unroll
-      for (int cc = 0; cc < 16; ++cc) {
-        float e[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-          e[j] = ex2(fmaf(__uint_as_float(sr[cc >> 2][(cc & 3) * 8 + j]), sl2, -mu));
-        const uint32_t w0 = pack_bf16(e[0], e[1]), w1 = pack_bf16(e[2], e[3]);
-        const uint32_t w2 = pack_bf16(e[4], e[5]), w3 = pack_bf16(e[6], e[7]);
-        // l sums the same bf16-rounded weights the PV MMA consumes, so a
-        // dominant key's rounding cancels in O / l
-        ls0 += (bf16_lo(w0) + bf16_hi(w0)) + (bf16_lo(w1) + bf16_hi(w1));
-        ls1 += (bf16_lo(w2) + bf16_hi(w2)) + (bf16_lo(w3) + bf16_hi(w3));
-        st_shared_v4(pbuf + (cc >> 3) * L::CHUNK + sw128_offset(r, cc & 7), w0, w1, w2, w3);
-      }
+      tmem_st_wait();
       l += ls0 + ls1;
-      fence_async_smem();
       tc_fence_before();
       mbar_arrive(bar(L::B_PF + s));
       ++cnt;

@@ -50,12 +50,16 @@ struct BwdParams {
 // 3-D bf16 view {d, N, B*H} of a [B, H, N, d] tensor, 128-row x 64-column
 // boxes with 128-byte swizzle.
 bool make_tile_map(CUtensorMap* map, const void* base, int BH, int N, int d);
+// 3-D fp32 view {d, N, B*H} of a [B, H, N, d] fp32 tensor, 32 x 32 boxes
+// (128-byte rows, 128-byte swizzle): the dQ accumulator for TMA reduce-add.
+bool make_acc_map(CUtensorMap* map, const void* base, int BH, int N, int d);
 
 cudaError_t launch_forward(const FwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                            const CUtensorMap& tv, cudaStream_t stream);
 cudaError_t launch_backward_main(const BwdParams& p, const CUtensorMap& tq,
                                  const CUtensorMap& tk, const CUtensorMap& tv,
-                                 const CUtensorMap& tdo, cudaStream_t stream);
+                                 const CUtensorMap& tdo, const CUtensorMap& tdq,
+                                 cudaStream_t stream);
 cudaError_t launch_bwd_preprocess(const void* o, const void* dO, float* delta, float* dq_acc,
                                   long long rows, int d, cudaStream_t stream);
 cudaError_t launch_dq_convert(const float* dq_acc, void* dq, long long n, float scale,

@@ -105,7 +105,7 @@ def test_blocksparse_rejects_bad_mask_args():
 
 def test_debug_entry_points_validate():
     assert fa.fa_debug_wait_timeout(0, 0) == fa.FA_ERR_INVALID_ARG
-    assert fa.fa_debug_mma_probe(ALIGNED, ALIGNED, ALIGNED, 3, 64, 0) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_debug_mma_probe(ALIGNED, ALIGNED, ALIGNED, 4, 64, 0) == fa.FA_ERR_INVALID_ARG
     assert fa.fa_debug_mma_probe(ALIGNED, ALIGNED, ALIGNED, 1, 96, 0) == fa.FA_ERR_UNSUPPORTED
     assert fa.fa_set_wait_limit_ns(0) == fa.FA_OK
 

@@ -8,7 +8,8 @@ import io_aware_exact_15_gb300 as fa
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("mode,n", [(0, 128), (1, 64), (1, 128), (2, 64), (2, 128)])
+@pytest.mark.parametrize("mode,n", [(0, 128), (1, 64), (1, 128), (2, 64), (2, 128), (3, 64),
+                                    (3, 128)])
 def test_mma_probe_matches_fp32_matmul(mode, n):
     dev = device()
     g = torch.Generator().manual_seed(100 + 10 * mode + n)
@@ -16,7 +17,7 @@ def test_mma_probe_matches_fp32_matmul(mode, n):
     b = torch.randn(128, n, generator=g).to(torch.bfloat16)
     if mode == 0:
         ref = a.float() @ b.float().T
-    elif mode == 1:
+    elif mode in (1, 3):
         ref = a.float() @ b.float()
     else:
         ref = a.float().T @ b.float()
