@@ -177,30 +177,37 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       constexpr uint32_t idSS = idesc_bf16(128, 128, false, false);  // S, dP
       constexpr uint32_t idTT = idesc_bf16(128, D, true, true);      // dV, dK
       constexpr uint32_t idDQ = idesc_bf16(128, D, false, true);     // dQ
+      // One k-step (K = 16) of each product.  A chain of k-steps into one
+      // accumulator is latency-bound on the tensor core, so independent
+      // chains are issued interleaved step by step where the data allows.
       // X[128 q x 128 k] = A[128 x D] B[128 x D]^T, both K-major
-      auto issue_qk = [&](uint32_t dst, uint32_t a, uint32_t b) {
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * L::CHUNK + (kk & 3) * 32;
-          mma_bf16_ss(dst, desc_sw128(a + off, 16, 1024), desc_sw128(b + off, 16, 1024), idSS,
-                      kk > 0);
-        }
+      auto qk_step = [&](uint32_t dst, uint32_t a, uint32_t b, int kk) {
+        const uint32_t off = (kk >> 2) * L::CHUNK + (kk & 3) * 32;
+        mma_bf16_ss(dst, desc_sw128(a + off, 16, 1024), desc_sw128(b + off, 16, 1024), idSS,
+                    kk > 0);
       };
       // Y[128 k x D] += X^T[128 k x 128 q] Z[128 q x D]; X stored [q][k]
-      auto issue_tt = [&](uint32_t dst, uint32_t x, uint32_t z, bool acc) {
-#pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk)
-          mma_bf16_ss(dst, desc_sw128(x + kk * 2048, L::CHUNK, 1024),
-                      desc_sw128(z + kk * 2048, L::CHUNK, 1024), idTT, (acc || kk > 0) ? 1u : 0u);
+      auto tt_step = [&](uint32_t dst, uint32_t x, uint32_t z, bool acc, int kk) {
+        mma_bf16_ss(dst, desc_sw128(x + kk * 2048, L::CHUNK, 1024),
+                    desc_sw128(z + kk * 2048, L::CHUNK, 1024), idTT, (acc || kk > 0) ? 1u : 0u);
       };
       // dQ[128 q x D] = dS[128 q x 128 k] K[128 k x D]
+      auto dq_step = [&](uint32_t dst, int kk) {
+        const uint32_t aoff = (kk >> 2) * L::CHUNK + (kk & 3) * 32;
+        mma_bf16_ss(dst, desc_sw128(sb + L::DS + aoff, 16, 1024),
+                    desc_sw128(sb + L::K + kk * 2048, L::CHUNK, 1024), idDQ, kk > 0);
+      };
+      auto issue_qk = [&](uint32_t dst, uint32_t a, uint32_t b) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) qk_step(dst, a, b, kk);
+      };
+      auto issue_tt = [&](uint32_t dst, uint32_t x, uint32_t z, bool acc) {
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk) tt_step(dst, x, z, acc, kk);
+      };
       auto issue_dq = [&](uint32_t dst) {
 #pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk) {
-          const uint32_t aoff = (kk >> 2) * L::CHUNK + (kk & 3) * 32;
-          mma_bf16_ss(dst, desc_sw128(sb + L::DS + aoff, 16, 1024),
-                      desc_sw128(sb + L::K + kk * 2048, L::CHUNK, 1024), idDQ, kk > 0);
-        }
+        for (int kk = 0; kk < kTile / 16; ++kk) dq_step(dst, kk);
       };
       const uint32_t tS = tmem + L::T_S, tDP = tmem + L::T_DP, tDV = tmem + L::T_DV,
                      tDK = tmem + L::T_DK, tDQ = tmem + L::T_DQ;
@@ -226,29 +233,53 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const bool have_n = sch.next(qt_n);
         const uint32_t qpos = n % L::NQ, dpos = n % L::NDO;
         const uint32_t n1 = n + 1;
-        // dV += P^T dO_i once P is in shared memory
+        // dV += P^T dO_i once P is in shared memory, interleaved with the
+        // next S when its Q tile is already in (the S columns were read)
         if (!(ok = wait_bar(bar(L::B_PR), n & 1, wc))) break;
         tc_fence_after();
-        issue_tt(tDV, sb + L::P, sb + L::DOR + dpos * L::TILE, n > 0);
-        mma_commit(bar(L::B_DOE + dpos));
-        // next S as soon as its Q tile is in (the S columns were read)
-        if (have_n) {
-          if (!(ok = wait_bar(bar(L::B_QF + n1 % L::NQ), (n1 / L::NQ) & 1, wc))) break;
+        const uint32_t qn = sb + L::QR + (n1 % L::NQ) * L::TILE;
+        const uint32_t dov = sb + L::DOR + dpos * L::TILE;
+        if (have_n && mbar_try(bar(L::B_QF + n1 % L::NQ), (n1 / L::NQ) & 1)) {
           tc_fence_after();
-          issue_qk(tS, sb + L::QR + (n1 % L::NQ) * L::TILE, sb + L::K);
+#pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk) {
+            tt_step(tDV, sb + L::P, dov, n > 0, kk);
+            if (kk < D / 16) qk_step(tS, qn, sb + L::K, kk);
+          }
+          mma_commit(bar(L::B_DOE + dpos));
           mma_commit(bar(L::B_SF));
+        } else {
+          issue_tt(tDV, sb + L::P, dov, n > 0);
+          mma_commit(bar(L::B_DOE + dpos));
+          if (have_n) {
+            if (!(ok = wait_bar(bar(L::B_QF + n1 % L::NQ), (n1 / L::NQ) & 1, wc))) break;
+            tc_fence_after();
+            issue_qk(tS, qn, sb + L::K);
+            mma_commit(bar(L::B_SF));
+          }
         }
-        // dK += dS^T Q_i, dQ_i = dS K once dS is in shared memory
+        // dK += dS^T Q_i and dQ_i = dS K once dS is in shared memory,
+        // interleaved when the dQ columns are free
         if (!(ok = wait_bar(bar(L::B_DSR), n & 1, wc))) break;
         tc_fence_after();
-        issue_tt(tDK, sb + L::DS, sb + L::QR + qpos * L::TILE, n > 0);
-        mma_commit(bar(L::B_QE + qpos));
-        if (D == 64 && n > 0) {
+        const uint32_t qv = sb + L::QR + qpos * L::TILE;
+        if (D != 64 || n == 0 || mbar_try(bar(L::B_DQE), (n - 1) & 1)) {
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk) {
+            tt_step(tDK, sb + L::DS, qv, n > 0, kk);
+            dq_step(tDQ, kk);
+          }
+          mma_commit(bar(L::B_QE + qpos));
+          mma_commit(bar(L::B_DQF));
+        } else {
+          issue_tt(tDK, sb + L::DS, qv, n > 0);
+          mma_commit(bar(L::B_QE + qpos));
           if (!(ok = wait_bar(bar(L::B_DQE), (n - 1) & 1, wc))) break;
           tc_fence_after();
+          issue_dq(tDQ);
+          mma_commit(bar(L::B_DQF));
         }
-        issue_dq(tDQ);
-        mma_commit(bar(L::B_DQF));
         if (have_n) {
           if (D != 64) {  // dQ_i shares the dP columns: wait until it is read out
             if (!(ok = wait_bar(bar(L::B_DQE), n & 1, wc))) break;
