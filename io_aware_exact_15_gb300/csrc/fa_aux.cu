@@ -73,53 +73,50 @@ cudaError_t launch_build_lists(const uint8_t* mask, int mask_heads, int nT, int*
 }
 
 // ------------------------------------------------------------------ backward helpers
-// D_i = sum_c dO_ic O_ic in fp32 (one warp per row) and dQ_acc = 0.
+// D_i = sum_c dO_ic O_ic in fp32 and dQ_acc = 0.  Each thread takes 8
+// consecutive elements of a row (16-byte loads of O and dO, 32 bytes of
+// zeros); the D/8 threads of a row reduce with shuffles.
 template <int D>
-__global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const uint16_t* __restrict__ o,
-                                                         const uint16_t* __restrict__ dO,
+__global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const uint4* __restrict__ o,
+                                                         const uint4* __restrict__ dO,
                                                          float* __restrict__ delta,
-                                                         float* __restrict__ dq_acc,
+                                                         float4* __restrict__ dq_acc,
                                                          long long rows) {
-  constexpr int PER = D / 32;  // elements per lane: 2 or 4
-  const int lane = threadIdx.x & 31;
-  const long long warps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
-  for (long long row = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
-       row < rows; row += warps) {
-    const size_t base = static_cast<size_t>(row) * D + lane * PER;
+  constexpr int TPR = D / 8;  // threads per row: 8 or 16
+  const long long total = rows * TPR;
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+       t - (threadIdx.x & 31) < total; t += stride) {
+    const bool live = t < total;
     float acc = 0.f;
-    if (PER == 2) {
-      const uint32_t a = *reinterpret_cast<const uint32_t*>(o + base);
-      const uint32_t b = *reinterpret_cast<const uint32_t*>(dO + base);
-      acc = __uint_as_float(a << 16) * __uint_as_float(b << 16) +
-            __uint_as_float(a & 0xFFFF0000u) * __uint_as_float(b & 0xFFFF0000u);
-      *reinterpret_cast<float2*>(dq_acc + base) = make_float2(0.f, 0.f);
-    } else {
-      const uint2 a = *reinterpret_cast<const uint2*>(o + base);
-      const uint2 b = *reinterpret_cast<const uint2*>(dO + base);
-      acc = __uint_as_float(a.x << 16) * __uint_as_float(b.x << 16) +
-            __uint_as_float(a.x & 0xFFFF0000u) * __uint_as_float(b.x & 0xFFFF0000u) +
-            __uint_as_float(a.y << 16) * __uint_as_float(b.y << 16) +
-            __uint_as_float(a.y & 0xFFFF0000u) * __uint_as_float(b.y & 0xFFFF0000u);
-      *reinterpret_cast<float4*>(dq_acc + base) = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (live) {
+      const uint4 a = o[t], b = dO[t];
+      acc = bf16_lo(a.x) * bf16_lo(b.x) + bf16_hi(a.x) * bf16_hi(b.x) +
+            bf16_lo(a.y) * bf16_lo(b.y) + bf16_hi(a.y) * bf16_hi(b.y) +
+            bf16_lo(a.z) * bf16_lo(b.z) + bf16_hi(a.z) * bf16_hi(b.z) +
+            bf16_lo(a.w) * bf16_lo(b.w) + bf16_hi(a.w) * bf16_hi(b.w);
+      dq_acc[2 * t] = make_float4(0.f, 0.f, 0.f, 0.f);
+      dq_acc[2 * t + 1] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (lane == 0) delta[row] = acc;
+    for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (live && (t % TPR) == 0) delta[t / TPR] = acc;
   }
 }
 
 cudaError_t launch_bwd_preprocess(const void* o, const void* dO, float* delta, float* dq_acc,
                                   long long rows, int d, cudaStream_t stream) {
-  const long long want = (rows + 7) / 8;
-  const int blocks = static_cast<int>(want < 152LL * 16 ? want : 152LL * 16);
+  const long long threads = rows * (d / 8);
+  const long long want = (threads + 255) / 256;
+  const int blocks = static_cast<int>(want < 152LL * 32 ? want : 152LL * 32);
   if (d == 64)
-    fa_bwd_pre_kernel<64><<<blocks, 256, 0, stream>>>(static_cast<const uint16_t*>(o),
-                                                      static_cast<const uint16_t*>(dO), delta,
-                                                      dq_acc, rows);
+    fa_bwd_pre_kernel<64><<<blocks, 256, 0, stream>>>(static_cast<const uint4*>(o),
+                                                      static_cast<const uint4*>(dO), delta,
+                                                      reinterpret_cast<float4*>(dq_acc), rows);
   else
-    fa_bwd_pre_kernel<128><<<blocks, 256, 0, stream>>>(static_cast<const uint16_t*>(o),
-                                                       static_cast<const uint16_t*>(dO), delta,
-                                                       dq_acc, rows);
+    fa_bwd_pre_kernel<128><<<blocks, 256, 0, stream>>>(static_cast<const uint4*>(o),
+                                                       static_cast<const uint4*>(dO), delta,
+                                                       reinterpret_cast<float4*>(dq_acc), rows);
   return cudaGetLastError();
 }
 

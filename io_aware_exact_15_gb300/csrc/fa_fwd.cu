@@ -21,9 +21,11 @@
 //               2^8 (the final O / l uses the same m, so this stays exact).
 // While one warpgroup does its softmax the tensor core runs the other tile's
 // MMAs.  TMEM columns: S0 [0,128) S1 [128,256) O0 [256,256+d) O1 [.., +d);
-// P_s takes the first 64 columns of S_s.  The MMA issuer puts PV_s(j) before
-// S_s(j+1) in its stream, so the tensor core reads P_s before the next scores
-// overwrite those columns.  The K/V ring is 5 (d = 128) or 8 (d = 64) tiles.
+// d = 64 keeps P0, P1 at [384,448), [448,512).  d = 128 has no free columns,
+// so P_s takes the first 64 columns of S_s and the MMA issuer puts PV_s(j)
+// before S_s(j+1) in its stream: the tensor core runs one CTA's MMAs in
+// issue order, so P_s is read before the next scores overwrite it.  The K/V
+// ring is 5 (d = 128) or 8 (d = 64) tiles.
 #include <math.h>
 
 #include "fa_internal.h"
@@ -45,6 +47,11 @@ struct FwdSmem {
   static constexpr int B_Q = 0, B_KVF = 1, B_KVE = 1 + NS, B_SF = 1 + 2 * NS, B_PF = B_SF + 2,
                        B_OF = B_PF + 2, NBAR = B_OF + 1;
   static constexpr int MISC = BAR + NBAR * 8;
+  // TMEM columns of P_s: d = 64 leaves room for P after O1 (384 + 64 s);
+  // d = 128 fills TMEM with S and O, so P_s overwrites the first 64 columns
+  // of S_s (already read into registers)
+  static constexpr int T_P = (D == 64) ? 384 : 0;
+  static constexpr int T_PSTRIDE = (D == 64) ? 64 : 128;
   static constexpr int ALLOC = MISC + 16 + 1024;  // + slack for 1024-byte alignment
   static_assert(ALLOC <= 232448, "shared memory budget");
 };
@@ -158,13 +165,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                       desc_sw128(kb + off, 16, 1024), idS, kk > 0);
         }
       };
-      // O_s += P_s V: P_s sits in TMEM (columns 128 s .. 128 s + 63, two bf16
-      // per column), V is MN-major in shared memory
+      // O_s += P_s V: P_s sits in TMEM (64 columns, two bf16 per column), V is
+      // MN-major in shared memory
       auto issue_pv = [&](int s, int vpos, bool acc) {
         const uint32_t vb = sb + L::KV + vpos * L::TILE;
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
-          mma_bf16_ts(tmem + 256 + s * D, tmem + s * 128 + kk * 8,
+          mma_bf16_ts(tmem + 256 + s * D, tmem + L::T_P + s * L::T_PSTRIDE + kk * 8,
                       desc_sw128(vb + kk * 2048, L::CHUNK, 1024), idO, (acc || kk > 0) ? 1u : 0u);
       };
       int kt, mem, kt_n = 0, mem_n = 0;
@@ -239,6 +246,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
     const uint32_t tS = tmem + lane_off + s * 128;
     const uint32_t tO = tmem + lane_off + 256 + s * D;
+    const uint32_t tP = tmem + lane_off + L::T_P + s * L::T_PSTRIDE;
     const float sl2 = p.scale * kLog2e;
     float m = -INFINITY, l = 0.f;
     int cnt = 0;
@@ -286,8 +294,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       const bool rescale_o = cnt > 0 && __any_sync(0xffffffffu, resc);
       const float mu = (m == -INFINITY) ? 0.f : m;
       float ls0 = 0.f, ls1 = 0.f;
-      // P (bf16, two per 32-bit column) overwrites the first 64 columns of
-      // this tile's S, which are already in registers
+      // P (bf16, two per 32-bit column) goes to TMEM: its own columns for
+      // d = 64, the first 64 columns of this tile's S (already in registers)
+      // for d = 128
 #pragma unroll
       for (int q = 0; q < 4; ++q) {  // 32 keys -> 16 columns per store
         // packed words overwrite the scores already consumed: group c4 reads
@@ -306,7 +315,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           ls1 += (bf16_lo(sr[q][4 * c4 + 2]) + bf16_hi(sr[q][4 * c4 + 2])) +
                  (bf16_lo(sr[q][4 * c4 + 3]) + bf16_hi(sr[q][4 * c4 + 3]));
         }
-        tmem_st16(tS + 16 * q, *reinterpret_cast<const uint32_t(*)[16]>(&sr[q][0]));
+        tmem_st16(tP + 16 * q, *reinterpret_cast<const uint32_t(*)[16]>(&sr[q][0]));
       }
       // rescale O only after P is out of the registers (lower register pressure)
       if (rescale_o) {
