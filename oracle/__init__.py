@@ -16,6 +16,9 @@ Parity status of each function (what pins it, tests/test_oracle_pins.py):
                    permutation equivariance, float64 autograd cross-check
   backward         pinned: central finite differences of forward, column-sum
                    invariants, N=1, golden closed-form gradients
+  grouped K/V      pinned: equals the pinned per-head path on repeated K/V,
+                   group sums of its key gradients, finite differences through
+                   a shared key/value row
   mask_lists       pinned: hand-derived golden lists, CSR/CSC transposition
   tile_counts      pinned: closed forms n(n+1)/2 and n^2, nnz of the mask
 """
@@ -60,10 +63,10 @@ def _load():
         ip = ctypes.POINTER(ctypes.c_int)
         u8p = ctypes.POINTER(ctypes.c_ubyte)
         L, I, D = ctypes.c_long, ctypes.c_int, ctypes.c_double
-        lib.fao_forward.argtypes = [dp, dp, dp, L, L, L, L, D, I, u8p, L, L, lp, L, dp, dp, I]
+        lib.fao_forward.argtypes = [dp, dp, dp, L, L, L, L, L, D, I, u8p, L, L, lp, L, dp, dp, I]
         lib.fao_forward.restype = I
-        lib.fao_backward.argtypes = [dp, dp, dp, dp, L, L, L, L, D, I, u8p, L, L, lp, L, lp, L,
-                                     dp, dp, dp, I]
+        lib.fao_backward.argtypes = [dp, dp, dp, dp, L, L, L, L, L, D, I, u8p, L, L, lp, L, lp,
+                                     L, dp, dp, dp, I]
         lib.fao_backward.restype = I
         lib.fao_mask_lists.argtypes = [u8p, L, L, ip, ip, ip, ip]
         lib.fao_mask_lists.restype = I
@@ -111,19 +114,23 @@ def _rows(rows):
 def forward(q, k, v, scale, causal=False, block_mask=None, tile=TILE, rows=None, nthreads=None):
     """O and natural-log lse of softmax(scale*QK^T + mask) V in fp64.
 
-    q, k, v: [B, H, N, d].  block_mask: [1 or H, nT, nT] (nonzero keeps the
-    tile), nT = ceil(N / tile).  rows: optional query rows evaluated in every
-    head.  Returns o [B, H, R, d] and lse [B, H, R] (R = N or len(rows)).
+    q: [B, H, N, d]; k, v: [B, Hkv, N, d] with H a multiple of Hkv (query
+    head h reads key/value head h // (H // Hkv)).  block_mask: [1 or H, nT,
+    nT] (nonzero keeps the tile), nT = ceil(N / tile).  rows: optional query
+    rows evaluated in every head.  Returns o [B, H, R, d] and lse [B, H, R]
+    (R = N or len(rows)).
     """
     q, k, v = _f64(q), _f64(k), _f64(v)
     B, H, N, d = q.shape
+    Hkv = k.shape[1]
     m, mh, keep = _mask_args(block_mask, H)
     rp, nr, keep_r = _rows(rows)
     R = N if rows is None else nr
     o = np.zeros((B, H, R, d))
     lse = np.zeros((B, H, R))
     st = _load().fao_forward(_ptr(q, ctypes.c_double), _ptr(k, ctypes.c_double),
-                             _ptr(v, ctypes.c_double), B, H, N, d, float(scale), int(bool(causal)),
+                             _ptr(v, ctypes.c_double), B, H, Hkv, N, d, float(scale),
+                             int(bool(causal)),
                              None if m is None else _ptr(m, ctypes.c_ubyte), mh, tile, rp, nr,
                              _ptr(o, ctypes.c_double), _ptr(lse, ctypes.c_double),
                              _threads(nthreads))
@@ -136,21 +143,23 @@ def backward(q, k, v, do, scale, causal=False, block_mask=None, tile=TILE, qrows
              krows=None, nthreads=None):
     """dQ, dK, dV of sum(O * dO) for O = softmax(scale*QK^T + mask) V, fp64.
 
-    qrows / krows: optional query / key rows evaluated in every head.
-    Returns dq [B,H,Rq,d], dk [B,H,Rk,d], dv [B,H,Rk,d].
+    qrows / krows: optional query / key rows evaluated in every head.  With
+    k, v of Hkv < H heads, dk and dv sum over the query heads of each group.
+    Returns dq [B,H,Rq,d], dk [B,Hkv,Rk,d], dv [B,Hkv,Rk,d].
     """
     q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
     B, H, N, d = q.shape
+    Hkv = k.shape[1]
     m, mh, keep = _mask_args(block_mask, H)
     qp, nq, keep_q = _rows(qrows)
     kp, nk, keep_k = _rows(krows)
     Rq = N if qrows is None else nq
     Rk = N if krows is None else nk
     dq = np.zeros((B, H, Rq, d))
-    dk = np.zeros((B, H, Rk, d))
-    dv = np.zeros((B, H, Rk, d))
+    dk = np.zeros((B, Hkv, Rk, d))
+    dv = np.zeros((B, Hkv, Rk, d))
     st = _load().fao_backward(_ptr(q, ctypes.c_double), _ptr(k, ctypes.c_double),
-                              _ptr(v, ctypes.c_double), _ptr(do, ctypes.c_double), B, H, N, d,
+                              _ptr(v, ctypes.c_double), _ptr(do, ctypes.c_double), B, H, Hkv, N, d,
                               float(scale), int(bool(causal)),
                               None if m is None else _ptr(m, ctypes.c_ubyte), mh, tile, qp, nq, kp,
                               nk, _ptr(dq, ctypes.c_double), _ptr(dk, ctypes.c_double),

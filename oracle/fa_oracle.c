@@ -29,6 +29,12 @@
  * A row with no allowed key has O_i = 0, lse_i = -inf and contributes nothing
  * to any gradient (reading taken where the pages are silent).
  *
+ * Grouped key/value heads (the multi-head-attention variants the summary's
+ * "Future Directions" section lists): with Hkv key/value heads and H query
+ * heads, query head h reads key/value head h / (H / Hkv).  A shared key or
+ * value row gets the sum of the gradients of every query head that reads it
+ * (chain rule over the shared parameter).  Hkv = H is ordinary attention.
+ *
  * Every loop is a straight restatement of a sum in the definition, in fp64,
  * summed in index order.  Work is split over independent (head, row-block)
  * units with POSIX threads; that changes nothing in any sum.
@@ -41,13 +47,20 @@
 #include <string.h>
 
 typedef struct {
-  const double *q, *k, *v, *dO;
+  const double *q, *k, *v, *dO; /* q, dO: [B,H,N,d];  k, v: [B,Hkv,N,d] */
   long B, H, N, d;
   double scale;
   int causal;
   const unsigned char *mask; /* [mask_heads, nT, nT] or NULL */
   long mask_heads, tile, nT;
+  long Hkv;
 } problem_t;
+
+/* (batch, key/value head) slice that query slice bh reads */
+static long kv_slice(const problem_t *p, long bh) {
+  long b = bh / p->H, h = bh % p->H;
+  return b * p->Hkv + h / (p->H / p->Hkv);
+}
 
 static int allowed(const problem_t *p, long h, long i, long j) {
   if (j < 0 || j >= p->N || i < 0 || i >= p->N) return 0;
@@ -113,8 +126,8 @@ static void parallel_for(long n, unit_fn fn, void *ctx, int nthreads) {
 static double row_forward(const problem_t *p, long bh, long i, double *o_row) {
   long h = bh % p->H;
   const double *qi = p->q + (bh * p->N + i) * p->d;
-  const double *K = p->k + bh * p->N * p->d;
-  const double *V = p->v + bh * p->N * p->d;
+  const double *K = p->k + kv_slice(p, bh) * p->N * p->d;
+  const double *V = p->v + kv_slice(p, bh) * p->N * p->d;
   /* m_i = max over allowed j of s_ij */
   double m = -INFINITY;
   long cnt = 0;
@@ -153,8 +166,8 @@ static double row_delta(const problem_t *p, long bh, long i, double lse) {
   long h = bh % p->H;
   const double *qi = p->q + (bh * p->N + i) * p->d;
   const double *doi = p->dO + (bh * p->N + i) * p->d;
-  const double *K = p->k + bh * p->N * p->d;
-  const double *V = p->v + bh * p->N * p->d;
+  const double *K = p->k + kv_slice(p, bh) * p->N * p->d;
+  const double *V = p->v + kv_slice(p, bh) * p->N * p->d;
   double D = 0.0;
   for (long j = 0; j < p->N; ++j) {
     if (!allowed(p, h, i, j)) continue;
@@ -190,6 +203,7 @@ static void fwd_unit(void *vctx, long unit) {
 
 static int check_problem(const problem_t *p) {
   if (p->B < 1 || p->H < 1 || p->N < 1 || p->d < 1) return 1;
+  if (p->Hkv < 1 || p->H % p->Hkv != 0) return 1;
   if (!isfinite(p->scale)) return 1;
   if (p->mask && (p->tile < 1 || (p->mask_heads != 1 && p->mask_heads != p->H))) return 1;
   return 0;
@@ -197,10 +211,11 @@ static int check_problem(const problem_t *p) {
 
 /* Forward over all rows (rows == NULL, nrows ignored) or the listed rows of
  * every head.  o: [B,H,nrows,d], lse: [B,H,nrows]. */
-int fao_forward(const double *q, const double *k, const double *v, long B, long H, long N, long d,
-                double scale, int causal, const unsigned char *mask, long mask_heads, long tile,
-                const long *rows, long nrows, double *o, double *lse, int nthreads) {
-  problem_t p = {q, k, v, NULL, B, H, N, d, scale, causal, mask, mask_heads, tile, 0};
+int fao_forward(const double *q, const double *k, const double *v, long B, long H, long Hkv,
+                long N, long d, double scale, int causal, const unsigned char *mask,
+                long mask_heads, long tile, const long *rows, long nrows, double *o, double *lse,
+                int nthreads) {
+  problem_t p = {q, k, v, NULL, B, H, N, d, scale, causal, mask, mask_heads, tile, 0, Hkv};
   if (mask) p.nT = (N + tile - 1) / tile;
   if (check_problem(&p)) return 1;
   if (!rows) nrows = N;
@@ -247,8 +262,8 @@ static void bwd_dq_unit(void *vctx, long unit) {
   long r0 = (unit % c->upH_q) * c->rows_per_unit;
   long r1 = r0 + c->rows_per_unit;
   if (r1 > c->nq) r1 = c->nq;
-  const double *K = p->k + bh * p->N * p->d;
-  const double *V = p->v + bh * p->N * p->d;
+  const double *K = p->k + kv_slice(p, bh) * p->N * p->d;
+  const double *V = p->v + kv_slice(p, bh) * p->N * p->d;
   for (long r = r0; r < r1; ++r) {
     long i = c->qrows ? c->qrows[r] : r;
     double *dqi = c->dq + (bh * c->nq + r) * p->d;
@@ -267,46 +282,51 @@ static void bwd_dq_unit(void *vctx, long unit) {
   }
 }
 
-/* dK_j = scale * sum_i dS_ij q_i,  dV_j = sum_i P_ij dO_i */
+/* dK_j = scale * sum_i dS_ij q_i,  dV_j = sum_i P_ij dO_i, summed over every
+ * query head that reads key/value head j belongs to */
 static void bwd_dkdv_unit(void *vctx, long unit) {
   bwd_ctx_t *c = (bwd_ctx_t *)vctx;
   const problem_t *p = c->p;
-  long bh = unit / c->upH_k, h = bh % p->H;
+  long bkv = unit / c->upH_k;             /* b * Hkv + kv head */
+  long b = bkv / p->Hkv, kvh = bkv % p->Hkv, G = p->H / p->Hkv;
   long r0 = (unit % c->upH_k) * c->rows_per_unit;
   long r1 = r0 + c->rows_per_unit;
   if (r1 > c->nk) r1 = c->nk;
-  const double *Q = p->q + bh * p->N * p->d;
-  const double *dO = p->dO + bh * p->N * p->d;
   for (long r = r0; r < r1; ++r) {
     long j = c->krows ? c->krows[r] : r;
-    double *dkj = c->dk + (bh * c->nk + r) * p->d;
-    double *dvj = c->dv + (bh * c->nk + r) * p->d;
+    double *dkj = c->dk + (bkv * c->nk + r) * p->d;
+    double *dvj = c->dv + (bkv * c->nk + r) * p->d;
     memset(dkj, 0, sizeof(double) * p->d);
     memset(dvj, 0, sizeof(double) * p->d);
-    const double *kj = p->k + (bh * p->N + j) * p->d;
-    const double *vj = p->v + (bh * p->N + j) * p->d;
-    for (long i = 0; i < p->N; ++i) {
-      if (!allowed(p, h, i, j)) continue;
-      double lse = c->lse_all[bh * p->N + i], D = c->D_all[bh * p->N + i];
-      double pij = exp(p->scale * dot(Q + i * p->d, kj, p->d) - lse);
-      double dpij = dot(dO + i * p->d, vj, p->d);
-      double dsij = pij * (dpij - D);
-      for (long cc = 0; cc < p->d; ++cc) {
-        dkj[cc] += p->scale * dsij * Q[i * p->d + cc];
-        dvj[cc] += pij * dO[i * p->d + cc];
+    const double *kj = p->k + (bkv * p->N + j) * p->d;
+    const double *vj = p->v + (bkv * p->N + j) * p->d;
+    for (long g = 0; g < G; ++g) {
+      long h = kvh * G + g, bh = b * p->H + h;
+      const double *Q = p->q + bh * p->N * p->d;
+      const double *dO = p->dO + bh * p->N * p->d;
+      for (long i = 0; i < p->N; ++i) {
+        if (!allowed(p, h, i, j)) continue;
+        double lse = c->lse_all[bh * p->N + i], D = c->D_all[bh * p->N + i];
+        double pij = exp(p->scale * dot(Q + i * p->d, kj, p->d) - lse);
+        double dpij = dot(dO + i * p->d, vj, p->d);
+        double dsij = pij * (dpij - D);
+        for (long cc = 0; cc < p->d; ++cc) {
+          dkj[cc] += p->scale * dsij * Q[i * p->d + cc];
+          dvj[cc] += pij * dO[i * p->d + cc];
+        }
       }
     }
   }
 }
 
 /* Backward for the listed query rows (dq: [B,H,nq,d]) and key rows
- * (dk, dv: [B,H,nk,d]); a NULL row list means every row (nq / nk ignored).
+ * (dk, dv: [B,Hkv,nk,d]); a NULL row list means every row (nq / nk ignored).
  * Only the rows whose statistics a requested gradient needs are evaluated. */
 int fao_backward(const double *q, const double *k, const double *v, const double *dO, long B,
-                 long H, long N, long d, double scale, int causal, const unsigned char *mask,
-                 long mask_heads, long tile, const long *qrows, long nq, const long *krows,
-                 long nk, double *dq, double *dk, double *dv, int nthreads) {
-  problem_t p = {q, k, v, dO, B, H, N, d, scale, causal, mask, mask_heads, tile, 0};
+                 long H, long Hkv, long N, long d, double scale, int causal,
+                 const unsigned char *mask, long mask_heads, long tile, const long *qrows, long nq,
+                 const long *krows, long nk, double *dq, double *dk, double *dv, int nthreads) {
+  problem_t p = {q, k, v, dO, B, H, N, d, scale, causal, mask, mask_heads, tile, 0, Hkv};
   if (mask) p.nT = (N + tile - 1) / tile;
   if (check_problem(&p)) return 1;
   if (!qrows) nq = N;
@@ -353,7 +373,7 @@ int fao_backward(const double *q, const double *k, const double *v, const double
   c.dv = dv;
   parallel_for(B * H * c.upH_stats, bwd_stats_unit, &c, nthreads);
   if (dq && c.upH_q) parallel_for(B * H * c.upH_q, bwd_dq_unit, &c, nthreads);
-  if (dk && dv && c.upH_k) parallel_for(B * H * c.upH_k, bwd_dkdv_unit, &c, nthreads);
+  if (dk && dv && c.upH_k) parallel_for(B * Hkv * c.upH_k, bwd_dkdv_unit, &c, nthreads);
   free(need);
   free(lse_all);
   free(D_all);

@@ -324,3 +324,58 @@ def test_tile_counts_closed_forms(N):
     assert dense[0].tolist() == [n] * n
     assert causal[0].tolist() == list(range(1, n + 1))
     assert int(causal.sum()) == n * (n + 1) // 2
+
+
+# --------------------------------------------------------------------------
+# grouped key/value heads (H query heads share Hkv key/value heads)
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_grouped_kv_equals_repeated_kv(causal):
+    rng = np.random.default_rng(14)
+    B, H, Hkv, N, d = 2, 6, 2, 19, 5
+    G = H // Hkv
+    q, do = _rand(rng, B, H, N, d), _rand(rng, B, H, N, d)
+    k, v = _rand(rng, B, Hkv, N, d), _rand(rng, B, Hkv, N, d)
+    kr, vr = np.repeat(k, G, axis=1), np.repeat(v, G, axis=1)
+    o, lse = oracle.forward(q, k, v, 0.45, causal=causal)
+    o_r, lse_r = oracle.forward(q, kr, vr, 0.45, causal=causal)
+    np.testing.assert_allclose(o, o_r, atol=1e-14)
+    np.testing.assert_allclose(lse, lse_r, atol=1e-14)
+    dq, dk, dv = oracle.backward(q, k, v, do, 0.45, causal=causal)
+    dq_r, dk_r, dv_r = oracle.backward(q, kr, vr, do, 0.45, causal=causal)
+    np.testing.assert_allclose(dq, dq_r, atol=1e-13)
+    # a shared parameter's gradient is the sum over its uses
+    np.testing.assert_allclose(dk, dk_r.reshape(B, Hkv, G, N, d).sum(axis=2), atol=1e-13)
+    np.testing.assert_allclose(dv, dv_r.reshape(B, Hkv, G, N, d).sum(axis=2), atol=1e-13)
+
+
+def test_grouped_kv_gradients_match_central_differences():
+    rng = np.random.default_rng(15)
+    B, H, Hkv, N, d = 1, 4, 1, 9, 3
+    q, do = _rand(rng, B, H, N, d), _rand(rng, B, H, N, d)
+    k, v = _rand(rng, B, Hkv, N, d), _rand(rng, B, Hkv, N, d)
+    dq, dk, dv = oracle.backward(q, k, v, do, 0.6, causal=True, nthreads=1)
+    h = 1e-5
+
+    def loss():
+        o, _ = oracle.forward(q, k, v, 0.6, causal=True, nthreads=1)
+        return float(np.sum(o * do))
+
+    for x, g in ((k, dk), (v, dv)):
+        fd = np.zeros_like(x)
+        for idx in np.ndindex(*x.shape):
+            old = x[idx]
+            x[idx] = old + h
+            lp = loss()
+            x[idx] = old - h
+            lm = loss()
+            x[idx] = old
+            fd[idx] = (lp - lm) / (2 * h)
+        assert np.max(np.abs(fd - g)) / max(1.0, np.max(np.abs(g))) < 1e-6
+
+
+def test_grouped_kv_rejects_bad_groups():
+    rng = np.random.default_rng(16)
+    q, k = _rand(rng, 1, 4, 8, 2), _rand(rng, 1, 3, 8, 2)
+    with pytest.raises(ValueError):
+        oracle.forward(q, k, k, 1.0)
