@@ -133,6 +133,26 @@ fa_status fa_backward_noalloc(const void* q, const void* k, const void* v, const
                               const void* dO, const float* lse, void* dq, void* dk, void* dv, int B,
                               int H, int N, int d, float scale, int causal, cudaStream_t stream);
 
+/*
+ * Grouped key/value heads (multi-head-attention variants, hackmd summary,
+ * "Future Directions": multi-query / grouped-query attention).  H query
+ * heads share Hkv key/value heads, H % Hkv == 0 (Hkv = 1: one key/value
+ * head for all); query head h reads key/value head h / (H / Hkv).
+ *   q, o, dO, dq  bf16 [B, H, N, d];   lse fp32 [B, H, N]
+ *   k, v, dk, dv  bf16 [B, Hkv, N, d]; dk, dv sum over the H / Hkv query
+ *                 heads that read each key/value head
+ * Workspace as fa_backward_workspace_size(B, H, N, d).  Other rules as
+ * fa_forward / fa_backward; Hkv outside [1, H] or not dividing H gives
+ * FA_ERR_INVALID_ARG.
+ */
+fa_status fa_forward_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                         int H, int Hkv, int N, int d, float scale, int causal,
+                         cudaStream_t stream);
+fa_status fa_backward_gqa(const void* q, const void* k, const void* v, const void* o,
+                          const void* dO, const float* lse, void* dq, void* dk, void* dv, int B,
+                          int H, int Hkv, int N, int d, float scale, int causal, void* workspace,
+                          size_t workspace_bytes, cudaStream_t stream);
+
 /* Bytes of workspace the block-sparse calls need: the CSR and CSC tile
  * lists of the mask (4 * mask_heads * (2*(nT+1) + 2*nT*nT) bytes) followed
  * by the fa_backward workspace.  The forward uses only the list part. */

@@ -30,7 +30,8 @@ EXPORTS = (
     "fa_backward_preprocess", "fa_backward_main", "fa_backward_dq_convert", "fa_backward_noalloc",
     "fa_blocksparse_workspace_size", "fa_blocksparse_build_lists", "fa_blocksparse_forward",
     "fa_blocksparse_backward", "fa_get_device_status", "fa_set_wait_limit_ns",
-    "fa_debug_wait_timeout", "fa_debug_schedule", "fa_debug_mma_probe",
+    "fa_debug_wait_timeout", "fa_debug_schedule", "fa_debug_mma_probe", "fa_forward_gqa",
+    "fa_backward_gqa",
 )
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -83,6 +84,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
             "fa_debug_wait_timeout": ([U, P], I),
             "fa_debug_schedule": ([I, I, P, I, P, Z, P, P, P, P, P], I),
             "fa_debug_mma_probe": ([P, P, P, I, I, P], I),
+            "fa_forward_gqa": ([P, P, P, P, P, I, I, I, I, I, F, I, P], I),
+            "fa_backward_gqa": ([P, P, P, P, P, P, P, P, P, I, I, I, I, I, F, I, P, Z, P], I),
         }
         for name, (args, res) in sig.items():
             fn = getattr(lib, name)
@@ -122,6 +125,18 @@ def fa_status_string(status: int) -> str:
 def fa_forward(q, k, v, o, lse, B, H, N, d, scale, causal, stream=None) -> int:
     return load().fa_forward(_p(q), _p(k), _p(v), _p(o), _p(lse), B, H, N, d, float(scale),
                              int(bool(causal)), _s(stream))
+
+
+def fa_forward_gqa(q, k, v, o, lse, B, H, Hkv, N, d, scale, causal, stream=None) -> int:
+    return load().fa_forward_gqa(_p(q), _p(k), _p(v), _p(o), _p(lse), B, H, Hkv, N, d,
+                                 float(scale), int(bool(causal)), _s(stream))
+
+
+def fa_backward_gqa(q, k, v, o, dO, lse, dq, dk, dv, B, H, Hkv, N, d, scale, causal, workspace,
+                    workspace_bytes, stream=None) -> int:
+    return load().fa_backward_gqa(_p(q), _p(k), _p(v), _p(o), _p(dO), _p(lse), _p(dq), _p(dk),
+                                  _p(dv), B, H, Hkv, N, d, float(scale), int(bool(causal)),
+                                  _p(workspace), int(workspace_bytes), _s(stream))
 
 
 def fa_backward_workspace_size(B, H, N, d) -> int:

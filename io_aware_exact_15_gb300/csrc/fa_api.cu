@@ -169,20 +169,21 @@ fa_status check_mask(const uint8_t* mask, int mask_heads, int H, int N) {
 }
 
 fa_status forward_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B,
-                       int H, int N, int d, float scale, int causal, const fa::TileLists* lists,
-                       cudaStream_t stream) {
+                       int H, int Hkv, int N, int d, float scale, int causal,
+                       const fa::TileLists* lists, cudaStream_t stream) {
   fa_status st = FA_OK;
   int* err = status_word(&st);
   if (!err) return st;
   CUtensorMap tq, tk, tv;
-  if (!fa::make_tile_map(&tq, q, B * H, N, d) || !fa::make_tile_map(&tk, k, B * H, N, d) ||
-      !fa::make_tile_map(&tv, v, B * H, N, d))
+  if (!fa::make_tile_map(&tq, q, B * H, N, d) || !fa::make_tile_map(&tk, k, B * Hkv, N, d) ||
+      !fa::make_tile_map(&tv, v, B * Hkv, N, d))
     return FA_ERR_CUDA;
   fa::FwdParams p;
   p.o = o;
   p.lse = lse;
   p.B = B;
   p.H = H;
+  p.Hkv = Hkv;
   p.N = N;
   p.d = d;
   p.scale = scale;
@@ -195,15 +196,15 @@ fa_status forward_impl(const void* q, const void* k, const void* v, void* o, flo
 }
 
 fa_status backward_main_impl(const void* q, const void* k, const void* v, const void* dO,
-                             const float* lse, void* dk, void* dv, int B, int H, int N, int d,
-                             float scale, int causal, const BwdWorkspace& w,
+                             const float* lse, void* dk, void* dv, int B, int H, int Hkv, int N,
+                             int d, float scale, int causal, const BwdWorkspace& w,
                              const fa::TileLists* lists, cudaStream_t stream) {
   fa_status st = FA_OK;
   int* err = status_word(&st);
   if (!err) return st;
   CUtensorMap tq, tk, tv, tdo, tdq;
-  if (!fa::make_tile_map(&tq, q, B * H, N, d) || !fa::make_tile_map(&tk, k, B * H, N, d) ||
-      !fa::make_tile_map(&tv, v, B * H, N, d) || !fa::make_tile_map(&tdo, dO, B * H, N, d) ||
+  if (!fa::make_tile_map(&tq, q, B * H, N, d) || !fa::make_tile_map(&tk, k, B * Hkv, N, d) ||
+      !fa::make_tile_map(&tv, v, B * Hkv, N, d) || !fa::make_tile_map(&tdo, dO, B * H, N, d) ||
       !fa::make_acc_map(&tdq, w.dq_acc, B * H, N, d))
     return FA_ERR_CUDA;
   fa::BwdParams p;
@@ -214,6 +215,7 @@ fa_status backward_main_impl(const void* q, const void* k, const void* v, const 
   p.dv = dv;
   p.B = B;
   p.H = H;
+  p.Hkv = Hkv;
   p.N = N;
   p.d = d;
   p.scale = scale;
@@ -244,6 +246,11 @@ fa_status check_bwd_args(const void* q, const void* k, const void* v, const void
                         static_cast<const void*>(dv)})
     FA_TRY(check_ptr16(p));
   FA_TRY(check_ptr4(lse));
+  return FA_OK;
+}
+
+fa_status check_groups(int H, int Hkv) {
+  if (Hkv < 1 || Hkv > H || H % Hkv != 0) return FA_ERR_INVALID_ARG;
   return FA_OK;
 }
 
@@ -303,7 +310,15 @@ const char* fa_status_string(fa_status s) {
 fa_status fa_forward(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                      int N, int d, float scale, int causal, cudaStream_t stream) {
   FA_TRY(check_fwd_args(q, k, v, o, lse, B, H, N, d, scale));
-  return forward_impl(q, k, v, o, lse, B, H, N, d, scale, causal, nullptr, stream);
+  return forward_impl(q, k, v, o, lse, B, H, H, N, d, scale, causal, nullptr, stream);
+}
+
+fa_status fa_forward_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                         int H, int Hkv, int N, int d, float scale, int causal,
+                         cudaStream_t stream) {
+  FA_TRY(check_fwd_args(q, k, v, o, lse, B, H, N, d, scale));
+  FA_TRY(check_groups(H, Hkv));
+  return forward_impl(q, k, v, o, lse, B, H, Hkv, N, d, scale, causal, nullptr, stream);
 }
 
 size_t fa_backward_workspace_size(int B, int H, int N, int d) {
@@ -332,7 +347,7 @@ fa_status fa_backward_main(const void* q, const void* k, const void* v, const vo
     FA_TRY(check_ptr16(p));
   FA_TRY(check_ptr4(lse));
   FA_TRY(check_ws(workspace, workspace_bytes, bwd_ws_bytes(B, H, N, d)));
-  return backward_main_impl(q, k, v, dO, lse, dk, dv, B, H, N, d, scale, causal,
+  return backward_main_impl(q, k, v, dO, lse, dk, dv, B, H, H, N, d, scale, causal,
                             bwd_ws(workspace, B, H, N), nullptr, stream);
 }
 
@@ -358,6 +373,19 @@ fa_status fa_backward(const void* q, const void* k, const void* v, const void* o
   return fa_backward_dq_convert(dq, B, H, N, d, scale, workspace, workspace_bytes, stream);
 }
 
+fa_status fa_backward_gqa(const void* q, const void* k, const void* v, const void* o,
+                          const void* dO, const float* lse, void* dq, void* dk, void* dv, int B,
+                          int H, int Hkv, int N, int d, float scale, int causal, void* workspace,
+                          size_t workspace_bytes, cudaStream_t stream) {
+  FA_TRY(check_bwd_args(q, k, v, o, dO, lse, dq, dk, dv, B, H, N, d, scale));
+  FA_TRY(check_groups(H, Hkv));
+  FA_TRY(check_ws(workspace, workspace_bytes, bwd_ws_bytes(B, H, N, d)));
+  FA_TRY(fa_backward_preprocess(o, dO, B, H, N, d, workspace, workspace_bytes, stream));
+  FA_TRY(backward_main_impl(q, k, v, dO, lse, dk, dv, B, H, Hkv, N, d, scale, causal,
+                            bwd_ws(workspace, B, H, N), nullptr, stream));
+  return fa_backward_dq_convert(dq, B, H, N, d, scale, workspace, workspace_bytes, stream);
+}
+
 size_t fa_blocksparse_workspace_size(int B, int H, int N, int d, int mask_heads) {
   if (B < 1 || H < 1 || N < 1 || d < 1 || mask_heads < 1) return 0;
   return lists_bytes(N, mask_heads) + bwd_ws_bytes(B, H, N, d);
@@ -380,7 +408,7 @@ fa_status fa_blocksparse_forward(const void* q, const void* k, const void* v, vo
   FA_TRY(check_ws(workspace, workspace_bytes, lists_bytes(N, mask_heads)));
   FA_TRY(build_lists(block_mask, mask_heads, N, workspace, stream));
   const fa::TileLists L = lists_in(workspace, N, mask_heads);
-  return forward_impl(q, k, v, o, lse, B, H, N, d, scale, causal, &L, stream);
+  return forward_impl(q, k, v, o, lse, B, H, H, N, d, scale, causal, &L, stream);
 }
 
 fa_status fa_blocksparse_backward(const void* q, const void* k, const void* v, const void* o,
@@ -397,7 +425,7 @@ fa_status fa_blocksparse_backward(const void* q, const void* k, const void* v, c
   void* bws = static_cast<char*>(workspace) + lb;
   const size_t bws_bytes = workspace_bytes - lb;
   FA_TRY(fa_backward_preprocess(o, dO, B, H, N, d, bws, bws_bytes, stream));
-  FA_TRY(backward_main_impl(q, k, v, dO, lse, dk, dv, B, H, N, d, scale, causal,
+  FA_TRY(backward_main_impl(q, k, v, dO, lse, dk, dv, B, H, H, N, d, scale, causal,
                             bwd_ws(bws, B, H, N), &L, stream));
   return fa_backward_dq_convert(dq, B, H, N, d, scale, bws, bws_bytes, stream);
 }

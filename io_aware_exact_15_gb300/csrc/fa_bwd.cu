@@ -8,8 +8,10 @@
 //   dS = P o (dP - D_i),
 //   dV_j += P^T dO_i,  dK_j += dS^T Q_i,  dQ_i += dS K_j  (dQ, dK scaled later).
 //
-// GB300 design (one CTA = one head x one 128-key tile; K_j, V_j stay in
-// shared memory while the CTA walks the query tiles):
+// GB300 design (one CTA = one key/value head x one 128-key tile; K_j, V_j
+// stay in shared memory while the CTA walks the query tiles of every query
+// head that reads this key/value head, so grouped K/V needs no atomics for
+// dK and dV):
 //   warp 0      TMA producer: K_j, V_j once; Q_i through an NQ-slot ring and
 //               dO_i through an NDO-slot ring (128-byte swizzle)
 //   warp 1      allocates 512 TMEM columns; lane 0 issues the five MMAs
@@ -26,6 +28,8 @@
 // TMEM: S [0,128) dP [128,256) dV [256,256+d) dK [256+d,256+2d);
 //       dQ at [384,448) for d = 64 and over the dP columns for d = 128.
 #include <math.h>
+
+#include <type_traits>
 
 #include "fa_internal.h"
 #include "fa_ptx.cuh"
@@ -64,7 +68,7 @@ struct BwdSmem {
 constexpr int kBwdThreads = 384;
 constexpr float kLog2e = 1.4426950408889634f;
 
-template <int D>
+template <int D, bool GQA>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     fa_bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
@@ -81,10 +85,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int N = p.N;
   const int nT = (N + kTile - 1) / kTile;
-  const int BH = p.B * p.H;
-  int bh, kt;
-  bwd_cta_coords(blockIdx.x, BH, nT, p.causal != 0, bh, kt);
-  const int head = bh % p.H;
+  // one CTA = one key/value head x one key tile; with grouped K/V it walks
+  // the query tiles of every query head of its group (G = H / Hkv)
+  // (the plain instantiation, GQA = false, carries no group arithmetic)
+  const int Hkv = GQA ? p.Hkv : p.H;
+  const int G = GQA ? p.H / p.Hkv : 1;
+  int bkv, kt;
+  bwd_cta_coords(blockIdx.x, p.B * Hkv, nT, p.causal != 0, bkv, kt);
+  // first query slice of the group
+  const int bq0 = GQA ? (bkv / Hkv) * p.H + (bkv % Hkv) * G : bkv;
 
   if (threadIdx.x == 0) {
     mbar_init(bar(L::B_KV), 1);
@@ -116,8 +125,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const WaitCtl wc{abort_flag, p.err, p.wait_ns};
 
-  BwdSchedule sch;
-  sch.init(kt, nT, p.causal != 0, p.lists, head);
+  typename std::conditional<GQA, BwdGroupSchedule, BwdSingleSchedule>::type sch;
+  sch.init(kt, nT, p.causal != 0, p.lists, bq0 % p.H, G);
 
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer
@@ -130,13 +139,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_arrive_expect_tx(bar(L::B_KV), 2 * L::TILE);
 #pragma unroll
       for (int c = 0; c < L::CH; ++c) {
-        tma_load_3d(sb + L::K + c * L::CHUNK, &tk, bar(L::B_KV), 64 * c, kt * kTile, bh);
-        tma_load_3d(sb + L::V + c * L::CHUNK, &tv, bar(L::B_KV), 64 * c, kt * kTile, bh);
+        tma_load_3d(sb + L::K + c * L::CHUNK, &tk, bar(L::B_KV), 64 * c, kt * kTile, bkv);
+        tma_load_3d(sb + L::V + c * L::CHUNK, &tv, bar(L::B_KV), 64 * c, kt * kTile, bkv);
       }
       uint32_t nq = 0, nd = 0;  // Q / dO copies issued
       bool ok = true;
-      int qt;
-      while (ok && sch.next(qt)) {
+      int qt, g;
+      while (ok && sch.next(qt, g, p.lists)) {
         const int qpos = nq % L::NQ, dpos = nd % L::NDO;
         const uint32_t qround = nq / L::NQ, dround = nd / L::NDO;
         if (qround > 0 && !wait_bar(bar(L::B_QE + qpos), (qround - 1) & 1, wc)) {
@@ -147,7 +156,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
         for (int c = 0; c < L::CH; ++c)
           tma_load_3d(sb + L::QR + qpos * L::TILE + c * L::CHUNK, &tq, bar(L::B_QF + qpos), 64 * c,
-                      qt * kTile, bh);
+                      qt * kTile, bq0 + g);
         ++nq;
         if (dround > 0 && !wait_bar(bar(L::B_DOE + dpos), (dround - 1) & 1, wc)) {
           ok = false;
@@ -157,7 +166,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
         for (int c = 0; c < L::CH; ++c)
           tma_load_3d(sb + L::DOR + dpos * L::TILE + c * L::CHUNK, &tdo, bar(L::B_DOF + dpos),
-                      64 * c, qt * kTile, bh);
+                      64 * c, qt * kTile, bq0 + g);
         ++nd;
       }
       // let copies still in flight land before the CTA can exit
@@ -211,9 +220,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       };
       const uint32_t tS = tmem + L::T_S, tDP = tmem + L::T_DP, tDV = tmem + L::T_DV,
                      tDK = tmem + L::T_DK, tDQ = tmem + L::T_DQ;
-      int qt, qt_n;
+      int qt, qt_n, g_unused;
       bool ok = wait_bar(bar(L::B_KV), 0, wc);
-      bool have = sch.next(qt);
+      bool have = sch.next(qt, g_unused, p.lists);
       uint32_t n = 0;
       if (ok && have) {
         ok = wait_bar(bar(L::B_QF + 0), 0, wc);
@@ -230,7 +239,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
       }
       while (ok && have) {
-        const bool have_n = sch.next(qt_n);
+        const bool have_n = sch.next(qt_n, g_unused, p.lists);
         const uint32_t qpos = n % L::NQ, dpos = n % L::NDO;
         const uint32_t n1 = n + 1;
         // dV += P^T dO_i once P is in shared memory, interleaved with the
@@ -319,19 +328,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int kcol0 = kbase + 64 * half;  // first key of this thread's columns
     bool ok = true;
     uint32_t n = 0;
-    int qt = 0, qt_prev = 0;
-    bool have = sch.next(qt);
-    auto load_stats = [&](int t, float& l_, float& d_) {
+    int qt = 0, qt_prev = 0, g = 0, g_prev = 0;
+    bool have = sch.next(qt, g, p.lists);
+    auto load_stats = [&](int t, int gg, float& l_, float& d_) {
       const int row = t * kTile + r;
-      const size_t idx = static_cast<size_t>(bh) * N + (row < N ? row : 0);
+      const size_t idx = static_cast<size_t>(bq0 + gg) * N + (row < N ? row : 0);
       l_ = p.lse[idx];
       d_ = p.delta[idx];
     };
     float lse_c = 0.f, dlt_c = 0.f;
-    if (have) load_stats(qt, lse_c, dlt_c);
+    if (have) load_stats(qt, g, lse_c, dlt_c);
     // dQ of query tile t (step m): TMEM -> registers, release the columns,
     // then add this thread's D/2 columns into the fp32 accumulator
-    auto drain_dq = [&](uint32_t m, int t) -> bool {
+    auto drain_dq = [&](uint32_t m, int t, int gg) -> bool {
       if (!__all_sync(0xffffffffu, wait_bar(bar(L::B_DQF), m & 1, wc))) return false;
       tc_fence_after();
       uint32_t dq[D / 64][32];
@@ -360,7 +369,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         fence_async_smem();
         __syncwarp();
         if (lane == 0) {
-          tma_reduce_add_3d(&tdq, stage, (D / 2) * half + 32 * c, t * kTile + 32 * q4, bh);
+          tma_reduce_add_3d(&tdq, stage, (D / 2) * half + 32 * c, t * kTile + 32 * q4, bq0 + gg);
           bulk_commit();
         }
       }
@@ -370,10 +379,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       return true;
     };
     while (ok && have) {
-      int qt_n = 0;
-      const bool have_n = sch.next(qt_n);
+      int qt_n = 0, g_n = 0;
+      const bool have_n = sch.next(qt_n, g_n, p.lists);
       float lse_n = 0.f, dlt_n = 0.f;
-      if (have_n) load_stats(qt_n, lse_n, dlt_n);  // prefetch the next tile's statistics
+      if (have_n) load_stats(qt_n, g_n, lse_n, dlt_n);  // prefetch the next tile's statistics
       const int qrow = qt * kTile + r;
       const bool live = qrow < N && lse_c != -INFINITY;
       const float lse2 = live ? lse_c * kLog2e : 0.f;
@@ -410,7 +419,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       fence_async_smem();
       tc_fence_before();
       mbar_arrive(bar(L::B_PR));
-      if (n > 0 && !drain_dq(n - 1, qt_prev)) {
+      if (n > 0 && !drain_dq(n - 1, qt_prev, g_prev)) {
         ok = false;
         break;
       }
@@ -441,13 +450,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tc_fence_before();
       mbar_arrive(bar(L::B_DSR));
       qt_prev = qt;
+      g_prev = g;
       qt = qt_n;
+      g = g_n;
       have = have_n;
       lse_c = lse_n;
       dlt_c = dlt_n;
       ++n;
     }
-    if (ok && n > 0) ok = drain_dq(n - 1, qt_prev);
+    if (ok && n > 0) ok = drain_dq(n - 1, qt_prev, g_prev);
     if (lane == 0) bulk_wait_all();  // every dQ reduce of this warp has landed
     // ---------------------------------------------------- epilogue: dV, dK
     // warps 4-7 write dV_j, warps 8-11 write scale * dK_j (thread = key row)
@@ -459,7 +470,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const uint32_t tcol = dv_side ? L::T_DV : L::T_DK;
       const float mul = dv_side ? 1.f : p.scale;
       uint8_t* dst = static_cast<uint8_t*>(dv_side ? p.dv : p.dk) +
-                     (static_cast<size_t>(bh) * N + (key < N ? key : 0)) * static_cast<size_t>(D) * 2;
+                     (static_cast<size_t>(bkv) * N + (key < N ? key : 0)) * static_cast<size_t>(D) * 2;
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t a[32];
@@ -494,18 +505,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
 }
 
-template <int D>
+template <int D, bool GQA>
 cudaError_t launch_bwd_d(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                          const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq,
                          cudaStream_t stream) {
   using L = BwdSmem<D>;
-  cudaError_t e = cudaFuncSetAttribute(fa_bwd_kernel<D>,
+  cudaError_t e = cudaFuncSetAttribute(fa_bwd_kernel<D, GQA>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
   if (e != cudaSuccess) return e;
   const int nT = (p.N + kTile - 1) / kTile;
-  const long long ctas = static_cast<long long>(nT) * p.B * p.H;
-  fa_bwd_kernel<D><<<static_cast<unsigned>(ctas), kBwdThreads, L::ALLOC, stream>>>(tq, tk, tv, tdo,
-                                                                                   tdq, p);
+  const long long ctas = static_cast<long long>(nT) * p.B * (p.Hkv > 0 ? p.Hkv : p.H);
+  fa_bwd_kernel<D, GQA><<<static_cast<unsigned>(ctas), kBwdThreads, L::ALLOC, stream>>>(
+      tq, tk, tv, tdo, tdq, p);
   return cudaGetLastError();
 }
 
@@ -514,8 +525,13 @@ cudaError_t launch_bwd_d(const BwdParams& p, const CUtensorMap& tq, const CUtens
 cudaError_t launch_backward_main(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                                  const CUtensorMap& tv, const CUtensorMap& tdo,
                                  const CUtensorMap& tdq, cudaStream_t stream) {
-  if (p.d == 64) return launch_bwd_d<64>(p, tq, tk, tv, tdo, tdq, stream);
-  if (p.d == 128) return launch_bwd_d<128>(p, tq, tk, tv, tdo, tdq, stream);
+  const bool gqa = p.Hkv > 0 && p.Hkv != p.H;
+  if (p.d == 64)
+    return gqa ? launch_bwd_d<64, true>(p, tq, tk, tv, tdo, tdq, stream)
+               : launch_bwd_d<64, false>(p, tq, tk, tv, tdo, tdq, stream);
+  if (p.d == 128)
+    return gqa ? launch_bwd_d<128, true>(p, tq, tk, tv, tdo, tdq, stream)
+               : launch_bwd_d<128, false>(p, tq, tk, tv, tdo, tdq, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -26,6 +26,7 @@ struct FwdParams {
   void* o = nullptr;      // bf16 [BH, N, d]
   float* lse = nullptr;   // fp32 [BH, N]
   int B = 0, H = 0, N = 0, d = 0;
+  int Hkv = 0;            // key/value heads (H % Hkv == 0); 0 means H
   float scale = 0.f;
   int causal = 0;
   TileLists lists;        // sparse when lists.row_ptr != nullptr
@@ -37,9 +38,10 @@ struct BwdParams {
   const float* lse = nullptr;   // fp32 [BH, N]
   const float* delta = nullptr; // fp32 [BH, N]  D_i = <dO_i, O_i>
   float* dq_acc = nullptr;      // fp32 [BH, N, d] (unscaled sum of dS K)
-  void* dk = nullptr;           // bf16 [BH, N, d]
-  void* dv = nullptr;           // bf16 [BH, N, d]
+  void* dk = nullptr;           // bf16 [B*Hkv, N, d]
+  void* dv = nullptr;           // bf16 [B*Hkv, N, d]
   int B = 0, H = 0, N = 0, d = 0;
+  int Hkv = 0;                  // key/value heads (H % Hkv == 0); 0 means H
   float scale = 0.f;
   int causal = 0;
   TileLists lists;              // sparse when lists.col_ptr != nullptr

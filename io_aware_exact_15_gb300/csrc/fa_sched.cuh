@@ -122,6 +122,49 @@ struct BwdSchedule {
   }
 };
 
+// Backward schedule of a key/value head shared by G query heads (grouped
+// K/V): the query tiles of query head hq0, then those of hq0 + 1, ...  Each
+// step yields (query tile, group member g).  G = 1 is the plain schedule.
+struct BwdGroupSchedule {
+  BwdSchedule s;
+  int g, G, kt, nT, hq0;
+  bool causal;
+
+  FA_DEV void init(int kt_, int nT_, bool causal_, const TileLists& L, int hq0_, int G_) {
+    kt = kt_;
+    nT = nT_;
+    causal = causal_;
+    hq0 = hq0_;
+    G = G_;
+    g = 0;
+    s.init(kt, nT, causal, L, hq0);
+  }
+
+  // L: the same lists init() was given
+  FA_DEV bool next(int& qt, int& gout, const TileLists& L) {
+    for (;;) {
+      if (s.next(qt)) {
+        gout = g;
+        return true;
+      }
+      if (++g >= G) return false;
+      s.init(kt, nT, causal, L, hq0 + g);
+    }
+  }
+};
+
+// The plain schedule behind the grouped interface (a group of one).
+struct BwdSingleSchedule {
+  BwdSchedule s;
+  FA_DEV void init(int kt, int nT, bool causal, const TileLists& L, int head, int) {
+    s.init(kt, nT, causal, L, head);
+  }
+  FA_DEV bool next(int& qt, int& g, const TileLists&) {
+    g = 0;
+    return s.next(qt);
+  }
+};
+
 // CTA index -> (head, query-tile pair) for the forward grid.  Causal CTAs
 // are issued longest-first (largest pair index first, all heads of one rank
 // together); dense CTAs go head by head so a head's K/V stay in L2.

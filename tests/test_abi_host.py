@@ -118,3 +118,13 @@ def test_product_package_does_not_reference_oracle():
                 text = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in text and "from oracle" not in text, f
                 assert "liboracle" not in text and "fa_oracle" not in text, f
+
+
+def test_gqa_rejects_bad_groups():
+    A = ALIGNED
+    need = fa.fa_backward_workspace_size(1, 6, 128, 64)
+    for Hkv in (0, 4, 7, -1):
+        assert fa.fa_forward_gqa(A, A, A, A, A, 1, 6, Hkv, 128, 64, 0.1, 0, 0) == \
+            fa.FA_ERR_INVALID_ARG
+        assert fa.fa_backward_gqa(A, A, A, A, A, A, A, A, A, 1, 6, Hkv, 128, 64, 0.1, 0, A, need,
+                                  0) == fa.FA_ERR_INVALID_ARG
