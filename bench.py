@@ -407,6 +407,58 @@ def run_reference(args, rank, world):
             "gpu_launches": 0}
 
 
+def run_tile_sweep(args):
+    """Block-size experiment: forward time per (rows per CTA, K/V stages),
+    one JSON line each.  DRAM bytes per configuration come from running this
+    mode under ncu (dram__bytes_read.sum + dram__bytes_write.sum)."""
+    import torch
+
+    import fa_workloads as W
+    import io_aware_exact_15_gb300 as fa
+
+    dev = torch.device("cuda", 0)
+    w = W.WORKLOADS[args.workload]
+    B, H, N, d = w.B, w.H, w.N, w.d
+    q, k, v, _, _ = W.make_inputs(w, with_do=False)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    o = torch.empty_like(qd)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    stages = (2, 3, 4, 5) if d == 128 else (2, 4, 8)
+    ff = W.fwd_flops(w)
+    peak = load_peaks()["bf16_tflops"]
+    configs = [(rows, st) for rows in (128, 256) for st in stages]
+    for rows, st in configs + [("default", None)]:
+        def call():
+            if st is None:
+                r = fa.fa_forward(qd, kd, vd, o, lse, B, H, N, d, w.scale, w.causal)
+            else:
+                r = fa.fa_debug_forward_config(qd, kd, vd, o, lse, B, H, N, d, w.scale, w.causal,
+                                               rows, st)
+            if r != fa.FA_OK:
+                raise RuntimeError(fa.fa_status_string(r))
+        for _ in range(args.warmup):
+            call()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(args.steps):
+            call()
+        b.record()
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / args.steps
+        nT = (N + 127) // 128
+        br = 256 if rows == "default" else rows
+        # K and V bytes a CTA streams, times the CTAs (the tile-model IO term)
+        kv_passes = B * H * ((nT + 1) // 2 if br == 256 else nT)
+        print(json.dumps({"sweep": "forward tile configuration", "workload": w.name,
+                          "rows_per_cta": br, "kv_stages": st if st else "fa_forward",
+                          "ms": round(ms, 4), "tflops": round(ff / (ms * 1e-3) / 1e12, 1),
+                          "frac_of_peak": round(ff / (ms * 1e-3) / 1e12 / peak, 4),
+                          "tile_model_kv_bytes": int(kv_passes) * 2 * N * d * 2}), flush=True)
+    if fa.fa_get_device_status() != fa.FA_OK:
+        raise RuntimeError("device status after the sweep")
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -415,7 +467,12 @@ def main():
     ap.add_argument("--workload", default="bert_large")
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--tile-sweep", action="store_true",
+                    help="time the forward per tile configuration (block-size experiment)")
     args = ap.parse_args()
+    if args.tile_sweep:
+        run_tile_sweep(args)
+        return
     if args.warmup < 3:
         args.warmup = 3
     world = int(os.environ.get("WORLD_SIZE", "1"))

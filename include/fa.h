@@ -218,6 +218,21 @@ fa_status fa_debug_schedule(int N, int causal, const uint8_t* block_mask, int ma
                             int* bwd_counts, int* fwd_lists, int* bwd_lists, cudaStream_t stream);
 
 /*
+ * fa_forward with its tile configuration chosen by the caller (the block-size
+ * experiment of the hackmd summary, "IO Complexity Analysis": a larger
+ * row block means fewer passes over K and V).
+ *   rows_per_cta  128 (one query tile per CTA) or 256 (two; fa_forward's
+ *                 choice)
+ *   kv_stages     K/V shared-memory ring depth: 2..5 for d = 128 (5 is
+ *                 fa_forward's), 2, 4 or 8 for d = 64 (8 is fa_forward's)
+ * Dense or causal, no grouped K/V.  Other arguments and results as
+ * fa_forward; unsupported choices give FA_ERR_UNSUPPORTED.
+ */
+fa_status fa_debug_forward_config(const void* q, const void* k, const void* v, void* o,
+                                  float* lse, int B, int H, int N, int d, float scale, int causal,
+                                  int rows_per_cta, int kv_stages, cudaStream_t stream);
+
+/*
  * One-tile tcgen05 check of the operand layouts the kernels use.
  *   mode 0: c[128x128] = a b^T, a and b bf16 [128 x 128]
  *   mode 1: c[128xn]   = a b,   a bf16 [128 x 128], b bf16 [128 x n]

@@ -31,7 +31,7 @@ EXPORTS = (
     "fa_blocksparse_workspace_size", "fa_blocksparse_build_lists", "fa_blocksparse_forward",
     "fa_blocksparse_backward", "fa_get_device_status", "fa_set_wait_limit_ns",
     "fa_debug_wait_timeout", "fa_debug_schedule", "fa_debug_mma_probe", "fa_forward_gqa",
-    "fa_backward_gqa",
+    "fa_backward_gqa", "fa_debug_forward_config",
 )
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -85,6 +85,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
             "fa_debug_schedule": ([I, I, P, I, P, Z, P, P, P, P, P], I),
             "fa_debug_mma_probe": ([P, P, P, I, I, P], I),
             "fa_forward_gqa": ([P, P, P, P, P, I, I, I, I, I, F, I, P], I),
+            "fa_debug_forward_config": ([P, P, P, P, P, I, I, I, I, F, I, I, I, P], I),
             "fa_backward_gqa": ([P, P, P, P, P, P, P, P, P, I, I, I, I, I, F, I, P, Z, P], I),
         }
         for name, (args, res) in sig.items():
@@ -219,6 +220,13 @@ def fa_debug_schedule(N, causal, block_mask, mask_heads, workspace, workspace_by
     return load().fa_debug_schedule(N, int(bool(causal)), _p(block_mask), mask_heads,
                                     _p(workspace), int(workspace_bytes), _p(fwd_counts),
                                     _p(bwd_counts), _p(fwd_lists), _p(bwd_lists), _s(stream))
+
+
+def fa_debug_forward_config(q, k, v, o, lse, B, H, N, d, scale, causal, rows_per_cta,
+                            kv_stages, stream=None) -> int:
+    return load().fa_debug_forward_config(_p(q), _p(k), _p(v), _p(o), _p(lse), B, H, N, d,
+                                          float(scale), int(bool(causal)), int(rows_per_cta),
+                                          int(kv_stages), _s(stream))
 
 
 def fa_debug_mma_probe(a, b, c, mode, n, stream=None) -> int:

@@ -477,6 +477,38 @@ fa_status fa_debug_schedule(int N, int causal, const uint8_t* block_mask, int ma
   return FA_OK;
 }
 
+fa_status fa_debug_forward_config(const void* q, const void* k, const void* v, void* o,
+                                  float* lse, int B, int H, int N, int d, float scale, int causal,
+                                  int rows_per_cta, int kv_stages, cudaStream_t stream) {
+  FA_TRY(check_fwd_args(q, k, v, o, lse, B, H, N, d, scale));
+  if (rows_per_cta != 128 && rows_per_cta != 256) return FA_ERR_UNSUPPORTED;
+  const bool ok_stages = (d == 128) ? (kv_stages >= 2 && kv_stages <= 5)
+                                    : (kv_stages == 2 || kv_stages == 4 || kv_stages == 8);
+  if (!ok_stages) return FA_ERR_UNSUPPORTED;
+  fa_status st = FA_OK;
+  int* err = status_word(&st);
+  if (!err) return st;
+  CUtensorMap tq, tk, tv;
+  if (!fa::make_tile_map(&tq, q, B * H, N, d) || !fa::make_tile_map(&tk, k, B * H, N, d) ||
+      !fa::make_tile_map(&tv, v, B * H, N, d))
+    return FA_ERR_CUDA;
+  fa::FwdParams p;
+  p.o = o;
+  p.lse = lse;
+  p.B = B;
+  p.H = H;
+  p.Hkv = H;
+  p.N = N;
+  p.d = d;
+  p.scale = scale;
+  p.causal = causal ? 1 : 0;
+  p.single_tile = rows_per_cta == 128 ? 1 : 0;
+  p.err = err;
+  p.wait_ns = wait_limit_ns();
+  FA_CUDA(fa::launch_forward_config(p, tq, tk, tv, kv_stages, stream));
+  return FA_OK;
+}
+
 fa_status fa_debug_mma_probe(const void* a, const void* b, float* c, int mode, int n,
                              cudaStream_t stream) {
   if (mode < 0 || mode > 3) return FA_ERR_INVALID_ARG;

@@ -34,12 +34,13 @@
 namespace fa {
 namespace {
 
-template <int D>
+template <int D, int NS_ = 0>
 struct FwdSmem {
   static constexpr int CH = D / 64;             // 128-byte column chunks per row
   static constexpr int CHUNK = kTile * 128;     // [128 rows x 128 B] = 16 KB
   static constexpr int TILE = CH * CHUNK;       // one 128 x D bf16 tile
-  static constexpr int NS = (D == 64) ? 8 : 5;  // K/V ring slots (one tile each)
+  // K/V ring slots (one tile each); NS_ != 0 overrides for the tile sweep
+  static constexpr int NS = NS_ != 0 ? NS_ : ((D == 64) ? 8 : 5);
   static constexpr int Q = 0;
   static constexpr int KV = Q + 2 * TILE;
   static constexpr int BAR = KV + NS * TILE;
@@ -60,11 +61,11 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleLog2 = 8.0f;  // lazy rescale threshold (factor 256)
 
-template <int D, bool GQA>
+template <int D, bool GQA, int NS_>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const FwdParams p) {
-  using L = FwdSmem<D>;
+  using L = FwdSmem<D, NS_>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -75,7 +76,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int N = p.N;
-  const int nT = (N + kTile - 1) / kTile, npairs = (nT + 1) / 2;
+  const int nT = (N + kTile - 1) / kTile;
+  // one query tile per CTA only in the tile-sweep instantiations (NS_ != 0)
+  const bool single = NS_ != 0 && p.single_tile != 0;
+  const int npairs = single ? nT : (nT + 1) / 2;
   const int BH = p.B * p.H;
   int bh, pair;
   fwd_cta_coords(blockIdx.x, BH, npairs, p.causal != 0, bh, pair);
@@ -110,7 +114,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   const WaitCtl wc{abort_flag, p.err, p.wait_ns};
 
   FwdSchedule sch;
-  sch.init(pair, nT, p.causal != 0, p.lists, head);
+  sch.init(pair, nT, p.causal != 0, p.lists, head, single);
 
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer
@@ -383,21 +387,41 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   }
 }
 
-template <int D, bool GQA>
+template <int D, bool GQA, int NS_ = 0>
 cudaError_t launch_fwd_d(const FwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                          const CUtensorMap& tv, cudaStream_t stream) {
-  using L = FwdSmem<D>;
-  cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<D, GQA>,
+  using L = FwdSmem<D, NS_>;
+  cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<D, GQA, NS_>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
   if (e != cudaSuccess) return e;
-  const int nT = (p.N + kTile - 1) / kTile, npairs = (nT + 1) / 2;
+  const int nT = (p.N + kTile - 1) / kTile;
+  const int npairs = (NS_ != 0 && p.single_tile) ? nT : (nT + 1) / 2;
   const long long ctas = static_cast<long long>(npairs) * p.B * p.H;
-  fa_fwd_kernel<D, GQA>
+  fa_fwd_kernel<D, GQA, NS_>
       <<<static_cast<unsigned>(ctas), kFwdThreads, L::ALLOC, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
 
 }  // namespace
+
+cudaError_t launch_forward_config(const FwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
+                                  const CUtensorMap& tv, int kv_stages, cudaStream_t stream) {
+  if (p.d == 128) {
+    switch (kv_stages) {
+      case 2: return launch_fwd_d<128, false, 2>(p, tq, tk, tv, stream);
+      case 3: return launch_fwd_d<128, false, 3>(p, tq, tk, tv, stream);
+      case 4: return launch_fwd_d<128, false, 4>(p, tq, tk, tv, stream);
+      case 5: return launch_fwd_d<128, false, 5>(p, tq, tk, tv, stream);
+    }
+  } else if (p.d == 64) {
+    switch (kv_stages) {
+      case 2: return launch_fwd_d<64, false, 2>(p, tq, tk, tv, stream);
+      case 4: return launch_fwd_d<64, false, 4>(p, tq, tk, tv, stream);
+      case 8: return launch_fwd_d<64, false, 8>(p, tq, tk, tv, stream);
+    }
+  }
+  return cudaErrorInvalidValue;
+}
 
 cudaError_t launch_forward(const FwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                            const CUtensorMap& tv, cudaStream_t stream) {

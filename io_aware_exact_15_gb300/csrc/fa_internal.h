@@ -30,6 +30,7 @@ struct FwdParams {
   float scale = 0.f;
   int causal = 0;
   TileLists lists;        // sparse when lists.row_ptr != nullptr
+  int single_tile = 0;    // 1: one 128-row query tile per CTA instead of two
   int* err = nullptr;     // device status word
   uint64_t wait_ns = 0;
 };
@@ -58,6 +59,9 @@ bool make_acc_map(CUtensorMap* map, const void* base, int BH, int N, int d);
 
 cudaError_t launch_forward(const FwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                            const CUtensorMap& tv, cudaStream_t stream);
+// the forward with a chosen K/V ring depth (d = 128: 2..5, d = 64: 2, 4, 8)
+cudaError_t launch_forward_config(const FwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
+                                  const CUtensorMap& tv, int kv_stages, cudaStream_t stream);
 cudaError_t launch_backward_main(const BwdParams& p, const CUtensorMap& tq,
                                  const CUtensorMap& tk, const CUtensorMap& tv,
                                  const CUtensorMap& tdo, const CUtensorMap& tdq,

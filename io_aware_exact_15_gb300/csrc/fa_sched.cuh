@@ -31,11 +31,13 @@ struct FwdSchedule {
   int na, nb, ia, ib;
   int next_dense, end_dense;
 
-  FA_DEV void init(int pair, int nT, bool causal_, const TileLists& L, int head) {
-    qt[0] = 2 * pair;
-    qt[1] = 2 * pair + 1;
+  // single: the CTA takes one query tile (index `pair`) instead of two
+  FA_DEV void init(int pair, int nT, bool causal_, const TileLists& L, int head,
+                   bool single = false) {
+    qt[0] = single ? pair : 2 * pair;
+    qt[1] = qt[0] + 1;
     act[0] = true;
-    act[1] = qt[1] < nT;
+    act[1] = !single && qt[1] < nT;
     causal = causal_;
     sparse = L.row_ptr != nullptr;
     next_dense = 0;
