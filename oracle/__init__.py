@@ -209,3 +209,46 @@ def tile_counts(N, tile=TILE, causal=False, block_mask=None):
     if st != 0:
         raise ValueError("oracle tile_counts rejected its arguments")
     return out
+
+
+# ------------------------------------------------------------------ variable-length batches
+def _seq_bounds(cu_seqlens):
+    cu = [int(x) for x in np.asarray(cu_seqlens).reshape(-1)]
+    if len(cu) < 2 or cu[0] != 0 or any(b < a for a, b in zip(cu, cu[1:])):
+        raise ValueError("cu_seqlens must start at 0 and be non-decreasing")
+    return cu
+
+
+def forward_varlen(q, k, v, cu_seqlens, scale, causal=False, nthreads=None):
+    """Packed variable-length batch: q, k, v are [H, T, d] with sequence b
+    in tokens cu_seqlens[b] .. cu_seqlens[b+1]; attention stays inside each
+    sequence (the padding-mask benchmark of the summary's section 4.4).
+    Evaluates the per-sequence definition above.  Returns o [H, T, d] and
+    lse [H, T]."""
+    q, k, v = (np.asarray(x, dtype=np.float64) for x in (q, k, v))
+    cu = _seq_bounds(cu_seqlens)
+    H, T, d = q.shape
+    o = np.zeros((H, T, d))
+    lse = np.full((H, T), -np.inf)
+    for a, b in zip(cu, cu[1:]):
+        if b == a:
+            continue
+        ob, lb = forward(q[None, :, a:b], k[None, :, a:b], v[None, :, a:b], scale, causal=causal,
+                         nthreads=nthreads)
+        o[:, a:b] = ob[0]
+        lse[:, a:b] = lb[0]
+    return o, lse
+
+
+def backward_varlen(q, k, v, do, cu_seqlens, scale, causal=False, nthreads=None):
+    """Gradients of sum(O * dO) for forward_varlen; each [H, T, d]."""
+    q, k, v, do = (np.asarray(x, dtype=np.float64) for x in (q, k, v, do))
+    cu = _seq_bounds(cu_seqlens)
+    dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    for a, b in zip(cu, cu[1:]):
+        if b == a:
+            continue
+        g = backward(q[None, :, a:b], k[None, :, a:b], v[None, :, a:b], do[None, :, a:b], scale,
+                     causal=causal, nthreads=nthreads)
+        dq[:, a:b], dk[:, a:b], dv[:, a:b] = g[0][0], g[1][0], g[2][0]
+    return dq, dk, dv

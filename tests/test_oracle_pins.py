@@ -379,3 +379,47 @@ def test_grouped_kv_rejects_bad_groups():
     q, k = _rand(rng, 1, 4, 8, 2), _rand(rng, 1, 3, 8, 2)
     with pytest.raises(ValueError):
         oracle.forward(q, k, k, 1.0)
+
+
+# --------------------------------------------------------------------------
+# variable-length batches: the block-diagonal mask of packed sequences
+
+def _block_diag_mask(cu, causal):
+    T = cu[-1]
+    m = np.zeros((1, T, T), dtype=np.uint8)
+    for a, b in zip(cu, cu[1:]):
+        m[0, a:b, a:b] = 1
+    if causal:
+        m[0] &= np.tril(np.ones((T, T), dtype=np.uint8))
+    return m
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_varlen_equals_packed_block_diagonal_mask(causal):
+    rng = np.random.default_rng(17)
+    cu = [0, 5, 5, 12, 30]  # includes an empty sequence
+    H, T, d = 2, cu[-1], 4
+    q, k, v, do = (_rand(rng, H, T, d) for _ in range(4))
+    o, lse = oracle.forward_varlen(q, k, v, cu, 0.55, causal=causal)
+    dq, dk, dv = oracle.backward_varlen(q, k, v, do, cu, 0.55, causal=causal)
+    # same problem as one packed sequence with an element mask (tile 1): a
+    # different path through the oracle
+    m = _block_diag_mask(cu, causal)
+    o2, lse2 = oracle.forward(q[None], k[None], v[None], 0.55, block_mask=m, tile=1)
+    g2 = oracle.backward(q[None], k[None], v[None], do[None], 0.55, block_mask=m, tile=1)
+    np.testing.assert_allclose(o, o2[0], atol=1e-13)
+    np.testing.assert_allclose(lse, lse2[0], atol=1e-13)
+    for a, b in ((dq, g2[0]), (dk, g2[1]), (dv, g2[2])):
+        np.testing.assert_allclose(a, b[0], atol=1e-12)
+
+
+def test_varlen_equal_lengths_equals_batch():
+    rng = np.random.default_rng(18)
+    B, H, N, d = 3, 2, 11, 4
+    q, k, v = (_rand(rng, B, H, N, d) for _ in range(3))
+    pack = lambda x: np.concatenate([x[b] for b in range(B)], axis=1)  # [H, B*N, d]
+    o, lse = oracle.forward_varlen(pack(q), pack(k), pack(v), [0, 11, 22, 33], 0.3, causal=True)
+    o_b, lse_b = oracle.forward(q, k, v, 0.3, causal=True)
+    np.testing.assert_allclose(o, pack(o_b), atol=1e-14)
+    np.testing.assert_allclose(lse, np.concatenate([lse_b[b] for b in range(B)], axis=1),
+                               atol=1e-14)
