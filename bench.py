@@ -137,7 +137,21 @@ def run_gpu(args, rank, world, dist):
     peaks = load_peaks()
     w = W.WORKLOADS[args.workload]
     B, H, N, d = w.B, w.H, w.N, w.d
-    q, k, v, do, mask = W.make_inputs(w, with_do=True)
+    Hkv = w.kv_heads
+    varlen = w.varlen
+    gqa = Hkv != H
+    if varlen:
+        q, k, v, do, cu = W.make_varlen_inputs(w, with_do=True)
+        mask = None
+        T = int(cu[-1])
+        max_seqlen = int(np.max(np.diff(cu)))
+        lse_shape = (H, T)
+        rows_b, rows_n = 1, T  # the packed batch as one (1, H, T) row problem
+    else:
+        q, k, v, do, mask = W.make_inputs(w, with_do=True)
+        cu = None
+        lse_shape = (B, H, N)
+        rows_b, rows_n = B, N
     stream = torch.cuda.Stream(device=dev)
     K = args.steps
     s_ptr = stream.cuda_stream
@@ -146,11 +160,13 @@ def run_gpu(args, rank, world, dist):
     with torch.cuda.stream(stream):
         qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
         md = torch.from_numpy(np.ascontiguousarray(mask)).to(dev) if sparse else None
+        cud = torch.from_numpy(cu).to(dev) if varlen else None
         o = torch.empty_like(qd)
-        lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
-        dq, dk, dv = (torch.empty_like(qd) for _ in range(3))
+        lse = torch.empty(lse_shape, dtype=torch.float32, device=dev)
+        dq = torch.empty_like(qd)
+        dk, dv = torch.empty_like(kd), torch.empty_like(vd)
         nbytes = (fa.fa_blocksparse_workspace_size(B, H, N, d, mh) if sparse
-                  else fa.fa_backward_workspace_size(B, H, N, d))
+                  else fa.fa_backward_workspace_size(rows_b, H, rows_n, d))
         ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
         flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     lists_bytes = nbytes - fa.fa_backward_workspace_size(B, H, N, d) if sparse else 0
@@ -162,7 +178,31 @@ def run_gpu(args, rank, world, dist):
     bws = ws[lists_bytes:] if sparse else ws
     bwb = nbytes - lists_bytes
 
-    # one step; `ev` (5 events) splits it into its kernels
+    def forward():
+        if varlen:
+            check(fa.fa_forward_varlen(qd, kd, vd, o, lse, cud, B, max_seqlen, T, H, Hkv, d,
+                                       w.scale, w.causal, s_ptr), "forward")
+        elif gqa:
+            check(fa.fa_forward_gqa(qd, kd, vd, o, lse, B, H, Hkv, N, d, w.scale, w.causal,
+                                    s_ptr), "forward")
+        else:
+            check(fa.fa_forward(qd, kd, vd, o, lse, B, H, N, d, w.scale, w.causal, s_ptr),
+                  "forward")
+
+    def backward_whole():
+        if varlen:
+            check(fa.fa_backward_varlen(qd, kd, vd, o, dod, lse, dq, dk, dv, cud, B, max_seqlen,
+                                        T, H, Hkv, d, w.scale, w.causal, ws, nbytes, s_ptr),
+                  "backward")
+        else:
+            check(fa.fa_backward_gqa(qd, kd, vd, o, dod, lse, dq, dk, dv, B, H, Hkv, N, d,
+                                     w.scale, w.causal, ws, nbytes, s_ptr), "backward")
+
+    # One step; `ev` (5 events) splits it into its kernels.  Grouped-head and
+    # variable-length batches have no split backward entry point: the split
+    # step then brackets their whole backward and times the row-wise
+    # preprocess and dQ conversion beside it (the main kernel's time is the
+    # difference); the unsplit step is exactly forward + backward.
     def step(ev=None):
         rec = (lambda i: ev[i].record(stream)) if ev else (lambda i: None)
         rec(0)
@@ -177,8 +217,20 @@ def run_gpu(args, rank, world, dist):
             rec(3)
             rec(4)
             return
-        check(fa.fa_forward(qd, kd, vd, o, lse, B, H, N, d, w.scale, w.causal, s_ptr), "forward")
+        forward()
         rec(1)
+        if varlen or gqa:
+            if ev:
+                check(fa.fa_backward_preprocess(o, dod, rows_b, H, rows_n, d, bws, bwb, s_ptr),
+                      "preprocess")
+            rec(2)
+            backward_whole()
+            rec(3)
+            if ev:
+                check(fa.fa_backward_dq_convert(dq, rows_b, H, rows_n, d, w.scale, bws, bwb,
+                                                s_ptr), "convert")
+            rec(4)
+            return
         check(fa.fa_backward_preprocess(o, dod, B, H, N, d, bws, bwb, s_ptr), "preprocess")
         rec(2)
         check(fa.fa_backward_main(qd, kd, vd, dod, lse, dk, dv, B, H, N, d, w.scale, w.causal,
@@ -242,6 +294,8 @@ def run_gpu(args, rank, world, dist):
     pre_ms = statistics.fmean(p[1] for p in per)
     main_ms = statistics.fmean(p[2] for p in per)
     conv_ms = statistics.fmean(p[3] for p in per)
+    if varlen or gqa:  # p[2] bracketed preprocess + main + convert
+        main_ms = main_ms - pre_ms - conv_ms
     ms_max = ms
     if dist is not None:
         t = torch.tensor([ms], dtype=torch.float64, device=dev)
@@ -252,13 +306,17 @@ def run_gpu(args, rank, world, dist):
     # end to end through the public API with host buffers (pinned)
     hq, hk, hv, hdo = (t.pin_memory() for t in (q, k, v, do))
     ho = torch.empty_like(q).pin_memory()
-    hl = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
-    hdq, hdk, hdv = (torch.empty_like(q).pin_memory() for _ in range(3))
+    hl = torch.empty(lse_shape, dtype=torch.float32).pin_memory()
+    hdq = torch.empty_like(q).pin_memory()
+    hdk, hdv = torch.empty_like(k).pin_memory(), torch.empty_like(v).pin_memory()
     hm = torch.from_numpy(np.ascontiguousarray(mask)).pin_memory() if sparse else None
+    hcu = torch.from_numpy(cu).pin_memory() if varlen else None
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo))
     d2h = sum(t.numel() * t.element_size() for t in (ho, hl, hdq, hdk, hdv))
     if sparse:
         h2d += hm.numel()
+    if varlen:
+        h2d += hcu.numel() * hcu.element_size()
 
     def e2e_step():
         with torch.cuda.stream(stream):
@@ -266,6 +324,8 @@ def run_gpu(args, rank, world, dist):
                 dst.copy_(src, non_blocking=True)
             if sparse:
                 md.copy_(hm, non_blocking=True)
+            if varlen:
+                cud.copy_(hcu, non_blocking=True)
         step()
         with torch.cuda.stream(stream):
             for dst, src in ((ho, o), (hl, lse), (hdq, dq), (hdk, dk), (hdv, dv)):
@@ -301,6 +361,8 @@ def run_gpu(args, rank, world, dist):
                 "frac": round(achieved / peak, 4),
                 "peak_source": f"{peaks['source']} bf16 burst",
                 "traffic": ncu_traffic(f"fa_bwd_kernel:{args.workload}", src_hash),
+                "main_time": ("combined backward minus separately timed preprocess and convert"
+                              if (varlen or gqa) else "CUDA events around the kernel's launch"),
                 "algorithmic_flops_per_launch": main_flops,
                 "avg_launch_ms": round(main_ms, 5)}
     fwd_tf = ff / (fwd_ms * 1e-3) / 1e12
@@ -310,7 +372,9 @@ def run_gpu(args, rank, world, dist):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) bf16)",
         "config": {"workload": f"{w.name}: {w.note}", "B": B, "H": H, "N": N, "d": d,
-                   "causal": w.causal, "sparse": sparse,
+                   "causal": w.causal, "sparse": sparse, "Hkv": Hkv,
+                   **({"total_tokens": T, "max_seqlen": max_seqlen,
+                       "seq_lens": [int(x) for x in np.diff(cu)]} if varlen else {}),
                    "l2": "flushed before every timed step (256 MiB device write, outside events)",
                    "parallelism": f"replicas x{world} (independent heads per GPU)"},
         "fwd": {"ms": round(fwd_ms, 5), "tflops": round(fwd_tf, 2),
@@ -329,25 +393,48 @@ def run_gpu(args, rank, world, dist):
 
 
 # ---------------------------------------------------------------------------- CPU oracle
-def oracle_sample(w, heads, q, k, v, do, mask, nthreads):
-    """fp64 oracle forward + backward on the first `heads` (batch, head)
-    slices of the workload."""
+def oracle_job(w):
+    """(sample(n), units, flops_per_unit): sample(n) runs the fp64 oracle
+    forward + backward on the first n units of the workload: (batch, head)
+    slices, or heads of a packed variable-length batch.  Grouped heads are
+    sampled per query head with its key/value head."""
+    import numpy as np
+
+    import fa_workloads as W
     import oracle
+    f = lambda t: t.float().double().numpy()
+    if w.varlen:
+        q, k, v, do, cu = W.make_varlen_inputs(w, with_do=True)
+        G = w.H // w.kv_heads
+
+        def sample(n, nthreads):
+            kv = np.arange(n) // G
+            oracle.forward_varlen(f(q[:n]), f(k[kv]), f(v[kv]), cu, w.scale, causal=w.causal,
+                                  nthreads=nthreads)
+            oracle.backward_varlen(f(q[:n]), f(k[kv]), f(v[kv]), f(do[:n]), cu, w.scale,
+                                   causal=w.causal, nthreads=nthreads)
+        return sample, w.H, W.fwd_bwd_flops(w) / w.H
+    q, k, v, do, mask = W.make_inputs(w, with_do=True)
     B, H, N, d = q.shape
-    f = lambda t: t.reshape(1, B * H, N, d)[:, :heads].float().double().numpy()
-    oracle.forward(f(q), f(k), f(v), w.scale, causal=w.causal, block_mask=mask,
-                   nthreads=nthreads)
-    oracle.backward(f(q), f(k), f(v), f(do), w.scale, causal=w.causal, block_mask=mask,
-                    nthreads=nthreads)
+    G = H // k.shape[1]
+    if G > 1:
+        k, v = k.repeat_interleave(G, dim=1), v.repeat_interleave(G, dim=1)
+    r = lambda t, n: f(t.reshape(1, B * H, N, d)[:, :n])
+
+    def sample(n, nthreads):
+        oracle.forward(r(q, n), r(k, n), r(v, n), w.scale, causal=w.causal, block_mask=mask,
+                       nthreads=nthreads)
+        oracle.backward(r(q, n), r(k, n), r(v, n), r(do, n), w.scale, causal=w.causal,
+                        block_mask=mask, nthreads=nthreads)
+    return sample, B * H, W.fwd_bwd_flops(w, mask) / (B * H)
 
 
-def calibrate_heads(w, q, k, v, do, mask, nthreads, budget_s):
-    """Heads whose oracle forward + backward take about budget_s seconds."""
-    total = w.B * w.H
+def calibrate_units(sample, total, nthreads, budget_s):
+    """Units whose oracle forward + backward take about budget_s seconds."""
     n = 1
     while True:
         t0 = time.perf_counter()
-        oracle_sample(w, n, q, k, v, do, mask, nthreads)
+        sample(n, nthreads)
         dt = time.perf_counter() - t0
         if n >= total or dt >= 0.2 * budget_s:
             break
@@ -356,18 +443,17 @@ def calibrate_heads(w, q, k, v, do, mask, nthreads, budget_s):
 
 
 def cpu_baseline(w, budget_s=12.0):
-    import fa_workloads as W
-    q, k, v, do, mask = W.make_inputs(w, with_do=True)
+    sample, total, per_unit = oracle_job(w)
     nthreads = os.cpu_count() or 1
-    heads = calibrate_heads(w, q, k, v, do, mask, nthreads, budget_s)
+    n = calibrate_units(sample, total, nthreads, budget_s)
     t0 = time.perf_counter()
-    oracle_sample(w, heads, q, k, v, do, mask, nthreads)
+    sample(n, nthreads)
     dt = time.perf_counter() - t0
-    per_head = W.fwd_bwd_flops(w, mask) / (w.B * w.H)
-    return {"value": round(per_head * heads / dt / 1e12, 9), "unit": "TFLOP/s",
+    unit = "heads of the packed batch" if w.varlen else "(batch, head) slices"
+    return {"value": round(per_unit * n / dt / 1e12, 9), "unit": "TFLOP/s",
             "cores": nthreads, "kind": "oracle",
-            "sample": f"fp64 C oracle forward+backward on {heads} of {w.B * w.H} (batch, head) "
-                      f"slices of {w.name}, {dt:.2f} s wall"}
+            "sample": f"fp64 C oracle forward+backward on {n} of {total} {unit} "
+                      f"of {w.name}, {dt:.2f} s wall"}
 
 
 def run_reference(args, rank, world):
@@ -377,22 +463,20 @@ def run_reference(args, rank, world):
     if rank != 0:
         return None
     w = W.WORKLOADS[args.workload]
-    q, k, v, do, mask = W.make_inputs(w, with_do=True)
+    sample, total, per_unit = oracle_job(w)
     nthreads = os.cpu_count() or 1
     per_step_budget = max(1.0, 150.0 / max(1, args.steps + args.warmup))
-    heads = calibrate_heads(w, q, k, v, do, mask, nthreads, per_step_budget)
+    n = calibrate_units(sample, total, nthreads, per_step_budget)
     for _ in range(args.warmup):
-        oracle_sample(w, heads, q, k, v, do, mask, nthreads)
+        sample(n, nthreads)
     times = []
     for _ in range(args.steps):
         t0 = time.perf_counter()
-        oracle_sample(w, heads, q, k, v, do, mask, nthreads)
+        sample(n, nthreads)
         times.append(time.perf_counter() - t0)
     ms = 1e3 * statistics.fmean(times)
-    per_head = W.fwd_bwd_flops(w, mask) / (w.B * w.H)
-    value = per_head * heads / (ms * 1e-3) / 1e12
-    sample = (f"fp64 C oracle forward+backward on {heads} of {w.B * w.H} heads per step "
-              f"({w.name})")
+    value = per_unit * n / (ms * 1e-3) / 1e12
+    sample_txt = f"fp64 C oracle forward+backward on {n} of {total} units per step ({w.name})"
     return {"metric": METRIC, "value": round(value, 9), "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
@@ -401,7 +485,7 @@ def run_reference(args, rank, world):
                        "d": w.d, "causal": w.causal},
             "impl": "reference",
             "cpu_baseline": {"value": round(value, 9), "unit": "TFLOP/s", "cores": nthreads,
-                             "kind": "oracle", "sample": sample},
+                             "kind": "oracle", "sample": sample_txt},
             "e2e": {"value": round(value, 9), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0},
             "gpu_launches": 0}

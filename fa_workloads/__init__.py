@@ -15,6 +15,11 @@ Recipe (one per workload):
   * Block mask over 128 x 128 tiles: the diagonal band |i - j| <= 1, block
     column 0, and exactly round(density * R) of the R remaining tiles chosen
     by a seeded permutation; one mask shared by every head.
+  * Variable-length batch (padding mask as lengths): B lengths drawn i.i.d.
+    uniform on the integers [N/4, N] from the mask generator; the sequences
+    are packed back to back, tensors [H, total, d] (K, V: [Hkv, total, d]),
+    drawn like the equal-length ones.
+  * Grouped heads: K and V have Hkv heads instead of H.
 """
 from __future__ import annotations
 
@@ -37,12 +42,18 @@ class Workload:
     backward: bool = True
     peaked_frac: float = 0.0
     sparse_density: float | None = None  # block-sparse when not None
+    Hkv: int | None = None  # grouped key/value heads when set (H % Hkv == 0)
+    varlen: bool = False    # packed batch of lengths in [N/4, N]
     seed_index: int = 0
     note: str = ""
 
     @property
     def scale(self) -> float:
         return 1.0 / float(self.d) ** 0.5
+
+    @property
+    def kv_heads(self) -> int:
+        return self.H if self.Hkv is None else self.Hkv
 
     @property
     def seed(self) -> int:
@@ -78,6 +89,13 @@ WORKLOADS = {
     "blocksparse_64k": Workload("blocksparse_64k", 1, 8, 65536, 64, sparse_density=0.05,
                                 seed_index=5,
                                 note="B=1 H=8 N=65536 d=64, band + column 0 + 5% random tiles"),
+    "bert_large_varlen": Workload("bert_large_varlen", 8, 16, 512, 64, varlen=True, seed_index=6,
+                                  note="BERT-large shapes with a padding mask: 8 packed "
+                                       "sequences of 128..512 tokens, H=16 d=64"),
+    "gqa_causal_n4096_d128": Workload("gqa_causal_n4096_d128", 4, 16, 4096, 128, causal=True,
+                                      Hkv=4, seed_index=7,
+                                      note="grouped heads: 16 query heads over 4 K/V heads, "
+                                           "B=4 N=4096 d=128 causal"),
 }
 
 
@@ -134,11 +152,41 @@ def sample_rows(N, n, seed):
     return np.sort(torch.randperm(N, generator=g)[:n].numpy().astype(np.int64))
 
 
+def varlen_lengths(w: Workload) -> np.ndarray:
+    """The B sequence lengths of a variable-length workload (int64)."""
+    g = torch.Generator().manual_seed(int(w.mask_seed))
+    return torch.randint(w.N // 4, w.N + 1, (w.B,), generator=g).numpy().astype(np.int64)
+
+
+def cu_seqlens(lengths) -> np.ndarray:
+    """int32 offsets [B+1] of sequences packed back to back."""
+    return np.concatenate([[0], np.cumsum(np.asarray(lengths, dtype=np.int64))]).astype(np.int32)
+
+
+def make_varlen_inputs(w: Workload, with_do=None):
+    """q, dO [H, total, d], k, v [Hkv, total, d] (bf16 CPU) and cu_seqlens."""
+    if with_do is None:
+        with_do = w.backward
+    cu = cu_seqlens(varlen_lengths(w))
+    T = int(cu[-1])
+    g = torch.Generator().manual_seed(int(w.seed))
+    q = randn_bf16((w.H, T, w.d), g)
+    k = randn_bf16((w.kv_heads, T, w.d), g)
+    v = randn_bf16((w.kv_heads, T, w.d), g)
+    do = randn_bf16((w.H, T, w.d), g) if with_do else None
+    return q, k, v, do, cu
+
+
 def make_inputs(w: Workload, with_do=None):
     """q, k, v, dO (bf16 CPU) and the block mask (numpy uint8 or None)."""
     if with_do is None:
         with_do = w.backward
+    if w.varlen:
+        raise ValueError("variable-length workloads: use make_varlen_inputs")
     q, k, v, do = make_qkv(w.B, w.H, w.N, w.d, w.seed, w.peaked_frac, w.mask_seed, with_do)
+    if w.Hkv is not None and w.Hkv != w.H:
+        # grouped heads: K and V keep the first Hkv heads' draws
+        k, v = k[:, :w.Hkv].contiguous(), v[:, :w.Hkv].contiguous()
     mask = None
     if w.sparse_density is not None:
         mask = band_random_block_mask(w.N, w.mask_seed, w.sparse_density)
@@ -147,7 +195,12 @@ def make_inputs(w: Workload, with_do=None):
 
 def fwd_flops(w: Workload, mask=None) -> float:
     """Algorithmic forward FLOPs: 4*B*H*N^2*d, halved when causal; block-
-    sparse counts 4*d*128^2 per kept tile per head."""
+    sparse counts 4*d*128^2 per kept tile per head; a variable-length batch
+    sums 4*H*n^2*d over its sequence lengths n."""
+    if w.varlen:
+        n = varlen_lengths(w).astype(np.float64)
+        f = 4.0 * w.H * w.d * float(np.sum(n * n))
+        return f / 2 if w.causal else f
     if mask is not None:
         nnz = int(np.count_nonzero(mask))
         per_head = 4.0 * w.d * TILE * TILE * nnz / mask.shape[0]

@@ -153,6 +153,35 @@ fa_status fa_backward_gqa(const void* q, const void* k, const void* v, const voi
                           int H, int Hkv, int N, int d, float scale, int causal, void* workspace,
                           size_t workspace_bytes, cudaStream_t stream);
 
+/*
+ * Packed variable-length batch (hackmd summary, section 4.4: attention over
+ * a batch of unequal lengths, which padding would waste work on).  The B
+ * sequences are packed back to back along the row axis; sequence b holds rows
+ * cu_seqlens[b] .. cu_seqlens[b+1]-1 and attends only within itself (causal:
+ * row i of a sequence sees that sequence's rows 0..i).
+ *   q, o, dO, dq  bf16 [H, total, d];   lse fp32 [H, total]
+ *   k, v, dk, dv  bf16 [Hkv, total, d]  (Hkv = H: ordinary multi-head;
+ *                 otherwise grouped heads as fa_forward_gqa)
+ *   cu_seqlens    int32 [B+1], DEVICE memory, cu_seqlens[0] = 0,
+ *                 nondecreasing, cu_seqlens[B] = total; empty sequences
+ *                 (equal neighbours) are allowed and produce nothing
+ *   max_seqlen    >= every length (it sizes the grid); 1 <= max_seqlen <= total
+ * The array is read only on the device.  The kernels clamp its entries to
+ * [0, total] and lengths to max_seqlen: an array that breaks the rules gives
+ * unspecified values in the outputs but no access outside the tensors.
+ * total = 0 returns FA_OK with nothing launched.  Workspace (backward):
+ * fa_backward_workspace_size(1, H, total, d).  Other rules as fa_forward /
+ * fa_backward; H * total * d must stay below 2^31.
+ */
+fa_status fa_forward_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                            const int* cu_seqlens, int B, int max_seqlen, int total, int H,
+                            int Hkv, int d, float scale, int causal, cudaStream_t stream);
+fa_status fa_backward_varlen(const void* q, const void* k, const void* v, const void* o,
+                             const void* dO, const float* lse, void* dq, void* dk, void* dv,
+                             const int* cu_seqlens, int B, int max_seqlen, int total, int H,
+                             int Hkv, int d, float scale, int causal, void* workspace,
+                             size_t workspace_bytes, cudaStream_t stream);
+
 /* Bytes of workspace the block-sparse calls need: the CSR and CSC tile
  * lists of the mask (4 * mask_heads * (2*(nT+1) + 2*nT*nT) bytes) followed
  * by the fa_backward workspace.  The forward uses only the list part. */

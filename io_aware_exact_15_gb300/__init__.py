@@ -31,7 +31,7 @@ EXPORTS = (
     "fa_blocksparse_workspace_size", "fa_blocksparse_build_lists", "fa_blocksparse_forward",
     "fa_blocksparse_backward", "fa_get_device_status", "fa_set_wait_limit_ns",
     "fa_debug_wait_timeout", "fa_debug_schedule", "fa_debug_mma_probe", "fa_forward_gqa",
-    "fa_backward_gqa", "fa_debug_forward_config",
+    "fa_backward_gqa", "fa_debug_forward_config", "fa_forward_varlen", "fa_backward_varlen",
 )
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -87,6 +87,9 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
             "fa_forward_gqa": ([P, P, P, P, P, I, I, I, I, I, F, I, P], I),
             "fa_debug_forward_config": ([P, P, P, P, P, I, I, I, I, F, I, I, I, P], I),
             "fa_backward_gqa": ([P, P, P, P, P, P, P, P, P, I, I, I, I, I, F, I, P, Z, P], I),
+            "fa_forward_varlen": ([P, P, P, P, P, P, I, I, I, I, I, I, F, I, P], I),
+            "fa_backward_varlen": ([P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, I, P, Z, P],
+                                   I),
         }
         for name, (args, res) in sig.items():
             fn = getattr(lib, name)
@@ -138,6 +141,21 @@ def fa_backward_gqa(q, k, v, o, dO, lse, dq, dk, dv, B, H, Hkv, N, d, scale, cau
     return load().fa_backward_gqa(_p(q), _p(k), _p(v), _p(o), _p(dO), _p(lse), _p(dq), _p(dk),
                                   _p(dv), B, H, Hkv, N, d, float(scale), int(bool(causal)),
                                   _p(workspace), int(workspace_bytes), _s(stream))
+
+
+def fa_forward_varlen(q, k, v, o, lse, cu_seqlens, B, max_seqlen, total, H, Hkv, d, scale,
+                      causal, stream=None) -> int:
+    return load().fa_forward_varlen(_p(q), _p(k), _p(v), _p(o), _p(lse), _p(cu_seqlens), B,
+                                    max_seqlen, total, H, Hkv, d, float(scale),
+                                    int(bool(causal)), _s(stream))
+
+
+def fa_backward_varlen(q, k, v, o, dO, lse, dq, dk, dv, cu_seqlens, B, max_seqlen, total, H, Hkv,
+                       d, scale, causal, workspace, workspace_bytes, stream=None) -> int:
+    return load().fa_backward_varlen(_p(q), _p(k), _p(v), _p(o), _p(dO), _p(lse), _p(dq), _p(dk),
+                                     _p(dv), _p(cu_seqlens), B, max_seqlen, total, H, Hkv, d,
+                                     float(scale), int(bool(causal)), _p(workspace),
+                                     int(workspace_bytes), _s(stream))
 
 
 def fa_backward_workspace_size(B, H, N, d) -> int:
@@ -245,17 +263,50 @@ def _shape(q):
     return tuple(int(x) for x in q.shape)
 
 
+def _varlen_shape(q, k, cu_seqlens, max_seqlen):
+    if q.dim() != 3 or k.dim() != 3:
+        raise ValueError("variable-length batches take [H, total, d] tensors")
+    H, T, d = (int(x) for x in q.shape)
+    B = int(cu_seqlens.numel()) - 1
+    if B < 1:
+        raise ValueError("cu_seqlens needs B + 1 >= 2 entries")
+    if max_seqlen is None:  # one host read of the offsets
+        cu = cu_seqlens.cpu()
+        max_seqlen = int((cu[1:] - cu[:-1]).max()) if T > 0 else 0
+    return B, H, int(k.shape[0]), T, d, int(max_seqlen)
+
+
 def attention_forward(q, k, v, scale=None, causal=False, block_mask=None, workspace=None,
-                      stream=None):
-    """(o, lse) for bf16 CUDA tensors q, k, v of shape [B, H, N, d]."""
+                      stream=None, cu_seqlens=None, max_seqlen=None):
+    """(o, lse) for bf16 CUDA tensors q [B, H, N, d] and k, v [B, Hkv, N, d]
+    (Hkv = H, or a divisor of H for grouped heads).  With cu_seqlens (int32
+    CUDA tensor [B+1]) the batch is packed: q [H, total, d], k, v
+    [Hkv, total, d], lse [H, total]."""
     import torch
+    if cu_seqlens is not None:
+        if block_mask is not None:
+            raise ValueError("block masks apply to equal-length batches only")
+        B, H, Hkv, T, d, ms = _varlen_shape(q, k, cu_seqlens, max_seqlen)
+        scale = (1.0 / d ** 0.5) if scale is None else scale
+        o = torch.empty_like(q)
+        lse = torch.empty((H, T), dtype=torch.float32, device=q.device)
+        _check(fa_forward_varlen(q, k, v, o, lse, cu_seqlens, B, ms, T, H, Hkv, d, scale, causal,
+                                 stream), "fa_forward_varlen")
+        return o, lse
     B, H, N, d = _shape(q)
+    Hkv = int(k.shape[1])
     scale = (1.0 / d ** 0.5) if scale is None else scale
     o = torch.empty_like(q)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
     if block_mask is None:
-        _check(fa_forward(q, k, v, o, lse, B, H, N, d, scale, causal, stream), "fa_forward")
+        if Hkv == H:
+            _check(fa_forward(q, k, v, o, lse, B, H, N, d, scale, causal, stream), "fa_forward")
+        else:
+            _check(fa_forward_gqa(q, k, v, o, lse, B, H, Hkv, N, d, scale, causal, stream),
+                   "fa_forward_gqa")
     else:
+        if Hkv != H:
+            raise ValueError("block masks apply to Hkv = H only")
         mh = int(block_mask.shape[0])
         nbytes = fa_blocksparse_workspace_size(B, H, N, d, mh)
         if workspace is None:
@@ -267,19 +318,38 @@ def attention_forward(q, k, v, scale=None, causal=False, block_mask=None, worksp
 
 
 def attention_backward(q, k, v, o, dO, lse, scale=None, causal=False, block_mask=None,
-                       workspace=None, stream=None):
-    """(dq, dk, dv) of sum(O * dO)."""
+                       workspace=None, stream=None, cu_seqlens=None, max_seqlen=None):
+    """(dq, dk, dv) of sum(O * dO); shapes and options as attention_forward."""
     import torch
-    B, H, N, d = _shape(q)
-    scale = (1.0 / d ** 0.5) if scale is None else scale
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    if cu_seqlens is not None:
+        if block_mask is not None:
+            raise ValueError("block masks apply to equal-length batches only")
+        B, H, Hkv, T, d, ms = _varlen_shape(q, k, cu_seqlens, max_seqlen)
+        scale = (1.0 / d ** 0.5) if scale is None else scale
+        nbytes = fa_backward_workspace_size(1, H, max(T, 1), d)
+        if workspace is None:
+            workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+        _check(fa_backward_varlen(q, k, v, o, dO, lse, dq, dk, dv, cu_seqlens, B, ms, T, H, Hkv, d,
+                                  scale, causal, workspace, workspace.numel(), stream),
+               "fa_backward_varlen")
+        return dq, dk, dv
+    B, H, N, d = _shape(q)
+    Hkv = int(k.shape[1])
+    scale = (1.0 / d ** 0.5) if scale is None else scale
     if block_mask is None:
         nbytes = fa_backward_workspace_size(B, H, N, d)
         if workspace is None:
             workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
-        _check(fa_backward(q, k, v, o, dO, lse, dq, dk, dv, B, H, N, d, scale, causal, workspace,
-                           workspace.numel(), stream), "fa_backward")
+        if Hkv == H:
+            _check(fa_backward(q, k, v, o, dO, lse, dq, dk, dv, B, H, N, d, scale, causal,
+                               workspace, workspace.numel(), stream), "fa_backward")
+        else:
+            _check(fa_backward_gqa(q, k, v, o, dO, lse, dq, dk, dv, B, H, Hkv, N, d, scale, causal,
+                                   workspace, workspace.numel(), stream), "fa_backward_gqa")
     else:
+        if Hkv != H:
+            raise ValueError("block masks apply to Hkv = H only")
         mh = int(block_mask.shape[0])
         nbytes = fa_blocksparse_workspace_size(B, H, N, d, mh)
         if workspace is None:

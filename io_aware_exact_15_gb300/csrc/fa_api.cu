@@ -168,15 +168,26 @@ fa_status check_mask(const uint8_t* mask, int mask_heads, int H, int N) {
   return FA_OK;
 }
 
+// Packed variable-length batch: tensors [H, total, d], sequence b in rows
+// cu_seqlens[b] .. cu_seqlens[b+1] (device array), N = the longest length.
+struct Varlen {
+  const int* cu_seqlens = nullptr;
+  int total = 0;
+};
+
 fa_status forward_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                        int H, int Hkv, int N, int d, float scale, int causal,
-                       const fa::TileLists* lists, cudaStream_t stream) {
+                       const fa::TileLists* lists, cudaStream_t stream,
+                       const Varlen& vl = Varlen()) {
   fa_status st = FA_OK;
   int* err = status_word(&st);
   if (!err) return st;
+  // TMA slices: (batch, head) pairs of N rows, or heads of `total` rows
+  const int zq = vl.cu_seqlens ? H : B * H, zkv = vl.cu_seqlens ? Hkv : B * Hkv;
+  const int rows = vl.cu_seqlens ? vl.total : N;
   CUtensorMap tq, tk, tv;
-  if (!fa::make_tile_map(&tq, q, B * H, N, d) || !fa::make_tile_map(&tk, k, B * Hkv, N, d) ||
-      !fa::make_tile_map(&tv, v, B * Hkv, N, d))
+  if (!fa::make_tile_map(&tq, q, zq, rows, d) || !fa::make_tile_map(&tk, k, zkv, rows, d) ||
+      !fa::make_tile_map(&tv, v, zkv, rows, d))
     return FA_ERR_CUDA;
   fa::FwdParams p;
   p.o = o;
@@ -189,6 +200,8 @@ fa_status forward_impl(const void* q, const void* k, const void* v, void* o, flo
   p.scale = scale;
   p.causal = causal ? 1 : 0;
   if (lists) p.lists = *lists;
+  p.cu_seqlens = vl.cu_seqlens;
+  p.total = vl.total;
   p.err = err;
   p.wait_ns = wait_limit_ns();
   FA_CUDA(fa::launch_forward(p, tq, tk, tv, stream));
@@ -198,14 +211,17 @@ fa_status forward_impl(const void* q, const void* k, const void* v, void* o, flo
 fa_status backward_main_impl(const void* q, const void* k, const void* v, const void* dO,
                              const float* lse, void* dk, void* dv, int B, int H, int Hkv, int N,
                              int d, float scale, int causal, const BwdWorkspace& w,
-                             const fa::TileLists* lists, cudaStream_t stream) {
+                             const fa::TileLists* lists, cudaStream_t stream,
+                             const Varlen& vl = Varlen()) {
   fa_status st = FA_OK;
   int* err = status_word(&st);
   if (!err) return st;
+  const int zq = vl.cu_seqlens ? H : B * H, zkv = vl.cu_seqlens ? Hkv : B * Hkv;
+  const int rows = vl.cu_seqlens ? vl.total : N;
   CUtensorMap tq, tk, tv, tdo, tdq;
-  if (!fa::make_tile_map(&tq, q, B * H, N, d) || !fa::make_tile_map(&tk, k, B * Hkv, N, d) ||
-      !fa::make_tile_map(&tv, v, B * Hkv, N, d) || !fa::make_tile_map(&tdo, dO, B * H, N, d) ||
-      !fa::make_acc_map(&tdq, w.dq_acc, B * H, N, d))
+  if (!fa::make_tile_map(&tq, q, zq, rows, d) || !fa::make_tile_map(&tk, k, zkv, rows, d) ||
+      !fa::make_tile_map(&tv, v, zkv, rows, d) || !fa::make_tile_map(&tdo, dO, zq, rows, d) ||
+      !fa::make_acc_map(&tdq, w.dq_acc, zq, rows, d))
     return FA_ERR_CUDA;
   fa::BwdParams p;
   p.lse = lse;
@@ -221,6 +237,8 @@ fa_status backward_main_impl(const void* q, const void* k, const void* v, const 
   p.scale = scale;
   p.causal = causal ? 1 : 0;
   if (lists) p.lists = *lists;
+  p.cu_seqlens = vl.cu_seqlens;
+  p.total = vl.total;
   p.err = err;
   p.wait_ns = wait_limit_ns();
   FA_CUDA(fa::launch_backward_main(p, tq, tk, tv, tdo, tdq, stream));
@@ -251,6 +269,23 @@ fa_status check_bwd_args(const void* q, const void* k, const void* v, const void
 
 fa_status check_groups(int H, int Hkv) {
   if (Hkv < 1 || Hkv > H || H % Hkv != 0) return FA_ERR_INVALID_ARG;
+  return FA_OK;
+}
+
+// Packed variable-length batch: B sequences, the longest max_seqlen rows,
+// `total` rows in all.  cu_seqlens lives on the device and is not read here;
+// the kernels clamp its entries to [0, total], so a malformed array gives
+// undefined values but no access outside the tensors.
+fa_status check_varlen(const int* cu_seqlens, int B, int max_seqlen, int total, int H, int d,
+                       float scale) {
+  if (B < 1 || H < 1 || total < 0 || max_seqlen < 0) return FA_ERR_INVALID_ARG;
+  if (!(isfinite(scale) && scale > 0.f)) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  FA_TRY(check_ptr4(cu_seqlens));
+  if (total > 0 && (max_seqlen < 1 || max_seqlen > total)) return FA_ERR_INVALID_ARG;
+  if (static_cast<long long>(H) * total * d >= (1LL << 31)) return FA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(B) * H * num_tiles(max_seqlen) >= (1LL << 31))
+    return FA_ERR_UNSUPPORTED;
   return FA_OK;
 }
 
@@ -384,6 +419,45 @@ fa_status fa_backward_gqa(const void* q, const void* k, const void* v, const voi
   FA_TRY(backward_main_impl(q, k, v, dO, lse, dk, dv, B, H, Hkv, N, d, scale, causal,
                             bwd_ws(workspace, B, H, N), nullptr, stream));
   return fa_backward_dq_convert(dq, B, H, N, d, scale, workspace, workspace_bytes, stream);
+}
+
+fa_status fa_forward_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                            const int* cu_seqlens, int B, int max_seqlen, int total, int H,
+                            int Hkv, int d, float scale, int causal, cudaStream_t stream) {
+  FA_TRY(check_varlen(cu_seqlens, B, max_seqlen, total, H, d, scale));
+  FA_TRY(check_groups(H, Hkv));
+  for (const void* p : {q, k, v, static_cast<const void*>(o)}) FA_TRY(check_ptr16(p));
+  FA_TRY(check_ptr4(lse));
+  if (total == 0) return FA_OK;  // every sequence empty: nothing to write
+  Varlen vl;
+  vl.cu_seqlens = cu_seqlens;
+  vl.total = total;
+  return forward_impl(q, k, v, o, lse, B, H, Hkv, max_seqlen, d, scale, causal, nullptr, stream,
+                      vl);
+}
+
+fa_status fa_backward_varlen(const void* q, const void* k, const void* v, const void* o,
+                             const void* dO, const float* lse, void* dq, void* dk, void* dv,
+                             const int* cu_seqlens, int B, int max_seqlen, int total, int H,
+                             int Hkv, int d, float scale, int causal, void* workspace,
+                             size_t workspace_bytes, cudaStream_t stream) {
+  FA_TRY(check_varlen(cu_seqlens, B, max_seqlen, total, H, d, scale));
+  FA_TRY(check_groups(H, Hkv));
+  for (const void* p : {q, k, v, o, dO, static_cast<const void*>(dq), static_cast<const void*>(dk),
+                        static_cast<const void*>(dv)})
+    FA_TRY(check_ptr16(p));
+  FA_TRY(check_ptr4(lse));
+  if (total == 0) return FA_OK;
+  // the whole packed batch is one (1, H, total) problem for the row-wise
+  // preprocess and the dQ conversion
+  FA_TRY(check_ws(workspace, workspace_bytes, bwd_ws_bytes(1, H, total, d)));
+  FA_TRY(fa_backward_preprocess(o, dO, 1, H, total, d, workspace, workspace_bytes, stream));
+  Varlen vl;
+  vl.cu_seqlens = cu_seqlens;
+  vl.total = total;
+  FA_TRY(backward_main_impl(q, k, v, dO, lse, dk, dv, B, H, Hkv, max_seqlen, d, scale, causal,
+                            bwd_ws(workspace, 1, H, total), nullptr, stream, vl));
+  return fa_backward_dq_convert(dq, 1, H, total, d, scale, workspace, workspace_bytes, stream);
 }
 
 size_t fa_blocksparse_workspace_size(int B, int H, int N, int d, int mask_heads) {

@@ -68,7 +68,7 @@ struct BwdSmem {
 constexpr int kBwdThreads = 384;
 constexpr float kLog2e = 1.4426950408889634f;
 
-template <int D, bool GQA>
+template <int D, int KIND>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     fa_bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
@@ -83,17 +83,34 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::MISC + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int N = p.N;
-  const int nT = (N + kTile - 1) / kTile;
+  constexpr bool GQA = KIND != kPlain;
+  const int ntmax = (p.N + kTile - 1) / kTile;
   // one CTA = one key/value head x one key tile; with grouped K/V it walks
   // the query tiles of every query head of its group (G = H / Hkv)
-  // (the plain instantiation, GQA = false, carries no group arithmetic)
+  // (the plain instantiation carries no group arithmetic)
   const int Hkv = GQA ? p.Hkv : p.H;
   const int G = GQA ? p.H / p.Hkv : 1;
   int bkv, kt;
-  bwd_cta_coords(blockIdx.x, p.B * Hkv, nT, p.causal != 0, bkv, kt);
-  // first query slice of the group
-  const int bq0 = GQA ? (bkv / Hkv) * p.H + (bkv % Hkv) * G : bkv;
+  bwd_cta_coords(blockIdx.x, p.B * Hkv, ntmax, p.causal != 0, bkv, kt);
+  // Sequence geometry: length N, first row row0 of the sequence in its
+  // slice, the K/V slice zkv and the first query slice bq0 of the group.
+  int N = p.N, row0 = 0, zkv = bkv;
+  int bq0 = GQA ? (bkv / Hkv) * p.H + (bkv % Hkv) * G : bkv;
+  if (KIND == kGeneral) {
+    // variable-length batch: slices are heads, sequences are row ranges
+    // (indices clamped to [0, total], so bad offsets cannot write outside)
+    const int b = bkv / Hkv;
+    const int a = min(max(p.cu_seqlens[b], 0), p.total);
+    const int e = min(max(p.cu_seqlens[b + 1], a), p.total);
+    row0 = a;
+    N = min(e - a, p.N);
+    zkv = bkv % Hkv;
+    bq0 = zkv * G;
+    if (kt * kTile >= N) return;  // no key of this tile here (CTA-uniform)
+  }
+  const size_t slice_rows = KIND == kGeneral ? static_cast<size_t>(p.total)
+                                             : static_cast<size_t>(p.N);
+  const int nT = (N + kTile - 1) / kTile;
 
   if (threadIdx.x == 0) {
     mbar_init(bar(L::B_KV), 1);
@@ -139,8 +156,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_arrive_expect_tx(bar(L::B_KV), 2 * L::TILE);
 #pragma unroll
       for (int c = 0; c < L::CH; ++c) {
-        tma_load_3d(sb + L::K + c * L::CHUNK, &tk, bar(L::B_KV), 64 * c, kt * kTile, bkv);
-        tma_load_3d(sb + L::V + c * L::CHUNK, &tv, bar(L::B_KV), 64 * c, kt * kTile, bkv);
+        tma_load_3d(sb + L::K + c * L::CHUNK, &tk, bar(L::B_KV), 64 * c, row0 + kt * kTile, zkv);
+        tma_load_3d(sb + L::V + c * L::CHUNK, &tv, bar(L::B_KV), 64 * c, row0 + kt * kTile, zkv);
       }
       uint32_t nq = 0, nd = 0;  // Q / dO copies issued
       bool ok = true;
@@ -156,7 +173,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
         for (int c = 0; c < L::CH; ++c)
           tma_load_3d(sb + L::QR + qpos * L::TILE + c * L::CHUNK, &tq, bar(L::B_QF + qpos), 64 * c,
-                      qt * kTile, bq0 + g);
+                      row0 + qt * kTile, bq0 + g);
         ++nq;
         if (dround > 0 && !wait_bar(bar(L::B_DOE + dpos), (dround - 1) & 1, wc)) {
           ok = false;
@@ -166,7 +183,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
         for (int c = 0; c < L::CH; ++c)
           tma_load_3d(sb + L::DOR + dpos * L::TILE + c * L::CHUNK, &tdo, bar(L::B_DOF + dpos),
-                      64 * c, qt * kTile, bq0 + g);
+                      64 * c, row0 + qt * kTile, bq0 + g);
         ++nd;
       }
       // let copies still in flight land before the CTA can exit
@@ -332,7 +349,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     bool have = sch.next(qt, g, p.lists);
     auto load_stats = [&](int t, int gg, float& l_, float& d_) {
       const int row = t * kTile + r;
-      const size_t idx = static_cast<size_t>(bq0 + gg) * N + (row < N ? row : 0);
+      const size_t idx = static_cast<size_t>(bq0 + gg) * slice_rows + row0 + (row < N ? row : 0);
       l_ = p.lse[idx];
       d_ = p.delta[idx];
     };
@@ -354,7 +371,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // Reduce-add through the TMA engine: the warp stages its 32 rows x 32
       // columns (4 KB, 128-byte swizzle) in its own rows of the dS buffer,
       // which no MMA reads between dQ's completion and the next dS, and lane 0
-      // adds the box into the fp32 accumulator (rows past N are clipped).
+      // adds the box into the fp32 accumulator (rows past the tensor are
+      // clipped; rows past this sequence but inside the tensor receive exact
+      // zeros, since their P and dS rows are 0).
       const uint32_t stage = dsbuf + q4 * 4096;
 #pragma unroll
       for (int c = 0; c < D / 64; ++c) {
@@ -369,7 +388,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         fence_async_smem();
         __syncwarp();
         if (lane == 0) {
-          tma_reduce_add_3d(&tdq, stage, (D / 2) * half + 32 * c, t * kTile + 32 * q4, bq0 + gg);
+          tma_reduce_add_3d(&tdq, stage, (D / 2) * half + 32 * c, row0 + t * kTile + 32 * q4,
+                            bq0 + gg);
           bulk_commit();
         }
       }
@@ -470,7 +490,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const uint32_t tcol = dv_side ? L::T_DV : L::T_DK;
       const float mul = dv_side ? 1.f : p.scale;
       uint8_t* dst = static_cast<uint8_t*>(dv_side ? p.dv : p.dk) +
-                     (static_cast<size_t>(bkv) * N + (key < N ? key : 0)) * static_cast<size_t>(D) * 2;
+                     (static_cast<size_t>(zkv) * slice_rows + row0 + (key < N ? key : 0)) *
+                         static_cast<size_t>(D) * 2;
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t a[32];
@@ -505,17 +526,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
 }
 
-template <int D, bool GQA>
+template <int D, int KIND>
 cudaError_t launch_bwd_d(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                          const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq,
                          cudaStream_t stream) {
   using L = BwdSmem<D>;
-  cudaError_t e = cudaFuncSetAttribute(fa_bwd_kernel<D, GQA>,
+  cudaError_t e = cudaFuncSetAttribute(fa_bwd_kernel<D, KIND>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
   if (e != cudaSuccess) return e;
   const int nT = (p.N + kTile - 1) / kTile;
   const long long ctas = static_cast<long long>(nT) * p.B * (p.Hkv > 0 ? p.Hkv : p.H);
-  fa_bwd_kernel<D, GQA><<<static_cast<unsigned>(ctas), kBwdThreads, L::ALLOC, stream>>>(
+  fa_bwd_kernel<D, KIND><<<static_cast<unsigned>(ctas), kBwdThreads, L::ALLOC, stream>>>(
       tq, tk, tv, tdo, tdq, p);
   return cudaGetLastError();
 }
@@ -525,13 +546,17 @@ cudaError_t launch_bwd_d(const BwdParams& p, const CUtensorMap& tq, const CUtens
 cudaError_t launch_backward_main(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                                  const CUtensorMap& tv, const CUtensorMap& tdo,
                                  const CUtensorMap& tdq, cudaStream_t stream) {
-  const bool gqa = p.Hkv > 0 && p.Hkv != p.H;
-  if (p.d == 64)
-    return gqa ? launch_bwd_d<64, true>(p, tq, tk, tv, tdo, tdq, stream)
-               : launch_bwd_d<64, false>(p, tq, tk, tv, tdo, tdq, stream);
-  if (p.d == 128)
-    return gqa ? launch_bwd_d<128, true>(p, tq, tk, tv, tdo, tdq, stream)
-               : launch_bwd_d<128, false>(p, tq, tk, tv, tdo, tdq, stream);
+  const int kind = p.cu_seqlens ? kGeneral : (p.Hkv > 0 && p.Hkv != p.H) ? kGrouped : kPlain;
+  if (p.d == 64) {
+    if (kind == kGeneral) return launch_bwd_d<64, kGeneral>(p, tq, tk, tv, tdo, tdq, stream);
+    if (kind == kGrouped) return launch_bwd_d<64, kGrouped>(p, tq, tk, tv, tdo, tdq, stream);
+    return launch_bwd_d<64, kPlain>(p, tq, tk, tv, tdo, tdq, stream);
+  }
+  if (p.d == 128) {
+    if (kind == kGeneral) return launch_bwd_d<128, kGeneral>(p, tq, tk, tv, tdo, tdq, stream);
+    if (kind == kGrouped) return launch_bwd_d<128, kGrouped>(p, tq, tk, tv, tdo, tdq, stream);
+    return launch_bwd_d<128, kPlain>(p, tq, tk, tv, tdo, tdq, stream);
+  }
   return cudaErrorInvalidValue;
 }
 

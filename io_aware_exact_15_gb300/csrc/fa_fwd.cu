@@ -61,7 +61,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleLog2 = 8.0f;  // lazy rescale threshold (factor 256)
 
-template <int D, bool GQA, int NS_>
+template <int D, int KIND, int NS_>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const FwdParams p) {
@@ -75,19 +75,35 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::MISC + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int N = p.N;
-  const int nT = (N + kTile - 1) / kTile;
   // one query tile per CTA only in the tile-sweep instantiations (NS_ != 0)
   const bool single = NS_ != 0 && p.single_tile != 0;
-  const int npairs = single ? nT : (nT + 1) / 2;
+  const int ntmax = (p.N + kTile - 1) / kTile;
+  const int npairs = single ? ntmax : (ntmax + 1) / 2;
   const int BH = p.B * p.H;
   int bh, pair;
   fwd_cta_coords(blockIdx.x, BH, npairs, p.causal != 0, bh, pair);
   const int head = bh % p.H;
-  // key/value slice this query head reads: grouped K/V has H / Hkv query
-  // heads per key/value head, and bh / (H / Hkv) = b * Hkv + h / (H / Hkv).
+  // Sequence geometry: length N, first row row0 of the sequence in its
+  // slice, the TMA slices zq (Q, O) and zkv (K, V).  Grouped K/V has H / Hkv
+  // query heads per key/value head: bh / (H / Hkv) = b * Hkv + h / (H / Hkv).
   // The plain instantiation carries no index arithmetic at all.
-  const int bhkv = GQA ? bh / (p.H / p.Hkv) : bh;
+  int N = p.N, row0 = 0, zq = bh, zkv = bh;
+  if (KIND == kGrouped) zkv = bh / (p.H / p.Hkv);
+  if (KIND == kGeneral) {
+    // variable-length batch: slices are heads, sequences are row ranges
+    // (indices clamped to [0, total], so bad offsets cannot write outside)
+    const int b = bh / p.H;
+    const int a = min(max(p.cu_seqlens[b], 0), p.total);
+    const int e = min(max(p.cu_seqlens[b + 1], a), p.total);
+    row0 = a;
+    N = min(e - a, p.N);
+    zq = head;
+    zkv = head / (p.H / p.Hkv);
+    if ((single ? pair : 2 * pair) * kTile >= N) return;  // no query tile here (CTA-uniform)
+  }
+  const size_t slice_rows = KIND == kGeneral ? static_cast<size_t>(p.total)
+                                             : static_cast<size_t>(p.N);
+  const int nT = (N + kTile - 1) / kTile;
 
   if (threadIdx.x == 0) {
     mbar_init(bar(L::B_Q), 1);
@@ -127,8 +143,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       mbar_arrive_expect_tx(bar(L::B_Q), 2 * L::TILE);
 #pragma unroll
       for (int c = 0; c < L::CH; ++c) {
-        tma_load_3d(sb + L::Q + c * L::CHUNK, &tq, bar(L::B_Q), 64 * c, y0, bh);
-        tma_load_3d(sb + L::Q + L::TILE + c * L::CHUNK, &tq, bar(L::B_Q), 64 * c, y1, bh);
+        tma_load_3d(sb + L::Q + c * L::CHUNK, &tq, bar(L::B_Q), 64 * c, row0 + y0, zq);
+        tma_load_3d(sb + L::Q + L::TILE + c * L::CHUNK, &tq, bar(L::B_Q), 64 * c, row0 + y1, zq);
       }
       uint32_t idx = 0;
       bool ok = true;
@@ -145,7 +161,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 #pragma unroll
           for (int c = 0; c < L::CH; ++c)
             tma_load_3d(sb + L::KV + pos * L::TILE + c * L::CHUNK, t == 0 ? &tk : &tv,
-                        bar(L::B_KVF + pos), 64 * c, kt * kTile, bhkv);
+                        bar(L::B_KVF + pos), 64 * c, row0 + kt * kTile, zkv);
           ++idx;
         }
       }
@@ -348,7 +364,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     tc_fence_after();
     if (ok && active) {
       uint8_t* orow = static_cast<uint8_t*>(p.o) +
-                      (static_cast<size_t>(bh) * N + qrow) * static_cast<size_t>(D) * 2;
+                      (static_cast<size_t>(zq) * slice_rows + row0 + qrow) * static_cast<size_t>(D) * 2;
       const bool store = qrow < N;
       const bool has = cnt > 0 && l > 0.f;
       const float inv = has ? 1.f / l : 0.f;
@@ -376,7 +392,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           }
         }
       }
-      if (store) p.lse[static_cast<size_t>(bh) * N + qrow] = has ? (m + lg2(l)) * kLn2 : -INFINITY;
+      if (store)
+        p.lse[static_cast<size_t>(zq) * slice_rows + row0 + qrow] =
+            has ? (m + lg2(l)) * kLn2 : -INFINITY;
     }
   }
   tc_fence_before();
@@ -387,17 +405,17 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   }
 }
 
-template <int D, bool GQA, int NS_ = 0>
+template <int D, int KIND, int NS_ = 0>
 cudaError_t launch_fwd_d(const FwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                          const CUtensorMap& tv, cudaStream_t stream) {
   using L = FwdSmem<D, NS_>;
-  cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<D, GQA, NS_>,
+  cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<D, KIND, NS_>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
   if (e != cudaSuccess) return e;
   const int nT = (p.N + kTile - 1) / kTile;
   const int npairs = (NS_ != 0 && p.single_tile) ? nT : (nT + 1) / 2;
   const long long ctas = static_cast<long long>(npairs) * p.B * p.H;
-  fa_fwd_kernel<D, GQA, NS_>
+  fa_fwd_kernel<D, KIND, NS_>
       <<<static_cast<unsigned>(ctas), kFwdThreads, L::ALLOC, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
@@ -408,16 +426,16 @@ cudaError_t launch_forward_config(const FwdParams& p, const CUtensorMap& tq, con
                                   const CUtensorMap& tv, int kv_stages, cudaStream_t stream) {
   if (p.d == 128) {
     switch (kv_stages) {
-      case 2: return launch_fwd_d<128, false, 2>(p, tq, tk, tv, stream);
-      case 3: return launch_fwd_d<128, false, 3>(p, tq, tk, tv, stream);
-      case 4: return launch_fwd_d<128, false, 4>(p, tq, tk, tv, stream);
-      case 5: return launch_fwd_d<128, false, 5>(p, tq, tk, tv, stream);
+      case 2: return launch_fwd_d<128, kPlain, 2>(p, tq, tk, tv, stream);
+      case 3: return launch_fwd_d<128, kPlain, 3>(p, tq, tk, tv, stream);
+      case 4: return launch_fwd_d<128, kPlain, 4>(p, tq, tk, tv, stream);
+      case 5: return launch_fwd_d<128, kPlain, 5>(p, tq, tk, tv, stream);
     }
   } else if (p.d == 64) {
     switch (kv_stages) {
-      case 2: return launch_fwd_d<64, false, 2>(p, tq, tk, tv, stream);
-      case 4: return launch_fwd_d<64, false, 4>(p, tq, tk, tv, stream);
-      case 8: return launch_fwd_d<64, false, 8>(p, tq, tk, tv, stream);
+      case 2: return launch_fwd_d<64, kPlain, 2>(p, tq, tk, tv, stream);
+      case 4: return launch_fwd_d<64, kPlain, 4>(p, tq, tk, tv, stream);
+      case 8: return launch_fwd_d<64, kPlain, 8>(p, tq, tk, tv, stream);
     }
   }
   return cudaErrorInvalidValue;
@@ -425,13 +443,17 @@ cudaError_t launch_forward_config(const FwdParams& p, const CUtensorMap& tq, con
 
 cudaError_t launch_forward(const FwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                            const CUtensorMap& tv, cudaStream_t stream) {
-  const bool gqa = p.Hkv > 0 && p.Hkv != p.H;
-  if (p.d == 64)
-    return gqa ? launch_fwd_d<64, true>(p, tq, tk, tv, stream)
-               : launch_fwd_d<64, false>(p, tq, tk, tv, stream);
-  if (p.d == 128)
-    return gqa ? launch_fwd_d<128, true>(p, tq, tk, tv, stream)
-               : launch_fwd_d<128, false>(p, tq, tk, tv, stream);
+  const int kind = p.cu_seqlens ? kGeneral : (p.Hkv > 0 && p.Hkv != p.H) ? kGrouped : kPlain;
+  if (p.d == 64) {
+    if (kind == kGeneral) return launch_fwd_d<64, kGeneral>(p, tq, tk, tv, stream);
+    if (kind == kGrouped) return launch_fwd_d<64, kGrouped>(p, tq, tk, tv, stream);
+    return launch_fwd_d<64, kPlain>(p, tq, tk, tv, stream);
+  }
+  if (p.d == 128) {
+    if (kind == kGeneral) return launch_fwd_d<128, kGeneral>(p, tq, tk, tv, stream);
+    if (kind == kGrouped) return launch_fwd_d<128, kGrouped>(p, tq, tk, tv, stream);
+    return launch_fwd_d<128, kPlain>(p, tq, tk, tv, stream);
+  }
   return cudaErrorInvalidValue;
 }
 

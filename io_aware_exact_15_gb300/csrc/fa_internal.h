@@ -31,6 +31,10 @@ struct FwdParams {
   int causal = 0;
   TileLists lists;        // sparse when lists.row_ptr != nullptr
   int single_tile = 0;    // 1: one 128-row query tile per CTA instead of two
+  // variable-length batch: tensors [H, total, d], sequence b in rows
+  // cu_seqlens[b] .. cu_seqlens[b+1] (N is then the longest sequence)
+  const int* cu_seqlens = nullptr;
+  int total = 0;
   int* err = nullptr;     // device status word
   uint64_t wait_ns = 0;
 };
@@ -46,9 +50,15 @@ struct BwdParams {
   float scale = 0.f;
   int causal = 0;
   TileLists lists;              // sparse when lists.col_ptr != nullptr
+  const int* cu_seqlens = nullptr;  // variable-length batch (as FwdParams)
+  int total = 0;
   int* err = nullptr;
   uint64_t wait_ns = 0;
 };
+
+// Kernel instantiations: plain, grouped K/V, and the general one
+// (variable-length batch, grouped K/V allowed).
+enum KernelKind : int { kPlain = 0, kGrouped = 1, kGeneral = 2 };
 
 // 3-D bf16 view {d, N, B*H} of a [B, H, N, d] tensor, 128-row x 64-column
 // boxes with 128-byte swizzle.

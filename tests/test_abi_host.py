@@ -128,3 +128,32 @@ def test_gqa_rejects_bad_groups():
             fa.FA_ERR_INVALID_ARG
         assert fa.fa_backward_gqa(A, A, A, A, A, A, A, A, A, 1, 6, Hkv, 128, 64, 0.1, 0, A, need,
                                   0) == fa.FA_ERR_INVALID_ARG
+
+
+def test_varlen_rejects_bad_args():
+    A = ALIGNED
+    need = fa.fa_backward_workspace_size(1, 4, 1000, 64)
+    # (cu, B, max_seqlen, total, H, Hkv, d, scale) -> status
+    cases = [
+        ((None, 2, 512, 1000, 4, 4, 64, 0.1), fa.FA_ERR_INVALID_ARG),
+        ((A + 2, 2, 512, 1000, 4, 4, 64, 0.1), fa.FA_ERR_MISALIGNED),
+        ((A, 0, 512, 1000, 4, 4, 64, 0.1), fa.FA_ERR_INVALID_ARG),
+        ((A, 2, 0, 1000, 4, 4, 64, 0.1), fa.FA_ERR_INVALID_ARG),
+        ((A, 2, 1001, 1000, 4, 4, 64, 0.1), fa.FA_ERR_INVALID_ARG),
+        ((A, 2, 512, -1, 4, 4, 64, 0.1), fa.FA_ERR_INVALID_ARG),
+        ((A, 2, 512, 1000, 4, 3, 64, 0.1), fa.FA_ERR_INVALID_ARG),
+        ((A, 2, 512, 1000, 4, 4, 96, 0.1), fa.FA_ERR_UNSUPPORTED),
+        ((A, 2, 512, 1000, 4, 4, 64, 0.0), fa.FA_ERR_INVALID_ARG),
+        ((A, 2, 512, 1 << 24, 1024, 1024, 128, 0.1), fa.FA_ERR_UNSUPPORTED),
+    ]
+    for (cu, B, ms, T, H, Hkv, d, sc), want in cases:
+        assert fa.fa_forward_varlen(A, A, A, A, A, cu, B, ms, T, H, Hkv, d, sc, 0, 0) == want, \
+            (cu, B, ms, T)
+        assert fa.fa_backward_varlen(A, A, A, A, A, A, A, A, A, cu, B, ms, T, H, Hkv, d, sc, 0, A,
+                                     need, 0) == want
+    base = (A, 2, 512, 1000, 4, 4, 64, 0.1, 0)
+    assert fa.fa_forward_varlen(MIS, A, A, A, A, *base, 0) == fa.FA_ERR_MISALIGNED
+    assert fa.fa_backward_varlen(A, A, A, A, A, A, A, A, A, *base, A, need - 1, 0) == \
+        fa.FA_ERR_WORKSPACE
+    assert fa.fa_backward_varlen(A, A, A, A, A, A, A, A, A, *base, A + 16, need, 0) == \
+        fa.FA_ERR_MISALIGNED
