@@ -19,6 +19,11 @@ Parity status of each function (what pins it, tests/test_oracle_pins.py):
   grouped K/V      pinned: equals the pinned per-head path on repeated K/V,
                    group sums of its key gradients, finite differences through
                    a shared key/value row
+  dropout          pinned: Philox4x32-10 known-answer vectors (through the
+                   per-element byte mapping), keep-rate statistics, p = 0 is
+                   exactly the undropped oracle, a closed-form two-key case,
+                   finite differences of the dropped forward, and the mean
+                   over seeds converging to the undropped output
   mask_lists       pinned: hand-derived golden lists, CSR/CSC transposition
   tile_counts      pinned: closed forms n(n+1)/2 and n^2, nnz of the mask
 """
@@ -63,11 +68,18 @@ def _load():
         ip = ctypes.POINTER(ctypes.c_int)
         u8p = ctypes.POINTER(ctypes.c_ubyte)
         L, I, D = ctypes.c_long, ctypes.c_int, ctypes.c_double
-        lib.fao_forward.argtypes = [dp, dp, dp, L, L, L, L, L, D, I, u8p, L, L, lp, L, dp, dp, I]
+        F, U64, U32 = ctypes.c_float, ctypes.c_uint64, ctypes.c_uint32
+        u32p = ctypes.POINTER(ctypes.c_uint32)
+        lib.fao_forward.argtypes = [dp, dp, dp, L, L, L, L, L, D, I, u8p, L, L, lp, L, dp, dp,
+                                    F, U64, U32, L, I]
         lib.fao_forward.restype = I
         lib.fao_backward.argtypes = [dp, dp, dp, dp, L, L, L, L, L, D, I, u8p, L, L, lp, L, lp,
-                                     L, dp, dp, dp, I]
+                                     L, dp, dp, dp, F, U64, U32, L, I]
         lib.fao_backward.restype = I
+        lib.fao_philox4x32_10.argtypes = [u32p, u32p, u32p]
+        lib.fao_philox4x32_10.restype = None
+        lib.fao_dropout_bytes.argtypes = [U64, U32, U64, U64, U64, L, u8p]
+        lib.fao_dropout_bytes.restype = None
         lib.fao_mask_lists.argtypes = [u8p, L, L, ip, ip, ip, ip]
         lib.fao_mask_lists.restype = I
         lib.fao_tile_counts.argtypes = [L, L, I, u8p, L, lp]
@@ -111,14 +123,61 @@ def _rows(rows):
     return _ptr(r, ctypes.c_long), len(r), r
 
 
-def forward(q, k, v, scale, causal=False, block_mask=None, tile=TILE, rows=None, nthreads=None):
+def _drop_args(dropout, batch0=0):
+    """(p, seed, offset, batch0) for the C calls; dropout = None or
+    (p, seed, offset) with p in [0, 1) taken in float32."""
+    if dropout is None:
+        return 0.0, 0, 0, 0
+    p, seed, offset = dropout
+    return float(np.float32(p)), int(seed), int(offset), int(batch0)
+
+
+def philox4x32_10(counter, key):
+    """Philox4x32-10 of a 4-word counter and a 2-word key (uint32 each)."""
+    c = np.ascontiguousarray(np.asarray(counter, dtype=np.uint32).reshape(4))
+    k_ = np.ascontiguousarray(np.asarray(key, dtype=np.uint32).reshape(2))
+    out = np.zeros(4, dtype=np.uint32)
+    _load().fao_philox4x32_10(_ptr(c, ctypes.c_uint32), _ptr(k_, ctypes.c_uint32),
+                              _ptr(out, ctypes.c_uint32))
+    return out
+
+
+def dropout_bytes(seed, offset, bhc, i, j0, count):
+    """Random bytes of dropout elements (bhc, i, j0 .. j0+count-1), where
+    bhc = b * H + h; element (i, j) is kept iff its byte >= rint(256 p)."""
+    out = np.zeros(int(count), dtype=np.uint8)
+    _load().fao_dropout_bytes(int(seed), int(offset), int(bhc), int(i), int(j0), int(count),
+                              _ptr(out, ctypes.c_ubyte))
+    return out
+
+
+def dropout_threshold(p):
+    """t = rint(256 p), p taken in float32: kept iff byte >= t."""
+    return int(np.rint(256.0 * float(np.float32(p))))
+
+
+def dropout_keep(seed, offset, p, B, H, N, batch0=0):
+    """Keep indicator z [B, H, N, N] (uint8) of the dropout definition."""
+    t = dropout_threshold(p)
+    z = np.zeros((B, H, N, N), dtype=np.uint8)
+    for b in range(B):
+        for h in range(H):
+            for i in range(N):
+                z[b, h, i] = dropout_bytes(seed, offset, (batch0 + b) * H + h, i, 0, N) >= t
+    return z
+
+
+def forward(q, k, v, scale, causal=False, block_mask=None, tile=TILE, rows=None, nthreads=None,
+            dropout=None, batch0=0):
     """O and natural-log lse of softmax(scale*QK^T + mask) V in fp64.
 
     q: [B, H, N, d]; k, v: [B, Hkv, N, d] with H a multiple of Hkv (query
     head h reads key/value head h // (H // Hkv)).  block_mask: [1 or H, nT,
     nT] (nonzero keeps the tile), nT = ceil(N / tile).  rows: optional query
-    rows evaluated in every head.  Returns o [B, H, R, d] and lse [B, H, R]
-    (R = N or len(rows)).
+    rows evaluated in every head.  dropout: None or (p, seed, offset):
+    inverted dropout of P with the Philox keep rule of fa_oracle.c (batch b
+    enters the counter as batch0 + b).  Returns o [B, H, R, d] and lse
+    [B, H, R] (R = N or len(rows)).
     """
     q, k, v = _f64(q), _f64(k), _f64(v)
     B, H, N, d = q.shape
@@ -133,19 +192,19 @@ def forward(q, k, v, scale, causal=False, block_mask=None, tile=TILE, rows=None,
                              int(bool(causal)),
                              None if m is None else _ptr(m, ctypes.c_ubyte), mh, tile, rp, nr,
                              _ptr(o, ctypes.c_double), _ptr(lse, ctypes.c_double),
-                             _threads(nthreads))
+                             *_drop_args(dropout, batch0), _threads(nthreads))
     if st != 0:
         raise ValueError(f"oracle forward rejected its arguments ({st})")
     return o, lse
 
 
 def backward(q, k, v, do, scale, causal=False, block_mask=None, tile=TILE, qrows=None,
-             krows=None, nthreads=None):
+             krows=None, nthreads=None, dropout=None, batch0=0):
     """dQ, dK, dV of sum(O * dO) for O = softmax(scale*QK^T + mask) V, fp64.
 
     qrows / krows: optional query / key rows evaluated in every head.  With
     k, v of Hkv < H heads, dk and dv sum over the query heads of each group.
-    Returns dq [B,H,Rq,d], dk [B,Hkv,Rk,d], dv [B,Hkv,Rk,d].
+    dropout, batch0: as forward.  Returns dq [B,H,Rq,d], dk [B,Hkv,Rk,d], dv [B,Hkv,Rk,d].
     """
     q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
     B, H, N, d = q.shape
@@ -163,7 +222,8 @@ def backward(q, k, v, do, scale, causal=False, block_mask=None, tile=TILE, qrows
                               float(scale), int(bool(causal)),
                               None if m is None else _ptr(m, ctypes.c_ubyte), mh, tile, qp, nq, kp,
                               nk, _ptr(dq, ctypes.c_double), _ptr(dk, ctypes.c_double),
-                              _ptr(dv, ctypes.c_double), _threads(nthreads))
+                              _ptr(dv, ctypes.c_double), *_drop_args(dropout, batch0),
+                              _threads(nthreads))
     if st != 0:
         raise ValueError(f"oracle backward failed ({st})")
     return dq, dk, dv
@@ -219,36 +279,36 @@ def _seq_bounds(cu_seqlens):
     return cu
 
 
-def forward_varlen(q, k, v, cu_seqlens, scale, causal=False, nthreads=None):
+def forward_varlen(q, k, v, cu_seqlens, scale, causal=False, nthreads=None, dropout=None):
     """Packed variable-length batch: q, k, v are [H, T, d] with sequence b
     in tokens cu_seqlens[b] .. cu_seqlens[b+1]; attention stays inside each
     sequence (the padding-mask benchmark of the summary's section 4.4).
-    Evaluates the per-sequence definition above.  Returns o [H, T, d] and
-    lse [H, T]."""
+    Evaluates the per-sequence definition above; with dropout, sequence b
+    is batch b of the dropout counter.  Returns o [H, T, d] and lse [H, T]."""
     q, k, v = (np.asarray(x, dtype=np.float64) for x in (q, k, v))
     cu = _seq_bounds(cu_seqlens)
     H, T, d = q.shape
     o = np.zeros((H, T, d))
     lse = np.full((H, T), -np.inf)
-    for a, b in zip(cu, cu[1:]):
+    for s, (a, b) in enumerate(zip(cu, cu[1:])):
         if b == a:
             continue
         ob, lb = forward(q[None, :, a:b], k[None, :, a:b], v[None, :, a:b], scale, causal=causal,
-                         nthreads=nthreads)
+                         nthreads=nthreads, dropout=dropout, batch0=s)
         o[:, a:b] = ob[0]
         lse[:, a:b] = lb[0]
     return o, lse
 
 
-def backward_varlen(q, k, v, do, cu_seqlens, scale, causal=False, nthreads=None):
+def backward_varlen(q, k, v, do, cu_seqlens, scale, causal=False, nthreads=None, dropout=None):
     """Gradients of sum(O * dO) for forward_varlen; each [H, T, d]."""
     q, k, v, do = (np.asarray(x, dtype=np.float64) for x in (q, k, v, do))
     cu = _seq_bounds(cu_seqlens)
     dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
-    for a, b in zip(cu, cu[1:]):
+    for s, (a, b) in enumerate(zip(cu, cu[1:])):
         if b == a:
             continue
         g = backward(q[None, :, a:b], k[None, :, a:b], v[None, :, a:b], do[None, :, a:b], scale,
-                     causal=causal, nthreads=nthreads)
+                     causal=causal, nthreads=nthreads, dropout=dropout, batch0=s)
         dq[:, a:b], dk[:, a:b], dv[:, a:b] = g[0][0], g[1][0], g[2][0]
     return dq, dk, dv

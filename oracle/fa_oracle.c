@@ -35,6 +35,22 @@
  * value row gets the sum of the gradients of every query head that reads it
  * (chain rule over the shared parameter).  Hkv = H is ordinary attention.
  *
+ * Dropout on P (the summary fuses dropout into the kernel, "Kernel Fusion",
+ * and benchmarks with it, section 4.4; it names no generator and no
+ * scaling).  Reading taken: inverted dropout of the attention weights,
+ *   P~_ij = z_ij * P_ij / (1 - p'),   O = P~ V,
+ * with lse still the statistic of the undropped row.  The keep indicator
+ * z_ij comes from a counter-based generator, Philox4x32-10 (Salmon, Moraes,
+ * Dror, Shaw, "Parallel random numbers: as easy as 1, 2, 3", SC 2011):
+ *   counter = (j / 16, i, b * H + h, offset),  key = (seed mod 2^32, seed / 2^32)
+ *   byte    = byte (j mod 4) of output word ((j / 4) mod 4), little-endian
+ *   z_ij    = byte >= t,   t = rint(256 * p) with p taken in float32
+ * so the effective drop probability is p' = t / 256 and kept weights are
+ * scaled by 1 / (1 - p') = 256 / (256 - t).  i and j are row indices within
+ * the sequence and b the batch (sequence) index.  The chain rule then gives
+ *   dV = P~^T dO,  dP_ij = z_ij <dO_i, v_j> / (1 - p'),
+ *   D_i = sum_j P_ij dP_ij,  dS = P o (dP - D),  dQ = scale dS K,  dK = scale dS^T Q.
+ *
  * Every loop is a straight restatement of a sum in the definition, in fp64,
  * summed in index order.  Work is split over independent (head, row-block)
  * units with POSIX threads; that changes nothing in any sum.
@@ -54,7 +70,52 @@ typedef struct {
   const unsigned char *mask; /* [mask_heads, nT, nT] or NULL */
   long mask_heads, tile, nT;
   long Hkv;
+  /* dropout: t = 0 means none */
+  unsigned t;
+  double keep_scale; /* 256 / (256 - t) */
+  uint64_t seed;
+  uint32_t offset;
+  long batch0; /* batch index of b = 0 in the dropout counter */
 } problem_t;
+
+/* ---------------------------------------------------------------------- */
+/* Philox4x32-10: ten rounds of the Philox S-box on a 128-bit counter; round
+ * r uses the key plus r times the Weyl increments.                        */
+static void philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4]) {
+  const uint64_t M0 = 0xD2511F53u, M1 = 0xCD9E8D57u;
+  const uint32_t W0 = 0x9E3779B9u, W1 = 0xBB67AE85u;
+  uint32_t c0 = ctr[0], c1 = ctr[1], c2 = ctr[2], c3 = ctr[3];
+  uint32_t k0 = key[0], k1 = key[1];
+  for (int r = 0; r < 10; ++r) {
+    uint64_t p0 = M0 * (uint64_t)c0; /* hi:lo of M0 * c0 */
+    uint64_t p1 = M1 * (uint64_t)c2;
+    uint32_t hi0 = (uint32_t)(p0 >> 32), lo0 = (uint32_t)p0;
+    uint32_t hi1 = (uint32_t)(p1 >> 32), lo1 = (uint32_t)p1;
+    uint32_t n0 = hi1 ^ c1 ^ k0, n1 = lo1, n2 = hi0 ^ c3 ^ k1, n3 = lo0;
+    c0 = n0; c1 = n1; c2 = n2; c3 = n3;
+    k0 += W0;
+    k1 += W1;
+  }
+  out[0] = c0; out[1] = c1; out[2] = c2; out[3] = c3;
+}
+
+/* random byte of element (bhc, i, j) of the dropout stream */
+static unsigned keep_byte(uint64_t seed, uint32_t offset, uint64_t bhc, uint64_t i, uint64_t j) {
+  uint32_t ctr[4] = {(uint32_t)(j >> 4), (uint32_t)i, (uint32_t)bhc, offset};
+  uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
+  uint32_t r[4];
+  philox4x32_10(ctr, key, r);
+  return (r[(j >> 2) & 3] >> (8 * (j & 3))) & 0xFFu;
+}
+
+/* dropout factor z_ij / (1 - p') of query slice bh, or 1 without dropout */
+static double drop_factor(const problem_t *p, long bh, long i, long j) {
+  if (p->t == 0) return 1.0;
+  long b = bh / p->H, h = bh % p->H;
+  uint64_t bhc = (uint64_t)((p->batch0 + b) * p->H + h);
+  return keep_byte(p->seed, p->offset, bhc, (uint64_t)i, (uint64_t)j) >= p->t ? p->keep_scale
+                                                                               : 0.0;
+}
 
 /* (batch, key/value head) slice that query slice bh reads */
 static long kv_slice(const problem_t *p, long bh) {
@@ -152,7 +213,7 @@ static double row_forward(const problem_t *p, long bh, long i, double *o_row) {
     for (long j = 0; j < p->N; ++j) {
       if (!allowed(p, h, i, j)) continue;
       double s = p->scale * dot(qi, K + j * p->d, p->d);
-      double pij = exp(s - lse);
+      double pij = exp(s - lse) * drop_factor(p, bh, i, j);
       const double *vj = V + j * p->d;
       for (long c = 0; c < p->d; ++c) o_row[c] += pij * vj[c];
     }
@@ -160,7 +221,7 @@ static double row_forward(const problem_t *p, long bh, long i, double *o_row) {
   return lse;
 }
 
-/* D_i = sum_j P_ij dP_ij with dP_ij = <dO_i, v_j>. */
+/* D_i = sum_j P_ij dP_ij with dP_ij = z_ij <dO_i, v_j> / (1 - p'). */
 static double row_delta(const problem_t *p, long bh, long i, double lse) {
   if (lse == -INFINITY) return 0.0;
   long h = bh % p->H;
@@ -172,7 +233,7 @@ static double row_delta(const problem_t *p, long bh, long i, double lse) {
   for (long j = 0; j < p->N; ++j) {
     if (!allowed(p, h, i, j)) continue;
     double pij = exp(p->scale * dot(qi, K + j * p->d, p->d) - lse);
-    D += pij * dot(doi, V + j * p->d, p->d);
+    D += pij * drop_factor(p, bh, i, j) * dot(doi, V + j * p->d, p->d);
   }
   return D;
 }
@@ -201,6 +262,16 @@ static void fwd_unit(void *vctx, long unit) {
   }
 }
 
+/* t = rint(256 p) for p in [0, 1); t = 256 (everything dropped) is refused */
+static int set_dropout(problem_t *p, float p_drop) {
+  if (!(p_drop >= 0.0f && p_drop < 1.0f)) return 1;
+  double t = nearbyint(256.0 * (double)p_drop);
+  if (t >= 256.0) return 1;
+  p->t = (unsigned)t;
+  p->keep_scale = 256.0 / (256.0 - t);
+  return 0;
+}
+
 static int check_problem(const problem_t *p) {
   if (p->B < 1 || p->H < 1 || p->N < 1 || p->d < 1) return 1;
   if (p->Hkv < 1 || p->H % p->Hkv != 0) return 1;
@@ -214,9 +285,11 @@ static int check_problem(const problem_t *p) {
 int fao_forward(const double *q, const double *k, const double *v, long B, long H, long Hkv,
                 long N, long d, double scale, int causal, const unsigned char *mask,
                 long mask_heads, long tile, const long *rows, long nrows, double *o, double *lse,
-                int nthreads) {
-  problem_t p = {q, k, v, NULL, B, H, N, d, scale, causal, mask, mask_heads, tile, 0, Hkv};
+                float p_drop, uint64_t seed, uint32_t offset, long batch0, int nthreads) {
+  problem_t p = {q, k, v, NULL, B, H, N, d, scale, causal, mask, mask_heads, tile, 0, Hkv,
+                 0, 1.0, seed, offset, batch0};
   if (mask) p.nT = (N + tile - 1) / tile;
+  if (set_dropout(&p, p_drop)) return 1;
   if (check_problem(&p)) return 1;
   if (!rows) nrows = N;
   for (long r = 0; rows && r < nrows; ++r)
@@ -275,14 +348,14 @@ static void bwd_dq_unit(void *vctx, long unit) {
     for (long j = 0; j < p->N; ++j) {
       if (!allowed(p, h, i, j)) continue;
       double pij = exp(p->scale * dot(qi, K + j * p->d, p->d) - lse);
-      double dpij = dot(doi, V + j * p->d, p->d);
+      double dpij = drop_factor(p, bh, i, j) * dot(doi, V + j * p->d, p->d);
       double dsij = pij * (dpij - D);
       for (long cc = 0; cc < p->d; ++cc) dqi[cc] += p->scale * dsij * K[j * p->d + cc];
     }
   }
 }
 
-/* dK_j = scale * sum_i dS_ij q_i,  dV_j = sum_i P_ij dO_i, summed over every
+/* dK_j = scale * sum_i dS_ij q_i,  dV_j = sum_i P~_ij dO_i, summed over every
  * query head that reads key/value head j belongs to */
 static void bwd_dkdv_unit(void *vctx, long unit) {
   bwd_ctx_t *c = (bwd_ctx_t *)vctx;
@@ -308,11 +381,12 @@ static void bwd_dkdv_unit(void *vctx, long unit) {
         if (!allowed(p, h, i, j)) continue;
         double lse = c->lse_all[bh * p->N + i], D = c->D_all[bh * p->N + i];
         double pij = exp(p->scale * dot(Q + i * p->d, kj, p->d) - lse);
-        double dpij = dot(dO + i * p->d, vj, p->d);
+        double zf = drop_factor(p, bh, i, j);
+        double dpij = zf * dot(dO + i * p->d, vj, p->d);
         double dsij = pij * (dpij - D);
         for (long cc = 0; cc < p->d; ++cc) {
           dkj[cc] += p->scale * dsij * Q[i * p->d + cc];
-          dvj[cc] += pij * dO[i * p->d + cc];
+          dvj[cc] += pij * zf * dO[i * p->d + cc];
         }
       }
     }
@@ -325,9 +399,12 @@ static void bwd_dkdv_unit(void *vctx, long unit) {
 int fao_backward(const double *q, const double *k, const double *v, const double *dO, long B,
                  long H, long Hkv, long N, long d, double scale, int causal,
                  const unsigned char *mask, long mask_heads, long tile, const long *qrows, long nq,
-                 const long *krows, long nk, double *dq, double *dk, double *dv, int nthreads) {
-  problem_t p = {q, k, v, dO, B, H, N, d, scale, causal, mask, mask_heads, tile, 0, Hkv};
+                 const long *krows, long nk, double *dq, double *dk, double *dv, float p_drop,
+                 uint64_t seed, uint32_t offset, long batch0, int nthreads) {
+  problem_t p = {q, k, v, dO, B, H, N, d, scale, causal, mask, mask_heads, tile, 0, Hkv,
+                 0, 1.0, seed, offset, batch0};
   if (mask) p.nT = (N + tile - 1) / tile;
+  if (set_dropout(&p, p_drop)) return 1;
   if (check_problem(&p)) return 1;
   if (!qrows) nq = N;
   if (!krows) nk = N;
@@ -443,4 +520,16 @@ int fao_tile_counts(long N, long tile, int causal, const unsigned char *mask, lo
     }
   }
   return 0;
+}
+
+/* ---------------------------------------------------------------------- */
+/* the dropout generator, exported for its known-answer pins               */
+void fao_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4]) {
+  philox4x32_10(ctr, key, out);
+}
+
+/* random bytes of elements (bhc, i, j0 + n), n < count */
+void fao_dropout_bytes(uint64_t seed, uint32_t offset, uint64_t bhc, uint64_t i, uint64_t j0,
+                       long count, unsigned char *out) {
+  for (long n = 0; n < count; ++n) out[n] = (unsigned char)keep_byte(seed, offset, bhc, i, j0 + n);
 }
