@@ -140,6 +140,8 @@ def run_gpu(args, rank, world, dist):
     Hkv = w.kv_heads
     varlen = w.varlen
     gqa = Hkv != H
+    drop = (w.dropout, W.DROPOUT_SEED, 0)
+    combined = varlen or gqa or w.dropout > 0  # no split backward entry point
     if varlen:
         q, k, v, do, cu = W.make_varlen_inputs(w, with_do=True)
         mask = None
@@ -181,7 +183,10 @@ def run_gpu(args, rank, world, dist):
     def forward():
         if varlen:
             check(fa.fa_forward_varlen(qd, kd, vd, o, lse, cud, B, max_seqlen, T, H, Hkv, d,
-                                       w.scale, w.causal, s_ptr), "forward")
+                                       w.scale, w.causal, *drop, s_ptr), "forward")
+        elif w.dropout > 0:
+            check(fa.fa_forward_dropout(qd, kd, vd, o, lse, B, H, N, d, w.scale, w.causal, *drop,
+                                        s_ptr), "forward")
         elif gqa:
             check(fa.fa_forward_gqa(qd, kd, vd, o, lse, B, H, Hkv, N, d, w.scale, w.causal,
                                     s_ptr), "forward")
@@ -192,8 +197,11 @@ def run_gpu(args, rank, world, dist):
     def backward_whole():
         if varlen:
             check(fa.fa_backward_varlen(qd, kd, vd, o, dod, lse, dq, dk, dv, cud, B, max_seqlen,
-                                        T, H, Hkv, d, w.scale, w.causal, ws, nbytes, s_ptr),
-                  "backward")
+                                        T, H, Hkv, d, w.scale, w.causal, *drop, ws, nbytes,
+                                        s_ptr), "backward")
+        elif w.dropout > 0:
+            check(fa.fa_backward_dropout(qd, kd, vd, o, dod, lse, dq, dk, dv, B, H, N, d, w.scale,
+                                         w.causal, *drop, ws, nbytes, s_ptr), "backward")
         else:
             check(fa.fa_backward_gqa(qd, kd, vd, o, dod, lse, dq, dk, dv, B, H, Hkv, N, d,
                                      w.scale, w.causal, ws, nbytes, s_ptr), "backward")
@@ -219,7 +227,7 @@ def run_gpu(args, rank, world, dist):
             return
         forward()
         rec(1)
-        if varlen or gqa:
+        if combined:
             if ev:
                 check(fa.fa_backward_preprocess(o, dod, rows_b, H, rows_n, d, bws, bwb, s_ptr),
                       "preprocess")
@@ -294,7 +302,7 @@ def run_gpu(args, rank, world, dist):
     pre_ms = statistics.fmean(p[1] for p in per)
     main_ms = statistics.fmean(p[2] for p in per)
     conv_ms = statistics.fmean(p[3] for p in per)
-    if varlen or gqa:  # p[2] bracketed preprocess + main + convert
+    if combined:  # p[2] bracketed preprocess + main + convert
         main_ms = main_ms - pre_ms - conv_ms
     ms_max = ms
     if dist is not None:
@@ -362,7 +370,7 @@ def run_gpu(args, rank, world, dist):
                 "peak_source": f"{peaks['source']} bf16 burst",
                 "traffic": ncu_traffic(f"fa_bwd_kernel:{args.workload}", src_hash),
                 "main_time": ("combined backward minus separately timed preprocess and convert"
-                              if (varlen or gqa) else "CUDA events around the kernel's launch"),
+                              if combined else "CUDA events around the kernel's launch"),
                 "algorithmic_flops_per_launch": main_flops,
                 "avg_launch_ms": round(main_ms, 5)}
     fwd_tf = ff / (fwd_ms * 1e-3) / 1e12
@@ -372,7 +380,7 @@ def run_gpu(args, rank, world, dist):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) bf16)",
         "config": {"workload": f"{w.name}: {w.note}", "B": B, "H": H, "N": N, "d": d,
-                   "causal": w.causal, "sparse": sparse, "Hkv": Hkv,
+                   "causal": w.causal, "sparse": sparse, "Hkv": Hkv, "dropout": w.dropout,
                    **({"total_tokens": T, "max_seqlen": max_seqlen,
                        "seq_lens": [int(x) for x in np.diff(cu)]} if varlen else {}),
                    "l2": "flushed before every timed step (256 MiB device write, outside events)",
@@ -403,6 +411,7 @@ def oracle_job(w):
     import fa_workloads as W
     import oracle
     f = lambda t: t.float().double().numpy()
+    drop = (w.dropout, W.DROPOUT_SEED, 0) if w.dropout > 0 else None
     if w.varlen:
         q, k, v, do, cu = W.make_varlen_inputs(w, with_do=True)
         G = w.H // w.kv_heads
@@ -410,9 +419,9 @@ def oracle_job(w):
         def sample(n, nthreads):
             kv = np.arange(n) // G
             oracle.forward_varlen(f(q[:n]), f(k[kv]), f(v[kv]), cu, w.scale, causal=w.causal,
-                                  nthreads=nthreads)
+                                  nthreads=nthreads, dropout=drop)
             oracle.backward_varlen(f(q[:n]), f(k[kv]), f(v[kv]), f(do[:n]), cu, w.scale,
-                                   causal=w.causal, nthreads=nthreads)
+                                   causal=w.causal, nthreads=nthreads, dropout=drop)
         return sample, w.H, W.fwd_bwd_flops(w) / w.H
     q, k, v, do, mask = W.make_inputs(w, with_do=True)
     B, H, N, d = q.shape
@@ -423,9 +432,9 @@ def oracle_job(w):
 
     def sample(n, nthreads):
         oracle.forward(r(q, n), r(k, n), r(v, n), w.scale, causal=w.causal, block_mask=mask,
-                       nthreads=nthreads)
+                       nthreads=nthreads, dropout=drop)
         oracle.backward(r(q, n), r(k, n), r(v, n), r(do, n), w.scale, causal=w.causal,
-                        block_mask=mask, nthreads=nthreads)
+                        block_mask=mask, nthreads=nthreads, dropout=drop)
     return sample, B * H, W.fwd_bwd_flops(w, mask) / (B * H)
 
 

@@ -20,6 +20,7 @@ Recipe (one per workload):
     are packed back to back, tensors [H, total, d] (K, V: [Hkv, total, d]),
     drawn like the equal-length ones.
   * Grouped heads: K and V have Hkv heads instead of H.
+  * Dropout: probability p on P, generator seed DROPOUT_SEED, offset 0.
 """
 from __future__ import annotations
 
@@ -29,6 +30,7 @@ import numpy as np
 import torch
 
 TILE = 128
+DROPOUT_SEED = 0x5EED0F00D
 
 
 @dataclass(frozen=True)
@@ -44,6 +46,7 @@ class Workload:
     sparse_density: float | None = None  # block-sparse when not None
     Hkv: int | None = None  # grouped key/value heads when set (H % Hkv == 0)
     varlen: bool = False    # packed batch of lengths in [N/4, N]
+    dropout: float = 0.0    # dropout probability on P
     seed_index: int = 0
     note: str = ""
 
@@ -92,6 +95,13 @@ WORKLOADS = {
     "bert_large_varlen": Workload("bert_large_varlen", 8, 16, 512, 64, varlen=True, seed_index=6,
                                   note="BERT-large shapes with a padding mask: 8 packed "
                                        "sequences of 128..512 tokens, H=16 d=64"),
+    "bert_large_varlen_dropout": Workload(
+        "bert_large_varlen_dropout", 8, 16, 512, 64, varlen=True, dropout=0.1, seed_index=6,
+        note="the section 4.4 benchmark setting (dropout + padding mask) at BERT-large shapes: "
+             "8 packed sequences of 128..512 tokens, H=16 d=64, p=0.1"),
+    "longseq_dense_n4096_d128_dropout": Workload(
+        "longseq_dense_n4096_d128_dropout", 4, 16, 4096, 128, peaked_frac=0.01, dropout=0.1,
+        seed_index=4, note="longseq_dense_n4096_d128 with dropout p=0.1 on P"),
     "gqa_causal_n4096_d128": Workload("gqa_causal_n4096_d128", 4, 16, 4096, 128, causal=True,
                                       Hkv=4, seed_index=7,
                                       note="grouped heads: 16 query heads over 4 K/V heads, "

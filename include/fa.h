@@ -170,17 +170,47 @@ fa_status fa_backward_gqa(const void* q, const void* k, const void* v, const voi
  * [0, total] and lengths to max_seqlen: an array that breaks the rules gives
  * unspecified values in the outputs but no access outside the tensors.
  * total = 0 returns FA_OK with nothing launched.  Workspace (backward):
- * fa_backward_workspace_size(1, H, total, d).  Other rules as fa_forward /
- * fa_backward; H * total * d must stay below 2^31.
+ * fa_backward_workspace_size(1, H, total, d).  p_drop, seed, offset:
+ * dropout on P as fa_forward_dropout, sequence b taking the place of batch
+ * b (p_drop = 0: none).  Other rules as fa_forward / fa_backward;
+ * H * total * d must stay below 2^31.
  */
 fa_status fa_forward_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
                             const int* cu_seqlens, int B, int max_seqlen, int total, int H,
-                            int Hkv, int d, float scale, int causal, cudaStream_t stream);
+                            int Hkv, int d, float scale, int causal, float p_drop,
+                            unsigned long long seed, unsigned offset, cudaStream_t stream);
 fa_status fa_backward_varlen(const void* q, const void* k, const void* v, const void* o,
                              const void* dO, const float* lse, void* dq, void* dk, void* dv,
                              const int* cu_seqlens, int B, int max_seqlen, int total, int H,
-                             int Hkv, int d, float scale, int causal, void* workspace,
+                             int Hkv, int d, float scale, int causal, float p_drop,
+                             unsigned long long seed, unsigned offset, void* workspace,
                              size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Dropout on the attention weights, fused into both passes (hackmd summary,
+ * "Kernel Fusion": masking and dropout are applied inside the kernel; the
+ * section 4.4 benchmark runs with dropout).  Inverted dropout of P:
+ *   O = (z o P) V / (1 - p'),   lse = the undropped row's logsumexp
+ * The keep indicator z_ij of query row i, key j of (batch b, head h) is
+ *   byte (j mod 16) of Philox4x32-10(counter = (j/16, i, b*H + h, offset),
+ *                                    key = (seed mod 2^32, seed / 2^32))
+ *   (output word (j/4) mod 4, byte j mod 4, little-endian)  >=  t,
+ *   t = rint(256 * p_drop),  p' = t / 256
+ * (Philox: Salmon, Moraes, Dror, Shaw, SC 2011).  Decisions are integer
+ * and reproducible bit for bit; the backward regenerates them from the same
+ * (seed, offset), which must match the forward's.  p_drop is rounded to a
+ * multiple of 1/256; p_drop outside [0, 1), or rounding to 1, gives
+ * FA_ERR_INVALID_ARG.  p_drop = 0 computes the undropped result.  Layouts,
+ * workspace and other rules as fa_forward / fa_backward.
+ */
+fa_status fa_forward_dropout(const void* q, const void* k, const void* v, void* o, float* lse,
+                             int B, int H, int N, int d, float scale, int causal, float p_drop,
+                             unsigned long long seed, unsigned offset, cudaStream_t stream);
+fa_status fa_backward_dropout(const void* q, const void* k, const void* v, const void* o,
+                              const void* dO, const float* lse, void* dq, void* dk, void* dv,
+                              int B, int H, int N, int d, float scale, int causal, float p_drop,
+                              unsigned long long seed, unsigned offset, void* workspace,
+                              size_t workspace_bytes, cudaStream_t stream);
 
 /* Bytes of workspace the block-sparse calls need: the CSR and CSC tile
  * lists of the mask (4 * mask_heads * (2*(nT+1) + 2*nT*nT) bytes) followed

@@ -32,6 +32,7 @@ EXPORTS = (
     "fa_blocksparse_backward", "fa_get_device_status", "fa_set_wait_limit_ns",
     "fa_debug_wait_timeout", "fa_debug_schedule", "fa_debug_mma_probe", "fa_forward_gqa",
     "fa_backward_gqa", "fa_debug_forward_config", "fa_forward_varlen", "fa_backward_varlen",
+    "fa_forward_dropout", "fa_backward_dropout",
 )
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -64,7 +65,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
                                "`python -m io_aware_exact_15_gb300.build`")
         lib = ctypes.CDLL(_build.LIB)
         P, I, F, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
-        U = ctypes.c_ulonglong
+        U, UI = ctypes.c_ulonglong, ctypes.c_uint
         sig = {
             "fa_status_string": ([I], ctypes.c_char_p),
             "fa_forward": ([P, P, P, P, P, I, I, I, I, F, I, P], I),
@@ -87,9 +88,12 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
             "fa_forward_gqa": ([P, P, P, P, P, I, I, I, I, I, F, I, P], I),
             "fa_debug_forward_config": ([P, P, P, P, P, I, I, I, I, F, I, I, I, P], I),
             "fa_backward_gqa": ([P, P, P, P, P, P, P, P, P, I, I, I, I, I, F, I, P, Z, P], I),
-            "fa_forward_varlen": ([P, P, P, P, P, P, I, I, I, I, I, I, F, I, P], I),
-            "fa_backward_varlen": ([P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, I, P, Z, P],
-                                   I),
+            "fa_forward_varlen": ([P, P, P, P, P, P, I, I, I, I, I, I, F, I, F, U, UI, P], I),
+            "fa_backward_varlen": ([P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, I, F, U,
+                                    UI, P, Z, P], I),
+            "fa_forward_dropout": ([P, P, P, P, P, I, I, I, I, F, I, F, U, UI, P], I),
+            "fa_backward_dropout": ([P, P, P, P, P, P, P, P, P, I, I, I, I, F, I, F, U, UI, P, Z,
+                                     P], I),
         }
         for name, (args, res) in sig.items():
             fn = getattr(lib, name)
@@ -144,18 +148,35 @@ def fa_backward_gqa(q, k, v, o, dO, lse, dq, dk, dv, B, H, Hkv, N, d, scale, cau
 
 
 def fa_forward_varlen(q, k, v, o, lse, cu_seqlens, B, max_seqlen, total, H, Hkv, d, scale,
-                      causal, stream=None) -> int:
+                      causal, p_drop, seed, offset, stream=None) -> int:
     return load().fa_forward_varlen(_p(q), _p(k), _p(v), _p(o), _p(lse), _p(cu_seqlens), B,
                                     max_seqlen, total, H, Hkv, d, float(scale),
-                                    int(bool(causal)), _s(stream))
+                                    int(bool(causal)), float(p_drop), int(seed), int(offset),
+                                    _s(stream))
 
 
 def fa_backward_varlen(q, k, v, o, dO, lse, dq, dk, dv, cu_seqlens, B, max_seqlen, total, H, Hkv,
-                       d, scale, causal, workspace, workspace_bytes, stream=None) -> int:
+                       d, scale, causal, p_drop, seed, offset, workspace, workspace_bytes,
+                       stream=None) -> int:
     return load().fa_backward_varlen(_p(q), _p(k), _p(v), _p(o), _p(dO), _p(lse), _p(dq), _p(dk),
                                      _p(dv), _p(cu_seqlens), B, max_seqlen, total, H, Hkv, d,
-                                     float(scale), int(bool(causal)), _p(workspace),
-                                     int(workspace_bytes), _s(stream))
+                                     float(scale), int(bool(causal)), float(p_drop), int(seed),
+                                     int(offset), _p(workspace), int(workspace_bytes), _s(stream))
+
+
+def fa_forward_dropout(q, k, v, o, lse, B, H, N, d, scale, causal, p_drop, seed, offset,
+                       stream=None) -> int:
+    return load().fa_forward_dropout(_p(q), _p(k), _p(v), _p(o), _p(lse), B, H, N, d,
+                                     float(scale), int(bool(causal)), float(p_drop), int(seed),
+                                     int(offset), _s(stream))
+
+
+def fa_backward_dropout(q, k, v, o, dO, lse, dq, dk, dv, B, H, N, d, scale, causal, p_drop, seed,
+                        offset, workspace, workspace_bytes, stream=None) -> int:
+    return load().fa_backward_dropout(_p(q), _p(k), _p(v), _p(o), _p(dO), _p(lse), _p(dq),
+                                      _p(dk), _p(dv), B, H, N, d, float(scale), int(bool(causal)),
+                                      float(p_drop), int(seed), int(offset), _p(workspace),
+                                      int(workspace_bytes), _s(stream))
 
 
 def fa_backward_workspace_size(B, H, N, d) -> int:
@@ -277,11 +298,13 @@ def _varlen_shape(q, k, cu_seqlens, max_seqlen):
 
 
 def attention_forward(q, k, v, scale=None, causal=False, block_mask=None, workspace=None,
-                      stream=None, cu_seqlens=None, max_seqlen=None):
+                      stream=None, cu_seqlens=None, max_seqlen=None, dropout_p=0.0, seed=0,
+                      offset=0):
     """(o, lse) for bf16 CUDA tensors q [B, H, N, d] and k, v [B, Hkv, N, d]
     (Hkv = H, or a divisor of H for grouped heads).  With cu_seqlens (int32
     CUDA tensor [B+1]) the batch is packed: q [H, total, d], k, v
-    [Hkv, total, d], lse [H, total]."""
+    [Hkv, total, d], lse [H, total].  dropout_p > 0: dropout on P with the
+    Philox keep rule of (seed, offset); the backward must get the same."""
     import torch
     if cu_seqlens is not None:
         if block_mask is not None:
@@ -291,14 +314,19 @@ def attention_forward(q, k, v, scale=None, causal=False, block_mask=None, worksp
         o = torch.empty_like(q)
         lse = torch.empty((H, T), dtype=torch.float32, device=q.device)
         _check(fa_forward_varlen(q, k, v, o, lse, cu_seqlens, B, ms, T, H, Hkv, d, scale, causal,
-                                 stream), "fa_forward_varlen")
+                                 dropout_p, seed, offset, stream), "fa_forward_varlen")
         return o, lse
     B, H, N, d = _shape(q)
     Hkv = int(k.shape[1])
     scale = (1.0 / d ** 0.5) if scale is None else scale
     o = torch.empty_like(q)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
-    if block_mask is None:
+    if dropout_p:
+        if block_mask is not None or Hkv != H:
+            raise ValueError("dropout applies to dense Hkv = H or variable-length batches")
+        _check(fa_forward_dropout(q, k, v, o, lse, B, H, N, d, scale, causal, dropout_p, seed,
+                                  offset, stream), "fa_forward_dropout")
+    elif block_mask is None:
         if Hkv == H:
             _check(fa_forward(q, k, v, o, lse, B, H, N, d, scale, causal, stream), "fa_forward")
         else:
@@ -318,7 +346,8 @@ def attention_forward(q, k, v, scale=None, causal=False, block_mask=None, worksp
 
 
 def attention_backward(q, k, v, o, dO, lse, scale=None, causal=False, block_mask=None,
-                       workspace=None, stream=None, cu_seqlens=None, max_seqlen=None):
+                       workspace=None, stream=None, cu_seqlens=None, max_seqlen=None,
+                       dropout_p=0.0, seed=0, offset=0):
     """(dq, dk, dv) of sum(O * dO); shapes and options as attention_forward."""
     import torch
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
@@ -331,13 +360,22 @@ def attention_backward(q, k, v, o, dO, lse, scale=None, causal=False, block_mask
         if workspace is None:
             workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
         _check(fa_backward_varlen(q, k, v, o, dO, lse, dq, dk, dv, cu_seqlens, B, ms, T, H, Hkv, d,
-                                  scale, causal, workspace, workspace.numel(), stream),
-               "fa_backward_varlen")
+                                  scale, causal, dropout_p, seed, offset, workspace,
+                                  workspace.numel(), stream), "fa_backward_varlen")
         return dq, dk, dv
     B, H, N, d = _shape(q)
     Hkv = int(k.shape[1])
     scale = (1.0 / d ** 0.5) if scale is None else scale
-    if block_mask is None:
+    if dropout_p:
+        if block_mask is not None or Hkv != H:
+            raise ValueError("dropout applies to dense Hkv = H or variable-length batches")
+        nbytes = fa_backward_workspace_size(B, H, N, d)
+        if workspace is None:
+            workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+        _check(fa_backward_dropout(q, k, v, o, dO, lse, dq, dk, dv, B, H, N, d, scale, causal,
+                                   dropout_p, seed, offset, workspace, workspace.numel(), stream),
+               "fa_backward_dropout")
+    elif block_mask is None:
         nbytes = fa_backward_workspace_size(B, H, N, d)
         if workspace is None:
             workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)

@@ -178,7 +178,8 @@ struct Varlen {
 fa_status forward_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                        int H, int Hkv, int N, int d, float scale, int causal,
                        const fa::TileLists* lists, cudaStream_t stream,
-                       const Varlen& vl = Varlen()) {
+                       const Varlen& vl = Varlen(),
+                       const fa::DropoutParams& drop = fa::DropoutParams()) {
   fa_status st = FA_OK;
   int* err = status_word(&st);
   if (!err) return st;
@@ -202,6 +203,7 @@ fa_status forward_impl(const void* q, const void* k, const void* v, void* o, flo
   if (lists) p.lists = *lists;
   p.cu_seqlens = vl.cu_seqlens;
   p.total = vl.total;
+  p.drop = drop;
   p.err = err;
   p.wait_ns = wait_limit_ns();
   FA_CUDA(fa::launch_forward(p, tq, tk, tv, stream));
@@ -212,7 +214,8 @@ fa_status backward_main_impl(const void* q, const void* k, const void* v, const 
                              const float* lse, void* dk, void* dv, int B, int H, int Hkv, int N,
                              int d, float scale, int causal, const BwdWorkspace& w,
                              const fa::TileLists* lists, cudaStream_t stream,
-                             const Varlen& vl = Varlen()) {
+                             const Varlen& vl = Varlen(),
+                             const fa::DropoutParams& drop = fa::DropoutParams()) {
   fa_status st = FA_OK;
   int* err = status_word(&st);
   if (!err) return st;
@@ -239,6 +242,7 @@ fa_status backward_main_impl(const void* q, const void* k, const void* v, const 
   if (lists) p.lists = *lists;
   p.cu_seqlens = vl.cu_seqlens;
   p.total = vl.total;
+  p.drop = drop;
   p.err = err;
   p.wait_ns = wait_limit_ns();
   FA_CUDA(fa::launch_backward_main(p, tq, tk, tv, tdo, tdq, stream));
@@ -286,6 +290,22 @@ fa_status check_varlen(const int* cu_seqlens, int B, int max_seqlen, int total, 
   if (static_cast<long long>(H) * total * d >= (1LL << 31)) return FA_ERR_UNSUPPORTED;
   if (static_cast<long long>(B) * H * num_tiles(max_seqlen) >= (1LL << 31))
     return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
+
+// Dropout probability p in [0, 1) -> threshold t = rint(256 p) (p taken in
+// float32, the product in double) and scale 256 / (256 - t); t = 256 (all
+// dropped) is refused.
+fa_status make_dropout(float p_drop, unsigned long long seed, unsigned offset,
+                       fa::DropoutParams* out) {
+  if (!(p_drop >= 0.f && p_drop < 1.f)) return FA_ERR_INVALID_ARG;
+  const double t = nearbyint(256.0 * static_cast<double>(p_drop));
+  if (t >= 256.0) return FA_ERR_INVALID_ARG;
+  out->t = static_cast<uint32_t>(t);
+  out->scale = static_cast<float>(256.0 / (256.0 - t));
+  out->seed_lo = static_cast<uint32_t>(seed);
+  out->seed_hi = static_cast<uint32_t>(seed >> 32);
+  out->offset = offset;
   return FA_OK;
 }
 
@@ -423,9 +443,12 @@ fa_status fa_backward_gqa(const void* q, const void* k, const void* v, const voi
 
 fa_status fa_forward_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
                             const int* cu_seqlens, int B, int max_seqlen, int total, int H,
-                            int Hkv, int d, float scale, int causal, cudaStream_t stream) {
+                            int Hkv, int d, float scale, int causal, float p_drop,
+                            unsigned long long seed, unsigned offset, cudaStream_t stream) {
   FA_TRY(check_varlen(cu_seqlens, B, max_seqlen, total, H, d, scale));
   FA_TRY(check_groups(H, Hkv));
+  fa::DropoutParams drop;
+  FA_TRY(make_dropout(p_drop, seed, offset, &drop));
   for (const void* p : {q, k, v, static_cast<const void*>(o)}) FA_TRY(check_ptr16(p));
   FA_TRY(check_ptr4(lse));
   if (total == 0) return FA_OK;  // every sequence empty: nothing to write
@@ -433,16 +456,19 @@ fa_status fa_forward_varlen(const void* q, const void* k, const void* v, void* o
   vl.cu_seqlens = cu_seqlens;
   vl.total = total;
   return forward_impl(q, k, v, o, lse, B, H, Hkv, max_seqlen, d, scale, causal, nullptr, stream,
-                      vl);
+                      vl, drop);
 }
 
 fa_status fa_backward_varlen(const void* q, const void* k, const void* v, const void* o,
                              const void* dO, const float* lse, void* dq, void* dk, void* dv,
                              const int* cu_seqlens, int B, int max_seqlen, int total, int H,
-                             int Hkv, int d, float scale, int causal, void* workspace,
+                             int Hkv, int d, float scale, int causal, float p_drop,
+                             unsigned long long seed, unsigned offset, void* workspace,
                              size_t workspace_bytes, cudaStream_t stream) {
   FA_TRY(check_varlen(cu_seqlens, B, max_seqlen, total, H, d, scale));
   FA_TRY(check_groups(H, Hkv));
+  fa::DropoutParams drop;
+  FA_TRY(make_dropout(p_drop, seed, offset, &drop));
   for (const void* p : {q, k, v, o, dO, static_cast<const void*>(dq), static_cast<const void*>(dk),
                         static_cast<const void*>(dv)})
     FA_TRY(check_ptr16(p));
@@ -456,8 +482,33 @@ fa_status fa_backward_varlen(const void* q, const void* k, const void* v, const 
   vl.cu_seqlens = cu_seqlens;
   vl.total = total;
   FA_TRY(backward_main_impl(q, k, v, dO, lse, dk, dv, B, H, Hkv, max_seqlen, d, scale, causal,
-                            bwd_ws(workspace, 1, H, total), nullptr, stream, vl));
+                            bwd_ws(workspace, 1, H, total), nullptr, stream, vl, drop));
   return fa_backward_dq_convert(dq, 1, H, total, d, scale, workspace, workspace_bytes, stream);
+}
+
+fa_status fa_forward_dropout(const void* q, const void* k, const void* v, void* o, float* lse,
+                             int B, int H, int N, int d, float scale, int causal, float p_drop,
+                             unsigned long long seed, unsigned offset, cudaStream_t stream) {
+  FA_TRY(check_fwd_args(q, k, v, o, lse, B, H, N, d, scale));
+  fa::DropoutParams drop;
+  FA_TRY(make_dropout(p_drop, seed, offset, &drop));
+  return forward_impl(q, k, v, o, lse, B, H, H, N, d, scale, causal, nullptr, stream, Varlen(),
+                      drop);
+}
+
+fa_status fa_backward_dropout(const void* q, const void* k, const void* v, const void* o,
+                              const void* dO, const float* lse, void* dq, void* dk, void* dv,
+                              int B, int H, int N, int d, float scale, int causal, float p_drop,
+                              unsigned long long seed, unsigned offset, void* workspace,
+                              size_t workspace_bytes, cudaStream_t stream) {
+  FA_TRY(check_bwd_args(q, k, v, o, dO, lse, dq, dk, dv, B, H, N, d, scale));
+  fa::DropoutParams drop;
+  FA_TRY(make_dropout(p_drop, seed, offset, &drop));
+  FA_TRY(check_ws(workspace, workspace_bytes, bwd_ws_bytes(B, H, N, d)));
+  FA_TRY(fa_backward_preprocess(o, dO, B, H, N, d, workspace, workspace_bytes, stream));
+  FA_TRY(backward_main_impl(q, k, v, dO, lse, dk, dv, B, H, H, N, d, scale, causal,
+                            bwd_ws(workspace, B, H, N), nullptr, stream, Varlen(), drop));
+  return fa_backward_dq_convert(dq, B, H, N, d, scale, workspace, workspace_bytes, stream);
 }
 
 size_t fa_blocksparse_workspace_size(int B, int H, int N, int d, int mask_heads) {

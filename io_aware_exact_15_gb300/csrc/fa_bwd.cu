@@ -33,6 +33,7 @@
 
 #include "fa_internal.h"
 #include "fa_ptx.cuh"
+#include "fa_philox.cuh"
 #include "fa_sched.cuh"
 
 namespace fa {
@@ -94,9 +95,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   bwd_cta_coords(blockIdx.x, p.B * Hkv, ntmax, p.causal != 0, bkv, kt);
   // Sequence geometry: length N, first row row0 of the sequence in its
   // slice, the K/V slice zkv and the first query slice bq0 of the group.
+  constexpr bool DROP = KIND == kGeneralDropout;
   int N = p.N, row0 = 0, zkv = bkv;
   int bq0 = GQA ? (bkv / Hkv) * p.H + (bkv % Hkv) * G : bkv;
-  if (KIND == kGeneral) {
+  int bh_base = 0;  // b * H when query slices are heads (variable-length batch)
+  const bool varlen = KIND >= kGeneral && p.cu_seqlens != nullptr;
+  if (varlen) {
     // variable-length batch: slices are heads, sequences are row ranges
     // (indices clamped to [0, total], so bad offsets cannot write outside)
     const int b = bkv / Hkv;
@@ -106,10 +110,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     N = min(e - a, p.N);
     zkv = bkv % Hkv;
     bq0 = zkv * G;
+    bh_base = b * p.H;
     if (kt * kTile >= N) return;  // no key of this tile here (CTA-uniform)
   }
-  const size_t slice_rows = KIND == kGeneral ? static_cast<size_t>(p.total)
-                                             : static_cast<size_t>(p.N);
+  const size_t slice_rows = varlen ? static_cast<size_t>(p.total) : static_cast<size_t>(p.N);
   const int nT = (N + kTile - 1) / kTile;
 
   if (threadIdx.x == 0) {
@@ -343,6 +347,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const float sl2 = p.scale * kLog2e;
     const int kbase = kt * kTile;
     const int kcol0 = kbase + 64 * half;  // first key of this thread's columns
+    const DropoutRng rng{p.drop.seed_lo, p.drop.seed_hi, p.drop.offset, p.drop.t * 0x01010101u};
     bool ok = true;
     uint32_t n = 0;
     int qt = 0, qt_prev = 0, g = 0, g_prev = 0;
@@ -432,10 +437,33 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         pw[i] = live ? pack_bf16(a, b) : 0u;
       }
+      // keep bits of this thread's 64 keys (bit k of kb[c]: key 32 c + k)
+      uint32_t kb[2] = {0u, 0u};
+      if (DROP) {
+        // the dV product takes the dropped weights z * P; dS needs P and z
 #pragma unroll
-      for (int u = 0; u < 8; ++u)
-        st_shared_v4(pbuf + sw128_offset(r, u), pw[4 * u], pw[4 * u + 1], pw[4 * u + 2],
-                     pw[4 * u + 3]);
+        for (int g4 = 0; g4 < 4; ++g4) {
+          const PhiloxOut rw = rng.group((kcol0 >> 4) + g4, qrow, bh_base + bq0 + g);
+          uint32_t mk[4];
+#pragma unroll
+          for (int w = 0; w < 4; ++w) mk[w] = DropoutRng::keep_bytes(rw.w[w], rng.t4);
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const uint32_t* pp = &pw[8 * g4 + 4 * hh];
+            st_shared_v4(pbuf + sw128_offset(r, 2 * g4 + hh), pp[0] & pair_mask(mk[2 * hh], 0),
+                         pp[1] & pair_mask(mk[2 * hh], 1), pp[2] & pair_mask(mk[2 * hh + 1], 0),
+                         pp[3] & pair_mask(mk[2 * hh + 1], 1));
+          }
+          kb[g4 >> 1] |= (keep_nibble(mk[0]) | (keep_nibble(mk[1]) << 4) |
+                          (keep_nibble(mk[2]) << 8) | (keep_nibble(mk[3]) << 12))
+                         << (16 * (g4 & 1));
+        }
+      } else {
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          st_shared_v4(pbuf + sw128_offset(r, u), pw[4 * u], pw[4 * u + 1], pw[4 * u + 2],
+                       pw[4 * u + 3]);
+      }
       fence_async_smem();
       tc_fence_before();
       mbar_arrive(bar(L::B_PR));
@@ -459,8 +487,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             const uint32_t pp = pw[16 * c + 4 * g + j];
-            const float x0 = bf16_lo(pp) * (__uint_as_float(dp[8 * g + 2 * j]) - dlt_c);
-            const float x1 = bf16_hi(pp) * (__uint_as_float(dp[8 * g + 2 * j + 1]) - dlt_c);
+            float d0 = __uint_as_float(dp[8 * g + 2 * j]);
+            float d1 = __uint_as_float(dp[8 * g + 2 * j + 1]);
+            if (DROP) {  // dP = z dP~ / (1 - p')
+              d0 = ((kb[c] >> (8 * g + 2 * j)) & 1u) ? d0 * p.drop.scale : 0.f;
+              d1 = ((kb[c] >> (8 * g + 2 * j + 1)) & 1u) ? d1 * p.drop.scale : 0.f;
+            }
+            const float x0 = bf16_lo(pp) * (d0 - dlt_c);
+            const float x1 = bf16_hi(pp) * (d1 - dlt_c);
             w[j] = pack_bf16(x0, x1);
           }
           st_shared_v4(dsbuf + sw128_offset(r, 4 * c + g), w[0], w[1], w[2], w[3]);
@@ -488,7 +522,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (ok) {  // warp-uniform: every lane takes part in the TMEM reads
       const bool dv_side = half == 0;
       const uint32_t tcol = dv_side ? L::T_DV : L::T_DK;
-      const float mul = dv_side ? 1.f : p.scale;
+      const float mul = dv_side ? (DROP ? p.drop.scale : 1.f) : p.scale;
       uint8_t* dst = static_cast<uint8_t*>(dv_side ? p.dv : p.dk) +
                      (static_cast<size_t>(zkv) * slice_rows + row0 + (key < N ? key : 0)) *
                          static_cast<size_t>(D) * 2;
@@ -546,13 +580,19 @@ cudaError_t launch_bwd_d(const BwdParams& p, const CUtensorMap& tq, const CUtens
 cudaError_t launch_backward_main(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                                  const CUtensorMap& tv, const CUtensorMap& tdo,
                                  const CUtensorMap& tdq, cudaStream_t stream) {
-  const int kind = p.cu_seqlens ? kGeneral : (p.Hkv > 0 && p.Hkv != p.H) ? kGrouped : kPlain;
+  const int kind = p.drop.t ? kGeneralDropout
+                   : p.cu_seqlens ? kGeneral
+                   : (p.Hkv > 0 && p.Hkv != p.H) ? kGrouped : kPlain;
   if (p.d == 64) {
+    if (kind == kGeneralDropout)
+      return launch_bwd_d<64, kGeneralDropout>(p, tq, tk, tv, tdo, tdq, stream);
     if (kind == kGeneral) return launch_bwd_d<64, kGeneral>(p, tq, tk, tv, tdo, tdq, stream);
     if (kind == kGrouped) return launch_bwd_d<64, kGrouped>(p, tq, tk, tv, tdo, tdq, stream);
     return launch_bwd_d<64, kPlain>(p, tq, tk, tv, tdo, tdq, stream);
   }
   if (p.d == 128) {
+    if (kind == kGeneralDropout)
+      return launch_bwd_d<128, kGeneralDropout>(p, tq, tk, tv, tdo, tdq, stream);
     if (kind == kGeneral) return launch_bwd_d<128, kGeneral>(p, tq, tk, tv, tdo, tdq, stream);
     if (kind == kGrouped) return launch_bwd_d<128, kGrouped>(p, tq, tk, tv, tdo, tdq, stream);
     return launch_bwd_d<128, kPlain>(p, tq, tk, tv, tdo, tdq, stream);

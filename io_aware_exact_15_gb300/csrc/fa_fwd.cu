@@ -29,6 +29,7 @@
 
 #include "fa_internal.h"
 #include "fa_ptx.cuh"
+#include "fa_philox.cuh"
 #include "fa_sched.cuh"
 
 namespace fa {
@@ -87,9 +88,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   // slice, the TMA slices zq (Q, O) and zkv (K, V).  Grouped K/V has H / Hkv
   // query heads per key/value head: bh / (H / Hkv) = b * Hkv + h / (H / Hkv).
   // The plain instantiation carries no index arithmetic at all.
+  constexpr bool DROP = KIND == kGeneralDropout;
   int N = p.N, row0 = 0, zq = bh, zkv = bh;
-  if (KIND == kGrouped) zkv = bh / (p.H / p.Hkv);
-  if (KIND == kGeneral) {
+  if (KIND == kGrouped || KIND >= kGeneral) zkv = bh / (p.H / p.Hkv);
+  const bool varlen = KIND >= kGeneral && p.cu_seqlens != nullptr;
+  if (varlen) {
     // variable-length batch: slices are heads, sequences are row ranges
     // (indices clamped to [0, total], so bad offsets cannot write outside)
     const int b = bh / p.H;
@@ -101,8 +104,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     zkv = head / (p.H / p.Hkv);
     if ((single ? pair : 2 * pair) * kTile >= N) return;  // no query tile here (CTA-uniform)
   }
-  const size_t slice_rows = KIND == kGeneral ? static_cast<size_t>(p.total)
-                                             : static_cast<size_t>(p.N);
+  const size_t slice_rows = varlen ? static_cast<size_t>(p.total) : static_cast<size_t>(p.N);
   const int nT = (N + kTile - 1) / kTile;
 
   if (threadIdx.x == 0) {
@@ -271,6 +273,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const uint32_t tO = tmem + lane_off + 256 + s * D;
     const uint32_t tP = tmem + lane_off + L::T_P + s * L::T_PSTRIDE;
     const float sl2 = p.scale * kLog2e;
+    DropoutRng rng{p.drop.seed_lo, p.drop.seed_hi, p.drop.offset, p.drop.t * 0x01010101u};
     float m = -INFINITY, l = 0.f;
     int cnt = 0;
     bool ok = true;
@@ -317,6 +320,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       const bool rescale_o = cnt > 0 && __any_sync(0xffffffffu, resc);
       const float mu = (m == -INFINITY) ? 0.f : m;
       float ls0 = 0.f, ls1 = 0.f;
+      PhiloxOut rw;
       // P (bf16, two per 32-bit column) overwrites the first 64 columns of
       // this tile's S, which are already in registers
 #pragma unroll
@@ -336,6 +340,17 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                  (bf16_lo(sr[q][4 * c4 + 1]) + bf16_hi(sr[q][4 * c4 + 1]));
           ls1 += (bf16_lo(sr[q][4 * c4 + 2]) + bf16_hi(sr[q][4 * c4 + 2])) +
                  (bf16_lo(sr[q][4 * c4 + 3]) + bf16_hi(sr[q][4 * c4 + 3]));
+          if (DROP) {
+            // dropped weights leave the PV product (l keeps them); one
+            // generator call covers keys 32 q + 16 (c4 / 2) .. + 15
+            if ((c4 & 1) == 0) rw = rng.group(kt * 8 + 2 * q + (c4 >> 1), qrow, bh);
+            const uint32_t m0 = DropoutRng::keep_bytes(rw.w[2 * (c4 & 1)], rng.t4);
+            const uint32_t m1 = DropoutRng::keep_bytes(rw.w[2 * (c4 & 1) + 1], rng.t4);
+            sr[q][4 * c4] &= pair_mask(m0, 0);
+            sr[q][4 * c4 + 1] &= pair_mask(m0, 1);
+            sr[q][4 * c4 + 2] &= pair_mask(m1, 0);
+            sr[q][4 * c4 + 3] &= pair_mask(m1, 1);
+          }
         }
         tmem_st16(tP + 16 * q, *reinterpret_cast<const uint32_t(*)[16]>(&sr[q][0]));
       }
@@ -367,7 +382,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                       (static_cast<size_t>(zq) * slice_rows + row0 + qrow) * static_cast<size_t>(D) * 2;
       const bool store = qrow < N;
       const bool has = cnt > 0 && l > 0.f;
-      const float inv = has ? 1.f / l : 0.f;
+      // inverted dropout scales the kept weights by 1 / (1 - p')
+      const float inv = has ? (DROP ? p.drop.scale : 1.f) / l : 0.f;
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
@@ -443,13 +459,17 @@ cudaError_t launch_forward_config(const FwdParams& p, const CUtensorMap& tq, con
 
 cudaError_t launch_forward(const FwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                            const CUtensorMap& tv, cudaStream_t stream) {
-  const int kind = p.cu_seqlens ? kGeneral : (p.Hkv > 0 && p.Hkv != p.H) ? kGrouped : kPlain;
+  const int kind = p.drop.t ? kGeneralDropout
+                   : p.cu_seqlens ? kGeneral
+                   : (p.Hkv > 0 && p.Hkv != p.H) ? kGrouped : kPlain;
   if (p.d == 64) {
+    if (kind == kGeneralDropout) return launch_fwd_d<64, kGeneralDropout>(p, tq, tk, tv, stream);
     if (kind == kGeneral) return launch_fwd_d<64, kGeneral>(p, tq, tk, tv, stream);
     if (kind == kGrouped) return launch_fwd_d<64, kGrouped>(p, tq, tk, tv, stream);
     return launch_fwd_d<64, kPlain>(p, tq, tk, tv, stream);
   }
   if (p.d == 128) {
+    if (kind == kGeneralDropout) return launch_fwd_d<128, kGeneralDropout>(p, tq, tk, tv, stream);
     if (kind == kGeneral) return launch_fwd_d<128, kGeneral>(p, tq, tk, tv, stream);
     if (kind == kGrouped) return launch_fwd_d<128, kGrouped>(p, tq, tk, tv, stream);
     return launch_fwd_d<128, kPlain>(p, tq, tk, tv, stream);

@@ -22,6 +22,15 @@ struct TileLists {
   int nT = 0;
 };
 
+// Dropout on P: element (i, j) of (batch, head) slice b*H + h is kept iff
+// byte j mod 16 of Philox4x32-10((j/16, i, b*H + h, offset), seed) >= t;
+// kept weights are scaled by 256 / (256 - t).  t = 0 means no dropout.
+struct DropoutParams {
+  uint32_t seed_lo = 0, seed_hi = 0, offset = 0;
+  uint32_t t = 0;
+  float scale = 1.f;
+};
+
 struct FwdParams {
   void* o = nullptr;      // bf16 [BH, N, d]
   float* lse = nullptr;   // fp32 [BH, N]
@@ -35,6 +44,7 @@ struct FwdParams {
   // cu_seqlens[b] .. cu_seqlens[b+1] (N is then the longest sequence)
   const int* cu_seqlens = nullptr;
   int total = 0;
+  DropoutParams drop;     // dropout on P (kernels of kind kGeneralDropout)
   int* err = nullptr;     // device status word
   uint64_t wait_ns = 0;
 };
@@ -52,13 +62,15 @@ struct BwdParams {
   TileLists lists;              // sparse when lists.col_ptr != nullptr
   const int* cu_seqlens = nullptr;  // variable-length batch (as FwdParams)
   int total = 0;
+  DropoutParams drop;
   int* err = nullptr;
   uint64_t wait_ns = 0;
 };
 
-// Kernel instantiations: plain, grouped K/V, and the general one
-// (variable-length batch, grouped K/V allowed).
-enum KernelKind : int { kPlain = 0, kGrouped = 1, kGeneral = 2 };
+// Kernel instantiations: plain, grouped K/V, the general one (variable-length
+// or equal-length batch, grouped K/V allowed) and the general one with
+// dropout on P.
+enum KernelKind : int { kPlain = 0, kGrouped = 1, kGeneral = 2, kGeneralDropout = 3 };
 
 // 3-D bf16 view {d, N, B*H} of a [B, H, N, d] tensor, 128-row x 64-column
 // boxes with 128-byte swizzle.

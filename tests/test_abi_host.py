@@ -147,13 +147,32 @@ def test_varlen_rejects_bad_args():
         ((A, 2, 512, 1 << 24, 1024, 1024, 128, 0.1), fa.FA_ERR_UNSUPPORTED),
     ]
     for (cu, B, ms, T, H, Hkv, d, sc), want in cases:
-        assert fa.fa_forward_varlen(A, A, A, A, A, cu, B, ms, T, H, Hkv, d, sc, 0, 0) == want, \
+        assert fa.fa_forward_varlen(A, A, A, A, A, cu, B, ms, T, H, Hkv, d, sc, 0, 0.0, 0, 0,
+                                    0) == want, \
             (cu, B, ms, T)
-        assert fa.fa_backward_varlen(A, A, A, A, A, A, A, A, A, cu, B, ms, T, H, Hkv, d, sc, 0, A,
+        assert fa.fa_backward_varlen(A, A, A, A, A, A, A, A, A, cu, B, ms, T, H, Hkv, d, sc, 0,
+                                     0.0, 0, 0, A,
                                      need, 0) == want
-    base = (A, 2, 512, 1000, 4, 4, 64, 0.1, 0)
+    base = (A, 2, 512, 1000, 4, 4, 64, 0.1, 0, 0.0, 0, 0)
     assert fa.fa_forward_varlen(MIS, A, A, A, A, *base, 0) == fa.FA_ERR_MISALIGNED
     assert fa.fa_backward_varlen(A, A, A, A, A, A, A, A, A, *base, A, need - 1, 0) == \
         fa.FA_ERR_WORKSPACE
     assert fa.fa_backward_varlen(A, A, A, A, A, A, A, A, A, *base, A + 16, need, 0) == \
         fa.FA_ERR_MISALIGNED
+
+
+def test_dropout_rejects_bad_probability():
+    A = ALIGNED
+    need = fa.fa_backward_workspace_size(1, 2, 256, 64)
+    for p in (-0.1, 1.0, 0.999, float("nan"), float("inf")):
+        assert fa.fa_forward_dropout(A, A, A, A, A, 1, 2, 256, 64, 0.1, 0, p, 1, 0, 0) == \
+            fa.FA_ERR_INVALID_ARG, p
+        assert fa.fa_backward_dropout(A, A, A, A, A, A, A, A, A, 1, 2, 256, 64, 0.1, 0, p, 1, 0, A,
+                                      need, 0) == fa.FA_ERR_INVALID_ARG, p
+        assert fa.fa_forward_varlen(A, A, A, A, A, A, 2, 128, 256, 2, 2, 64, 0.1, 0, p, 1, 0,
+                                    0) == fa.FA_ERR_INVALID_ARG, p
+    # shape checks come first, as for fa_forward
+    assert fa.fa_forward_dropout(A, A, A, A, A, 1, 2, 256, 96, 0.1, 0, 0.1, 1, 0, 0) == \
+        fa.FA_ERR_UNSUPPORTED
+    assert fa.fa_backward_dropout(A, A, A, A, A, A, A, A, A, 1, 2, 256, 64, 0.1, 0, 0.1, 1, 0, A,
+                                  need - 1, 0) == fa.FA_ERR_WORKSPACE

@@ -29,7 +29,7 @@ def make(H, Hkv, lens, d, seed):
     return q, k, v, do, cu
 
 
-def run(q, k, v, do, cu, scale, causal, dev, backward=True):
+def run(q, k, v, do, cu, scale, causal, dev, backward=True, drop=(0.0, 0, 0)):
     H, T, d = q.shape
     Hkv = k.shape[0]
     B = len(cu) - 1
@@ -39,7 +39,7 @@ def run(q, k, v, do, cu, scale, causal, dev, backward=True):
     o = torch.full_like(qd, float("nan"))
     lse = torch.full((H, T), float("nan"), dtype=torch.float32, device=dev)
     assert fa.fa_forward_varlen(qd, kd, vd, o, lse, cud, B, ms, T, H, Hkv, d, scale,
-                                causal) == fa.FA_OK
+                                causal, *drop) == fa.FA_OK
     out = [o, lse]
     if backward:
         dq = torch.full_like(qd, float("nan"))
@@ -47,7 +47,7 @@ def run(q, k, v, do, cu, scale, causal, dev, backward=True):
         nbytes = fa.fa_backward_workspace_size(1, H, T, d)
         ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
         assert fa.fa_backward_varlen(qd, kd, vd, o, dod, lse, dq, dk, dv, cud, B, ms, T, H, Hkv, d,
-                                     scale, causal, ws, nbytes) == fa.FA_OK
+                                     scale, causal, *drop, ws, nbytes) == fa.FA_OK
         out += [dq, dk, dv]
     status_ok()
     return [t.cpu() for t in out]
@@ -118,10 +118,10 @@ def test_varlen_all_empty_and_empty_edges():
     # aligned dummy buffer stands in for the empty tensors)
     buf = torch.zeros(1024, dtype=torch.bfloat16, device=dev)
     cu = torch.zeros(4, dtype=torch.int32, device=dev)
-    assert fa.fa_forward_varlen(buf, buf, buf, buf, buf, cu, 3, 0, 0, H, H, d, 0.125,
+    assert fa.fa_forward_varlen(buf, buf, buf, buf, buf, cu, 3, 0, 0, H, H, d, 0.125, 0, 0.0, 0,
                                 0) == fa.FA_OK
     assert fa.fa_backward_varlen(buf, buf, buf, buf, buf, buf, buf, buf, buf, cu, 3, 0, 0, H, H,
-                                 d, 0.125, 0, buf, buf.numel() * 2) == fa.FA_OK
+                                 d, 0.125, 0, 0.0, 0, 0, buf, buf.numel() * 2) == fa.FA_OK
     status_ok()
     assert not buf.any()
     # empty sequences first and last around a ragged one
