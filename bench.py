@@ -141,7 +141,10 @@ def run_gpu(args, rank, world, dist):
     varlen = w.varlen
     gqa = Hkv != H
     drop = (w.dropout, W.DROPOUT_SEED, 0)
-    combined = varlen or gqa or w.dropout > 0  # no split backward entry point
+    det = bool(getattr(args, "deterministic", False))
+    if det and (varlen or gqa or w.dropout > 0 or w.sparse_density is not None):
+        raise SystemExit("--deterministic applies to dense or causal equal-length workloads")
+    combined = varlen or gqa or w.dropout > 0 or det  # no split backward entry point
     if varlen:
         q, k, v, do, cu = W.make_varlen_inputs(w, with_do=True)
         mask = None
@@ -195,7 +198,10 @@ def run_gpu(args, rank, world, dist):
                   "forward")
 
     def backward_whole():
-        if varlen:
+        if det:
+            check(fa.fa_backward_deterministic(qd, kd, vd, o, dod, lse, dq, dk, dv, B, H, N, d,
+                                               w.scale, w.causal, ws, nbytes, s_ptr), "backward")
+        elif varlen:
             check(fa.fa_backward_varlen(qd, kd, vd, o, dod, lse, dq, dk, dv, cud, B, max_seqlen,
                                         T, H, Hkv, d, w.scale, w.causal, *drop, ws, nbytes,
                                         s_ptr), "backward")
@@ -234,7 +240,7 @@ def run_gpu(args, rank, world, dist):
             rec(2)
             backward_whole()
             rec(3)
-            if ev:
+            if ev and not det:  # the deterministic backward has no conversion pass
                 check(fa.fa_backward_dq_convert(dq, rows_b, H, rows_n, d, w.scale, bws, bwb,
                                                 s_ptr), "convert")
             rec(4)
@@ -302,8 +308,8 @@ def run_gpu(args, rank, world, dist):
     pre_ms = statistics.fmean(p[1] for p in per)
     main_ms = statistics.fmean(p[2] for p in per)
     conv_ms = statistics.fmean(p[3] for p in per)
-    if combined:  # p[2] bracketed preprocess + main + convert
-        main_ms = main_ms - pre_ms - conv_ms
+    if combined:  # p[2] bracketed preprocess + main (+ dQ pass or convert)
+        main_ms = main_ms - pre_ms - (0.0 if det else conv_ms)
     ms_max = ms
     if dist is not None:
         t = torch.tensor([ms], dtype=torch.float64, device=dev)
@@ -364,12 +370,17 @@ def run_gpu(args, rank, world, dist):
     main_flops = 2.5 * ff
     achieved = main_flops / (main_ms * 1e-3) / 1e12
     peak = peaks["bf16_tflops"]
-    roofline = {"kernel": "fa_bwd_kernel (recompute: S, dP, dV, dK, dQ MMAs)", "bound": "tensor",
+    kname = ("fa_bwd_kernel without dQ + fa_bwd_dq_kernel (deterministic backward; algorithmic "
+             "FLOPs count the five products once)" if det else
+             "fa_bwd_kernel (recompute: S, dP, dV, dK, dQ MMAs)")
+    roofline = {"kernel": kname, "bound": "tensor",
                 "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
                 "frac": round(achieved / peak, 4),
                 "peak_source": f"{peaks['source']} bf16 burst",
                 "traffic": ncu_traffic(f"fa_bwd_kernel:{args.workload}", src_hash),
-                "main_time": ("combined backward minus separately timed preprocess and convert"
+                "main_time": ("deterministic backward minus the separately timed preprocess: "
+                              "key-tile pass + query-tile dQ pass together" if det else
+                              "combined backward minus separately timed preprocess and convert"
                               if combined else "CUDA events around the kernel's launch"),
                 "algorithmic_flops_per_launch": main_flops,
                 "avg_launch_ms": round(main_ms, 5)}
@@ -381,6 +392,7 @@ def run_gpu(args, rank, world, dist):
         "data": "synthetic (seeded N(0,1) bf16)",
         "config": {"workload": f"{w.name}: {w.note}", "B": B, "H": H, "N": N, "d": d,
                    "causal": w.causal, "sparse": sparse, "Hkv": Hkv, "dropout": w.dropout,
+                   "deterministic_backward": det,
                    **({"total_tokens": T, "max_seqlen": max_seqlen,
                        "seq_lens": [int(x) for x in np.diff(cu)]} if varlen else {}),
                    "l2": "flushed before every timed step (256 MiB device write, outside events)",
@@ -560,6 +572,8 @@ def main():
     ap.add_argument("--workload", default="bert_large")
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--deterministic", action="store_true",
+                    help="time fa_backward_deterministic instead of fa_backward")
     ap.add_argument("--tile-sweep", action="store_true",
                     help="time the forward per tile configuration (block-size experiment)")
     args = ap.parse_args()

@@ -187,6 +187,26 @@ fa_status fa_backward_varlen(const void* q, const void* k, const void* v, const 
                              size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * Deterministic backward: dQ, dK, dV identical bit for bit from run to run
+ * (fa_backward sums dQ with unordered fp32 atomic adds, so its dQ may differ
+ * in the last bits between runs).  Two passes after the D preprocess:
+ *   key-tile pass   per key tile: S, P, dP, dS, dV += P^T dO, dK += dS^T Q
+ *                   (fixed order inside one CTA), no dQ product
+ *   query-tile pass per query tile: S, P, dP, dS recomputed, dQ += dS K over
+ *                   the key tiles in ascending order; bf16(scale * dQ)
+ *                   written directly
+ * It recomputes S and dP once more (7 tile products per (query, key) tile
+ * pair instead of 5), the price of the fixed order ("Recomputation" leaves
+ * the summation order open).  Same arguments and results as fa_backward;
+ * the workspace needs only align256(4 * B*H*N) bytes (D); any size from
+ * fa_backward_workspace_size works.
+ */
+fa_status fa_backward_deterministic(const void* q, const void* k, const void* v, const void* o,
+                                    const void* dO, const float* lse, void* dq, void* dk, void* dv,
+                                    int B, int H, int N, int d, float scale, int causal,
+                                    void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * Dropout on the attention weights, fused into both passes (hackmd summary,
  * "Kernel Fusion": masking and dropout are applied inside the kernel; the
  * section 4.4 benchmark runs with dropout).  Inverted dropout of P:

@@ -32,7 +32,7 @@ EXPORTS = (
     "fa_blocksparse_backward", "fa_get_device_status", "fa_set_wait_limit_ns",
     "fa_debug_wait_timeout", "fa_debug_schedule", "fa_debug_mma_probe", "fa_forward_gqa",
     "fa_backward_gqa", "fa_debug_forward_config", "fa_forward_varlen", "fa_backward_varlen",
-    "fa_forward_dropout", "fa_backward_dropout",
+    "fa_forward_dropout", "fa_backward_dropout", "fa_backward_deterministic",
 )
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -92,6 +92,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
             "fa_backward_varlen": ([P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, I, F, U,
                                     UI, P, Z, P], I),
             "fa_forward_dropout": ([P, P, P, P, P, I, I, I, I, F, I, F, U, UI, P], I),
+            "fa_backward_deterministic": ([P, P, P, P, P, P, P, P, P, I, I, I, I, F, I, P, Z, P],
+                                          I),
             "fa_backward_dropout": ([P, P, P, P, P, P, P, P, P, I, I, I, I, F, I, F, U, UI, P, Z,
                                      P], I),
         }
@@ -177,6 +179,14 @@ def fa_backward_dropout(q, k, v, o, dO, lse, dq, dk, dv, B, H, N, d, scale, caus
                                       _p(dk), _p(dv), B, H, N, d, float(scale), int(bool(causal)),
                                       float(p_drop), int(seed), int(offset), _p(workspace),
                                       int(workspace_bytes), _s(stream))
+
+
+def fa_backward_deterministic(q, k, v, o, dO, lse, dq, dk, dv, B, H, N, d, scale, causal,
+                              workspace, workspace_bytes, stream=None) -> int:
+    return load().fa_backward_deterministic(_p(q), _p(k), _p(v), _p(o), _p(dO), _p(lse), _p(dq),
+                                            _p(dk), _p(dv), B, H, N, d, float(scale),
+                                            int(bool(causal)), _p(workspace),
+                                            int(workspace_bytes), _s(stream))
 
 
 def fa_backward_workspace_size(B, H, N, d) -> int:

@@ -16,8 +16,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libfa_gb300.so")
-SOURCES = ["fa_fwd.cu", "fa_bwd.cu", "fa_aux.cu", "fa_api.cu", "fa_noalloc.cu"]
-HEADERS = ["fa_ptx.cuh", "fa_sched.cuh", "fa_internal.h"]
+SOURCES = ["fa_fwd.cu", "fa_bwd.cu", "fa_bwd_dq.cu", "fa_aux.cu", "fa_api.cu", "fa_noalloc.cu"]
+HEADERS = ["fa_ptx.cuh", "fa_sched.cuh", "fa_internal.h", "fa_philox.cuh"]
 CUDA_HOME = os.environ.get("CUDA_HOME", "/usr/local/cuda")
 NVCC = os.path.join(CUDA_HOME, "bin", "nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

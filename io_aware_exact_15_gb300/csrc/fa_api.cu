@@ -486,6 +486,59 @@ fa_status fa_backward_varlen(const void* q, const void* k, const void* v, const 
   return fa_backward_dq_convert(dq, 1, H, total, d, scale, workspace, workspace_bytes, stream);
 }
 
+fa_status fa_backward_deterministic(const void* q, const void* k, const void* v, const void* o,
+                                    const void* dO, const float* lse, void* dq, void* dk, void* dv,
+                                    int B, int H, int N, int d, float scale, int causal,
+                                    void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  FA_TRY(check_bwd_args(q, k, v, o, dO, lse, dq, dk, dv, B, H, N, d, scale));
+  const size_t rows = static_cast<size_t>(B) * H * N;
+  FA_TRY(check_ws(workspace, workspace_bytes, align256(rows * sizeof(float))));
+  fa_status st = FA_OK;
+  int* err = status_word(&st);
+  if (!err) return st;
+  float* delta = static_cast<float*>(workspace);
+  // D only: the dQ accumulator is not used
+  FA_CUDA(fa::launch_bwd_preprocess(o, dO, delta, nullptr, static_cast<long long>(rows), d,
+                                    stream));
+  CUtensorMap tq, tk, tv, tdo, tdq;
+  // tdq is never dereferenced by the key-tile pass without its dQ product;
+  // it only has to be a well-formed map
+  if (!fa::make_tile_map(&tq, q, B * H, N, d) || !fa::make_tile_map(&tk, k, B * H, N, d) ||
+      !fa::make_tile_map(&tv, v, B * H, N, d) || !fa::make_tile_map(&tdo, dO, B * H, N, d) ||
+      !fa::make_acc_map(&tdq, workspace, 1, 32, 32))
+    return FA_ERR_CUDA;
+  fa::BwdParams p;
+  p.lse = lse;
+  p.delta = delta;
+  p.dk = dk;
+  p.dv = dv;
+  p.B = B;
+  p.H = H;
+  p.Hkv = H;
+  p.N = N;
+  p.d = d;
+  p.scale = scale;
+  p.causal = causal ? 1 : 0;
+  p.skip_dq = 1;
+  p.err = err;
+  p.wait_ns = wait_limit_ns();
+  FA_CUDA(fa::launch_backward_main(p, tq, tk, tv, tdo, tdq, stream));
+  fa::DqParams pq;
+  pq.lse = lse;
+  pq.delta = delta;
+  pq.dq = dq;
+  pq.B = B;
+  pq.H = H;
+  pq.N = N;
+  pq.d = d;
+  pq.scale = scale;
+  pq.causal = p.causal;
+  pq.err = err;
+  pq.wait_ns = p.wait_ns;
+  FA_CUDA(fa::launch_backward_dq(pq, tq, tk, tv, tdo, stream));
+  return FA_OK;
+}
+
 fa_status fa_forward_dropout(const void* q, const void* k, const void* v, void* o, float* lse,
                              int B, int H, int N, int d, float scale, int causal, float p_drop,
                              unsigned long long seed, unsigned offset, cudaStream_t stream) {

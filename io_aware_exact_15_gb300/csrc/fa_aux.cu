@@ -95,8 +95,10 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const uint4* __restrict
             bf16_lo(a.y) * bf16_lo(b.y) + bf16_hi(a.y) * bf16_hi(b.y) +
             bf16_lo(a.z) * bf16_lo(b.z) + bf16_hi(a.z) * bf16_hi(b.z) +
             bf16_lo(a.w) * bf16_lo(b.w) + bf16_hi(a.w) * bf16_hi(b.w);
-      dq_acc[2 * t] = make_float4(0.f, 0.f, 0.f, 0.f);
-      dq_acc[2 * t + 1] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (dq_acc) {  // null when dQ does not go through the accumulator
+        dq_acc[2 * t] = make_float4(0.f, 0.f, 0.f, 0.f);
+        dq_acc[2 * t + 1] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
     }
 #pragma unroll
     for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);

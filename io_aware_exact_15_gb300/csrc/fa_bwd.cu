@@ -69,7 +69,9 @@ struct BwdSmem {
 constexpr int kBwdThreads = 384;
 constexpr float kLog2e = 1.4426950408889634f;
 
-template <int D, int KIND>
+// DQ = false: no dQ product and no reduce-adds (dQ comes from the query-tile
+// pass of the deterministic backward)
+template <int D, int KIND, bool DQ = true>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     fa_bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
@@ -293,7 +295,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (!(ok = wait_bar(bar(L::B_DSR), n & 1, wc))) break;
         tc_fence_after();
         const uint32_t qv = sb + L::QR + qpos * L::TILE;
-        if (D != 64 || n == 0 || mbar_try(bar(L::B_DQE), (n - 1) & 1)) {
+        if (!DQ) {
+          issue_tt(tDK, sb + L::DS, qv, n > 0);
+          mma_commit(bar(L::B_QE + qpos));
+        } else if (D != 64 || n == 0 || mbar_try(bar(L::B_DQE), (n - 1) & 1)) {
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < kTile / 16; ++kk) {
@@ -311,7 +316,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           mma_commit(bar(L::B_DQF));
         }
         if (have_n) {
-          if (D != 64) {  // dQ_i shares the dP columns: wait until it is read out
+          if (DQ && D != 64) {  // dQ_i shares the dP columns: wait until it is read out
             if (!(ok = wait_bar(bar(L::B_DQE), n & 1, wc))) break;
             tc_fence_after();
           }
@@ -467,7 +472,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       fence_async_smem();
       tc_fence_before();
       mbar_arrive(bar(L::B_PR));
-      if (n > 0 && !drain_dq(n - 1, qt_prev, g_prev)) {
+      if (DQ && n > 0 && !drain_dq(n - 1, qt_prev, g_prev)) {
         ok = false;
         break;
       }
@@ -512,7 +517,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       dlt_c = dlt_n;
       ++n;
     }
-    if (ok && n > 0) ok = drain_dq(n - 1, qt_prev, g_prev);
+    if (DQ && ok && n > 0) ok = drain_dq(n - 1, qt_prev, g_prev);
     if (lane == 0) bulk_wait_all();  // every dQ reduce of this warp has landed
     // ---------------------------------------------------- epilogue: dV, dK
     // warps 4-7 write dV_j, warps 8-11 write scale * dK_j (thread = key row)
@@ -560,17 +565,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
 }
 
-template <int D, int KIND>
+template <int D, int KIND, bool DQ = true>
 cudaError_t launch_bwd_d(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                          const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq,
                          cudaStream_t stream) {
   using L = BwdSmem<D>;
-  cudaError_t e = cudaFuncSetAttribute(fa_bwd_kernel<D, KIND>,
+  cudaError_t e = cudaFuncSetAttribute(fa_bwd_kernel<D, KIND, DQ>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
   if (e != cudaSuccess) return e;
   const int nT = (p.N + kTile - 1) / kTile;
   const long long ctas = static_cast<long long>(nT) * p.B * (p.Hkv > 0 ? p.Hkv : p.H);
-  fa_bwd_kernel<D, KIND><<<static_cast<unsigned>(ctas), kBwdThreads, L::ALLOC, stream>>>(
+  fa_bwd_kernel<D, KIND, DQ><<<static_cast<unsigned>(ctas), kBwdThreads, L::ALLOC, stream>>>(
       tq, tk, tv, tdo, tdq, p);
   return cudaGetLastError();
 }
@@ -583,6 +588,12 @@ cudaError_t launch_backward_main(const BwdParams& p, const CUtensorMap& tq, cons
   const int kind = p.drop.t ? kGeneralDropout
                    : p.cu_seqlens ? kGeneral
                    : (p.Hkv > 0 && p.Hkv != p.H) ? kGrouped : kPlain;
+  if (p.skip_dq) {  // deterministic backward: plain layout only
+    if (kind != kPlain) return cudaErrorInvalidValue;
+    if (p.d == 64) return launch_bwd_d<64, kPlain, false>(p, tq, tk, tv, tdo, tdq, stream);
+    if (p.d == 128) return launch_bwd_d<128, kPlain, false>(p, tq, tk, tv, tdo, tdq, stream);
+    return cudaErrorInvalidValue;
+  }
   if (p.d == 64) {
     if (kind == kGeneralDropout)
       return launch_bwd_d<64, kGeneralDropout>(p, tq, tk, tv, tdo, tdq, stream);

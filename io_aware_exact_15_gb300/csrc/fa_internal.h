@@ -63,6 +63,7 @@ struct BwdParams {
   const int* cu_seqlens = nullptr;  // variable-length batch (as FwdParams)
   int total = 0;
   DropoutParams drop;
+  int skip_dq = 0;  // 1: no dQ product (dQ comes from the query-tile pass)
   int* err = nullptr;
   uint64_t wait_ns = 0;
 };
@@ -88,6 +89,23 @@ cudaError_t launch_backward_main(const BwdParams& p, const CUtensorMap& tq,
                                  const CUtensorMap& tk, const CUtensorMap& tv,
                                  const CUtensorMap& tdo, const CUtensorMap& tdq,
                                  cudaStream_t stream);
+// Query-tile dQ pass of the deterministic backward (plain layout).
+struct DqParams {
+  const float* lse = nullptr;
+  const float* delta = nullptr;
+  void* dq = nullptr;  // bf16 [B, H, N, d], written whole
+  int B = 0, H = 0, N = 0, d = 0;
+  float scale = 0.f;
+  int causal = 0;
+  TileLists lists;
+  int* err = nullptr;
+  uint64_t wait_ns = 0;
+};
+
+cudaError_t launch_backward_dq(const DqParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
+                               const CUtensorMap& tv, const CUtensorMap& tdo,
+                               cudaStream_t stream);
+
 cudaError_t launch_bwd_preprocess(const void* o, const void* dO, float* delta, float* dq_acc,
                                   long long rows, int d, cudaStream_t stream);
 cudaError_t launch_dq_convert(const float* dq_acc, void* dq, long long n, float scale,

@@ -176,3 +176,15 @@ def test_dropout_rejects_bad_probability():
         fa.FA_ERR_UNSUPPORTED
     assert fa.fa_backward_dropout(A, A, A, A, A, A, A, A, A, 1, 2, 256, 64, 0.1, 0, 0.1, 1, 0, A,
                                   need - 1, 0) == fa.FA_ERR_WORKSPACE
+
+
+def test_deterministic_backward_validates():
+    A = ALIGNED
+    need = (1 * 2 * 300 * 4 + 255) // 256 * 256
+    args = (A, A, A, A, A, A, A, A, A, 1, 2, 300, 64, 0.1, 0)
+    assert fa.fa_backward_deterministic(*args, A, need - 1, 0) == fa.FA_ERR_WORKSPACE
+    assert fa.fa_backward_deterministic(*args, None, need, 0) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_backward_deterministic(A, A, A, A, A, A, MIS, A, A, 1, 2, 300, 64, 0.1, 0, A,
+                                        need, 0) == fa.FA_ERR_MISALIGNED
+    assert fa.fa_backward_deterministic(A, A, A, A, A, A, A, A, A, 1, 2, 300, 96, 0.1, 0, A,
+                                        need, 0) == fa.FA_ERR_UNSUPPORTED
