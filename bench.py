@@ -25,6 +25,7 @@ import subprocess
 import sys
 import threading
 import time
+import types
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
@@ -183,33 +184,49 @@ def run_gpu(args, rank, world, dist):
     bws = ws[lists_bytes:] if sparse else ws
     bwb = nbytes - lists_bytes
 
-    def forward():
+    # device buffers of one step (the double-buffered e2e loop uses two sets)
+    def buffer_set(src=None):
+        if src is not None:
+            return types.SimpleNamespace(**vars(src))
+        with torch.cuda.stream(stream):
+            bs = types.SimpleNamespace(
+                qd=torch.empty_like(qd), kd=torch.empty_like(kd), vd=torch.empty_like(vd),
+                dod=torch.empty_like(dod), md=None if md is None else torch.empty_like(md),
+                cud=None if cud is None else torch.empty_like(cud), o=torch.empty_like(o),
+                lse=torch.empty_like(lse), dq=torch.empty_like(dq), dk=torch.empty_like(dk),
+                dv=torch.empty_like(dv))
+        return bs
+
+    b0 = types.SimpleNamespace(qd=qd, kd=kd, vd=vd, dod=dod, md=md, cud=cud, o=o, lse=lse,
+                               dq=dq, dk=dk, dv=dv)
+
+    def forward(bs):
         if varlen:
-            check(fa.fa_forward_varlen(qd, kd, vd, o, lse, cud, B, max_seqlen, T, H, Hkv, d,
+            check(fa.fa_forward_varlen(bs.qd, bs.kd, bs.vd, bs.o, bs.lse, bs.cud, B, max_seqlen, T, H, Hkv, d,
                                        w.scale, w.causal, *drop, s_ptr), "forward")
         elif w.dropout > 0:
-            check(fa.fa_forward_dropout(qd, kd, vd, o, lse, B, H, N, d, w.scale, w.causal, *drop,
+            check(fa.fa_forward_dropout(bs.qd, bs.kd, bs.vd, bs.o, bs.lse, B, H, N, d, w.scale, w.causal, *drop,
                                         s_ptr), "forward")
         elif gqa:
-            check(fa.fa_forward_gqa(qd, kd, vd, o, lse, B, H, Hkv, N, d, w.scale, w.causal,
+            check(fa.fa_forward_gqa(bs.qd, bs.kd, bs.vd, bs.o, bs.lse, B, H, Hkv, N, d, w.scale, w.causal,
                                     s_ptr), "forward")
         else:
-            check(fa.fa_forward(qd, kd, vd, o, lse, B, H, N, d, w.scale, w.causal, s_ptr),
+            check(fa.fa_forward(bs.qd, bs.kd, bs.vd, bs.o, bs.lse, B, H, N, d, w.scale, w.causal, s_ptr),
                   "forward")
 
-    def backward_whole():
+    def backward_whole(bs):
         if det:
-            check(fa.fa_backward_deterministic(qd, kd, vd, o, dod, lse, dq, dk, dv, B, H, N, d,
+            check(fa.fa_backward_deterministic(bs.qd, bs.kd, bs.vd, bs.o, bs.dod, bs.lse, bs.dq, bs.dk, bs.dv, B, H, N, d,
                                                w.scale, w.causal, ws, nbytes, s_ptr), "backward")
         elif varlen:
-            check(fa.fa_backward_varlen(qd, kd, vd, o, dod, lse, dq, dk, dv, cud, B, max_seqlen,
+            check(fa.fa_backward_varlen(bs.qd, bs.kd, bs.vd, bs.o, bs.dod, bs.lse, bs.dq, bs.dk, bs.dv, bs.cud, B, max_seqlen,
                                         T, H, Hkv, d, w.scale, w.causal, *drop, ws, nbytes,
                                         s_ptr), "backward")
         elif w.dropout > 0:
-            check(fa.fa_backward_dropout(qd, kd, vd, o, dod, lse, dq, dk, dv, B, H, N, d, w.scale,
+            check(fa.fa_backward_dropout(bs.qd, bs.kd, bs.vd, bs.o, bs.dod, bs.lse, bs.dq, bs.dk, bs.dv, B, H, N, d, w.scale,
                                          w.causal, *drop, ws, nbytes, s_ptr), "backward")
         else:
-            check(fa.fa_backward_gqa(qd, kd, vd, o, dod, lse, dq, dk, dv, B, H, Hkv, N, d,
+            check(fa.fa_backward_gqa(bs.qd, bs.kd, bs.vd, bs.o, bs.dod, bs.lse, bs.dq, bs.dk, bs.dv, B, H, Hkv, N, d,
                                      w.scale, w.causal, ws, nbytes, s_ptr), "backward")
 
     # One step; `ev` (5 events) splits it into its kernels.  Grouped-head and
@@ -217,40 +234,41 @@ def run_gpu(args, rank, world, dist):
     # step then brackets their whole backward and times the row-wise
     # preprocess and dQ conversion beside it (the main kernel's time is the
     # difference); the unsplit step is exactly forward + backward.
-    def step(ev=None):
+    def step(ev=None, bs=None):
+        bs = bs or b0
         rec = (lambda i: ev[i].record(stream)) if ev else (lambda i: None)
         rec(0)
         if sparse:
-            check(fa.fa_blocksparse_forward(qd, kd, vd, o, lse, B, H, N, d, w.scale, w.causal, md,
+            check(fa.fa_blocksparse_forward(bs.qd, bs.kd, bs.vd, bs.o, bs.lse, B, H, N, d, w.scale, w.causal, bs.md,
                                             mh, ws, nbytes, s_ptr), "forward")
             rec(1)
             rec(2)
-            check(fa.fa_blocksparse_backward(qd, kd, vd, o, dod, lse, dq, dk, dv, B, H, N, d,
-                                             w.scale, w.causal, md, mh, ws, nbytes, s_ptr),
+            check(fa.fa_blocksparse_backward(bs.qd, bs.kd, bs.vd, bs.o, bs.dod, bs.lse, bs.dq, bs.dk, bs.dv, B, H, N, d,
+                                             w.scale, w.causal, bs.md, mh, ws, nbytes, s_ptr),
                   "backward")
             rec(3)
             rec(4)
             return
-        forward()
+        forward(bs)
         rec(1)
         if combined:
             if ev:
-                check(fa.fa_backward_preprocess(o, dod, rows_b, H, rows_n, d, bws, bwb, s_ptr),
+                check(fa.fa_backward_preprocess(bs.o, bs.dod, rows_b, H, rows_n, d, bws, bwb, s_ptr),
                       "preprocess")
             rec(2)
-            backward_whole()
+            backward_whole(bs)
             rec(3)
             if ev and not det:  # the deterministic backward has no conversion pass
-                check(fa.fa_backward_dq_convert(dq, rows_b, H, rows_n, d, w.scale, bws, bwb,
+                check(fa.fa_backward_dq_convert(bs.dq, rows_b, H, rows_n, d, w.scale, bws, bwb,
                                                 s_ptr), "convert")
             rec(4)
             return
-        check(fa.fa_backward_preprocess(o, dod, B, H, N, d, bws, bwb, s_ptr), "preprocess")
+        check(fa.fa_backward_preprocess(bs.o, bs.dod, B, H, N, d, bws, bwb, s_ptr), "preprocess")
         rec(2)
-        check(fa.fa_backward_main(qd, kd, vd, dod, lse, dk, dv, B, H, N, d, w.scale, w.causal,
+        check(fa.fa_backward_main(bs.qd, bs.kd, bs.vd, bs.dod, bs.lse, bs.dk, bs.dv, B, H, N, d, w.scale, w.causal,
                                   bws, bwb, s_ptr), "backward")
         rec(3)
-        check(fa.fa_backward_dq_convert(dq, B, H, N, d, w.scale, bws, bwb, s_ptr), "convert")
+        check(fa.fa_backward_dq_convert(bs.dq, B, H, N, d, w.scale, bws, bwb, s_ptr), "convert")
         rec(4)
 
     launches_per_step = (2 + 4) if sparse else 4
@@ -332,30 +350,77 @@ def run_gpu(args, rank, world, dist):
     if varlen:
         h2d += hcu.numel() * hcu.element_size()
 
-    def e2e_step():
-        with torch.cuda.stream(stream):
-            for dst, src in ((qd, hq), (kd, hk), (vd, hv), (dod, hdo)):
+    # Streamed batches: step i's inputs go up on `cin`, its forward + backward
+    # run on the compute stream, its outputs come down on `cout`; two buffer
+    # sets let the copies of steps i+1 and i-1 overlap the compute of step i.
+    # Every step's host -> device and device -> host copies are inside the
+    # timed region.
+    sets = [b0, buffer_set()]
+    cin = torch.cuda.Stream(device=dev)
+    cout = torch.cuda.Stream(device=dev)
+    ev_in = [torch.cuda.Event() for _ in range(2)]      # inputs of set s loaded
+    ev_done = [torch.cuda.Event() for _ in range(2)]    # compute on set s finished
+    ev_out = [torch.cuda.Event() for _ in range(2)]     # outputs of set s copied out
+    used = [False, False]
+
+    def e2e_step(i):
+        sidx = i & 1
+        bs = sets[sidx]
+        with torch.cuda.stream(cin):
+            if used[sidx]:
+                cin.wait_event(ev_done[sidx])  # the set's previous inputs are consumed
+            for dst, src in ((bs.qd, hq), (bs.kd, hk), (bs.vd, hv), (bs.dod, hdo)):
                 dst.copy_(src, non_blocking=True)
             if sparse:
-                md.copy_(hm, non_blocking=True)
+                bs.md.copy_(hm, non_blocking=True)
             if varlen:
-                cud.copy_(hcu, non_blocking=True)
-        step()
-        with torch.cuda.stream(stream):
-            for dst, src in ((ho, o), (hl, lse), (hdq, dq), (hdk, dk), (hdv, dv)):
+                bs.cud.copy_(hcu, non_blocking=True)
+            ev_in[sidx].record(cin)
+        stream.wait_event(ev_in[sidx])
+        if used[sidx]:
+            stream.wait_event(ev_out[sidx])  # the set's previous outputs are copied out
+        step(bs=bs)
+        ev_done[sidx].record(stream)
+        with torch.cuda.stream(cout):
+            cout.wait_event(ev_done[sidx])
+            for dst, src in ((ho, bs.o), (hl, bs.lse), (hdq, bs.dq), (hdk, bs.dk), (hdv, bs.dv)):
                 dst.copy_(src, non_blocking=True)
+            ev_out[sidx].record(cout)
+        used[sidx] = True
 
-    for _ in range(3):
-        e2e_step()
+    for i in range(4):
+        e2e_step(i)
     torch.cuda.synchronize(dev)
     Ke = max(3, min(K, 200))
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(Ke):
-        e2e_step()
-    b.record(stream)
+    a.record(cin)
+    for i in range(Ke):
+        e2e_step(i)
+    b.record(cout)
     torch.cuda.synchronize(dev)
     ems = a.elapsed_time(b) / Ke
+    # the same steps one after another on one stream, for comparison
+    def serial_step():
+        with torch.cuda.stream(stream):
+            for dst, src in ((b0.qd, hq), (b0.kd, hk), (b0.vd, hv), (b0.dod, hdo)):
+                dst.copy_(src, non_blocking=True)
+            if sparse:
+                b0.md.copy_(hm, non_blocking=True)
+            if varlen:
+                b0.cud.copy_(hcu, non_blocking=True)
+        step()
+        with torch.cuda.stream(stream):
+            for dst, src in ((ho, b0.o), (hl, b0.lse), (hdq, b0.dq), (hdk, b0.dk), (hdv, b0.dv)):
+                dst.copy_(src, non_blocking=True)
+    serial_step()
+    torch.cuda.synchronize(dev)
+    a2, b2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a2.record(stream)
+    for _ in range(Ke):
+        serial_step()
+    b2.record(stream)
+    torch.cuda.synchronize(dev)
+    ems_serial = a2.elapsed_time(b2) / Ke
     if dist is not None:
         t = torch.tensor([ems], dtype=torch.float64, device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -363,8 +428,10 @@ def run_gpu(args, rank, world, dist):
     e2e = {"value": round(world * fb / (ems * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
            "ms_per_step": round(ems, 4), "h2d_bytes_per_step": int(h2d),
            "d2h_bytes_per_step": int(d2h),
-           "path": "pinned host -> device copies, forward + backward via the C ABI, "
-                   "device -> host copies of o, lse, dq, dk, dv"}
+           "path": "per step: pinned host -> device copies of the inputs, forward + backward "
+                   "via the C ABI, device -> host copies of o, lse, dq, dk, dv; streamed with "
+                   "two device buffer sets so the copies of neighbouring steps overlap compute",
+           "serial_ms_per_step": round(ems_serial, 4)}
 
     src_hash = kernel_source_hash(["fa_bwd.cu", "fa_ptx.cuh", "fa_sched.cuh"])
     main_flops = 2.5 * ff
