@@ -18,6 +18,8 @@ namespace fa {
 __global__ void __launch_bounds__(1024) fa_lists_kernel(const uint8_t* __restrict__ mask, int nT,
                                                         int* row_ptr, int* col_idx, int* col_ptr,
                                                         int* row_idx) {
+  grid_dep_wait();  // the previous kernel's writes are visible from here on
+  grid_dep_launch();
   extern __shared__ int cnt[];  // [nT + 1]
   const int h = blockIdx.x;
   const uint8_t* m = mask + static_cast<size_t>(h) * nT * nT;
@@ -68,85 +70,122 @@ cudaError_t launch_build_lists(const uint8_t* mask, int mask_heads, int nT, int*
         cudaFuncSetAttribute(fa_lists_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
   }
-  fa_lists_kernel<<<mask_heads, 1024, smem, stream>>>(mask, nT, row_ptr, col_idx, col_ptr, row_idx);
-  return cudaGetLastError();
+  return launch_pdl(fa_lists_kernel, dim3(mask_heads), dim3(1024), smem, stream, mask, nT, row_ptr,
+                    col_idx, col_ptr, row_idx);
 }
 
 // ------------------------------------------------------------------ backward helpers
-// D_i = sum_c dO_ic O_ic in fp32 and dQ_acc = 0.  Each thread takes 8
-// consecutive elements of a row (16-byte loads of O and dO, 32 bytes of
-// zeros); the D/8 threads of a row reduce with shuffles.
+// D_i = sum_c dO_ic O_ic in fp32 and dQ_acc = 0.  Each thread takes items of
+// 8 consecutive elements of a row (16-byte loads of O and dO, 32 bytes of
+// zeros); the D/8 threads of a row reduce with shuffles.  Every thread keeps
+// kUnroll grid-stride items in flight, and the grid is sized so that each
+// thread has about that many.
+constexpr int kUnroll = 4;
+
 template <int D>
 __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const uint4* __restrict__ o,
                                                          const uint4* __restrict__ dO,
                                                          float* __restrict__ delta,
                                                          float4* __restrict__ dq_acc,
                                                          long long rows) {
+  grid_dep_wait();  // the previous kernel's writes are visible from here on
+  grid_dep_launch();
   constexpr int TPR = D / 8;  // threads per row: 8 or 16
   const long long total = rows * TPR;
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
-  for (long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-       t - (threadIdx.x & 31) < total; t += stride) {
-    const bool live = t < total;
-    float acc = 0.f;
-    if (live) {
-      const uint4 a = o[t], b = dO[t];
-      acc = bf16_lo(a.x) * bf16_lo(b.x) + bf16_hi(a.x) * bf16_hi(b.x) +
-            bf16_lo(a.y) * bf16_lo(b.y) + bf16_hi(a.y) * bf16_hi(b.y) +
-            bf16_lo(a.z) * bf16_lo(b.z) + bf16_hi(a.z) * bf16_hi(b.z) +
-            bf16_lo(a.w) * bf16_lo(b.w) + bf16_hi(a.w) * bf16_hi(b.w);
-      if (dq_acc) {  // null when dQ does not go through the accumulator
-        dq_acc[2 * t] = make_float4(0.f, 0.f, 0.f, 0.f);
-        dq_acc[2 * t + 1] = make_float4(0.f, 0.f, 0.f, 0.f);
+  // the loop condition is warp-uniform (the warp's first item), so every
+  // lane takes part in the shuffles
+  for (long long t0 = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+       t0 - (threadIdx.x & 31) < total; t0 += kUnroll * stride) {
+    uint4 a[kUnroll], b[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const long long t = t0 + u * stride;
+      if (t < total) {
+        a[u] = o[t];
+        b[u] = dO[t];
+      } else {
+        a[u] = make_uint4(0u, 0u, 0u, 0u);
+        b[u] = a[u];
       }
     }
 #pragma unroll
-    for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (live && (t % TPR) == 0) delta[t / TPR] = acc;
+    for (int u = 0; u < kUnroll; ++u) {
+      const long long t = t0 + u * stride;
+      float acc = bf16_lo(a[u].x) * bf16_lo(b[u].x) + bf16_hi(a[u].x) * bf16_hi(b[u].x) +
+                  bf16_lo(a[u].y) * bf16_lo(b[u].y) + bf16_hi(a[u].y) * bf16_hi(b[u].y) +
+                  bf16_lo(a[u].z) * bf16_lo(b[u].z) + bf16_hi(a[u].z) * bf16_hi(b[u].z) +
+                  bf16_lo(a[u].w) * bf16_lo(b[u].w) + bf16_hi(a[u].w) * bf16_hi(b[u].w);
+      if (dq_acc && t < total) {  // null when dQ does not go through the accumulator
+        dq_acc[2 * t] = make_float4(0.f, 0.f, 0.f, 0.f);
+        dq_acc[2 * t + 1] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+      if (t < total && (t % TPR) == 0) delta[t / TPR] = acc;
+    }
   }
+}
+
+// enough 256-thread blocks for about kUnroll items per thread, at most
+// `per_sm` blocks per SM of a 152-SM GPU
+static int stream_blocks(long long items, int per_sm) {
+  const long long want = (items + 256LL * kUnroll - 1) / (256LL * kUnroll);
+  const long long cap = 152LL * per_sm;
+  return static_cast<int>(want < 1 ? 1 : (want < cap ? want : cap));
 }
 
 cudaError_t launch_bwd_preprocess(const void* o, const void* dO, float* delta, float* dq_acc,
                                   long long rows, int d, cudaStream_t stream) {
-  const long long threads = rows * (d / 8);
-  const long long want = (threads + 255) / 256;
-  const int blocks = static_cast<int>(want < 152LL * 32 ? want : 152LL * 32);
+  const int blocks = stream_blocks(rows * (d / 8), 8);
+  const uint4* o4 = static_cast<const uint4*>(o);
+  const uint4* do4 = static_cast<const uint4*>(dO);
+  float4* acc4 = reinterpret_cast<float4*>(dq_acc);
   if (d == 64)
-    fa_bwd_pre_kernel<64><<<blocks, 256, 0, stream>>>(static_cast<const uint4*>(o),
-                                                      static_cast<const uint4*>(dO), delta,
-                                                      reinterpret_cast<float4*>(dq_acc), rows);
-  else
-    fa_bwd_pre_kernel<128><<<blocks, 256, 0, stream>>>(static_cast<const uint4*>(o),
-                                                       static_cast<const uint4*>(dO), delta,
-                                                       reinterpret_cast<float4*>(dq_acc), rows);
-  return cudaGetLastError();
+    return launch_pdl(fa_bwd_pre_kernel<64>, dim3(blocks), dim3(256), 0, stream, o4, do4, delta,
+                      acc4, rows);
+  return launch_pdl(fa_bwd_pre_kernel<128>, dim3(blocks), dim3(256), 0, stream, o4, do4, delta,
+                    acc4, rows);
 }
 
-// dq = bf16(scale * dq_acc), 8 elements per thread
+// dq = bf16(scale * dq_acc), 8 elements per item, kUnroll items in flight
 __global__ void __launch_bounds__(256) fa_dq_convert_kernel(const float4* __restrict__ acc,
                                                             uint4* __restrict__ dq, long long n8,
                                                             float scale) {
+  grid_dep_wait();  // the previous kernel's writes are visible from here on
+  grid_dep_launch();
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
-  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
-       i += stride) {
-    const float4 a = acc[2 * i], b = acc[2 * i + 1];
-    uint4 w;
-    w.x = pack_bf16(a.x * scale, a.y * scale);
-    w.y = pack_bf16(a.z * scale, a.w * scale);
-    w.z = pack_bf16(b.x * scale, b.y * scale);
-    w.w = pack_bf16(b.z * scale, b.w * scale);
-    dq[i] = w;
+  for (long long i0 = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i0 < n8;
+       i0 += kUnroll * stride) {
+    float4 a[kUnroll], b[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const long long i = i0 + u * stride;
+      if (i < n8) {
+        a[u] = acc[2 * i];
+        b[u] = acc[2 * i + 1];
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const long long i = i0 + u * stride;
+      if (i < n8) {
+        uint4 w;
+        w.x = pack_bf16(a[u].x * scale, a[u].y * scale);
+        w.y = pack_bf16(a[u].z * scale, a[u].w * scale);
+        w.z = pack_bf16(b[u].x * scale, b[u].y * scale);
+        w.w = pack_bf16(b[u].z * scale, b[u].w * scale);
+        dq[i] = w;
+      }
+    }
   }
 }
 
 cudaError_t launch_dq_convert(const float* dq_acc, void* dq, long long n, float scale,
                               cudaStream_t stream) {
   const long long n8 = n / 8;
-  const long long want = (n8 + 255) / 256;
-  const int blocks = static_cast<int>(want < 152LL * 16 ? want : 152LL * 16);
-  fa_dq_convert_kernel<<<blocks, 256, 0, stream>>>(reinterpret_cast<const float4*>(dq_acc),
-                                                   static_cast<uint4*>(dq), n8, scale);
-  return cudaGetLastError();
+  return launch_pdl(fa_dq_convert_kernel, dim3(stream_blocks(n8, 8)), dim3(256), 0, stream,
+                    reinterpret_cast<const float4*>(dq_acc), static_cast<uint4*>(dq), n8, scale);
 }
 
 // ------------------------------------------------------------------ schedule export

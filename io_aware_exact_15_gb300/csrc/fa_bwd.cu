@@ -77,6 +77,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                   const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
                   const __grid_constant__ CUtensorMap tdq, const BwdParams p) {
   using L = BwdSmem<D>;
+  grid_dep_wait();  // the previous kernel's writes are visible from here on
+  grid_dep_launch();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -575,9 +577,8 @@ cudaError_t launch_bwd_d(const BwdParams& p, const CUtensorMap& tq, const CUtens
   if (e != cudaSuccess) return e;
   const int nT = (p.N + kTile - 1) / kTile;
   const long long ctas = static_cast<long long>(nT) * p.B * (p.Hkv > 0 ? p.Hkv : p.H);
-  fa_bwd_kernel<D, KIND, DQ><<<static_cast<unsigned>(ctas), kBwdThreads, L::ALLOC, stream>>>(
-      tq, tk, tv, tdo, tdq, p);
-  return cudaGetLastError();
+  return launch_pdl(fa_bwd_kernel<D, KIND, DQ>, dim3(static_cast<unsigned>(ctas)),
+                    dim3(kBwdThreads), L::ALLOC, stream, tq, tk, tv, tdo, tdq, p);
 }
 
 }  // namespace

@@ -60,6 +60,8 @@ __global__ void __launch_bounds__(kDqThreads, 1)
                      const __grid_constant__ CUtensorMap tv,
                      const __grid_constant__ CUtensorMap tdo, const DqParams p) {
   using L = DqSmem<D>;
+  grid_dep_wait();  // the previous kernel's writes are visible from here on
+  grid_dep_launch();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -341,9 +343,8 @@ cudaError_t launch_dq_d(const DqParams& p, const CUtensorMap& tq, const CUtensor
   if (e != cudaSuccess) return e;
   const int nT = (p.N + kTile - 1) / kTile;
   const long long ctas = static_cast<long long>(nT) * p.B * p.H;
-  fa_bwd_dq_kernel<D><<<static_cast<unsigned>(ctas), kDqThreads, L::ALLOC, stream>>>(tq, tk, tv,
-                                                                                    tdo, p);
-  return cudaGetLastError();
+  return launch_pdl(fa_bwd_dq_kernel<D>, dim3(static_cast<unsigned>(ctas)), dim3(kDqThreads),
+                    L::ALLOC, stream, tq, tk, tv, tdo, p);
 }
 
 }  // namespace

@@ -67,6 +67,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const FwdParams p) {
   using L = FwdSmem<D, NS_>;
+  grid_dep_wait();  // the previous kernel's writes are visible from here on
+  grid_dep_launch();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -431,9 +433,8 @@ cudaError_t launch_fwd_d(const FwdParams& p, const CUtensorMap& tq, const CUtens
   const int nT = (p.N + kTile - 1) / kTile;
   const int npairs = (NS_ != 0 && p.single_tile) ? nT : (nT + 1) / 2;
   const long long ctas = static_cast<long long>(npairs) * p.B * p.H;
-  fa_fwd_kernel<D, KIND, NS_>
-      <<<static_cast<unsigned>(ctas), kFwdThreads, L::ALLOC, stream>>>(tq, tk, tv, p);
-  return cudaGetLastError();
+  return launch_pdl(fa_fwd_kernel<D, KIND, NS_>, dim3(static_cast<unsigned>(ctas)),
+                    dim3(kFwdThreads), L::ALLOC, stream, tq, tk, tv, p);
 }
 
 }  // namespace

@@ -7,6 +7,25 @@
 
 namespace fa {
 
+// Launch with programmatic stream serialization (the kernel starts with
+// grid_dep_wait, see fa_ptx.cuh), so that its scheduling overlaps the tail of
+// the previous kernel in the stream.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 constexpr int kTile = 128;  // query rows and keys per tile (Br = Bc = 128)
 
 // Block-sparse tile lists for one mask head layout:

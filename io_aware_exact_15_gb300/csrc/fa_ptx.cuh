@@ -83,6 +83,16 @@ FA_DEV void drain_bar(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
   }
 }
 
+// ---------------------------------------------------------------- launch order
+// Kernels of the library are launched with programmatic stream serialization:
+// a kernel may be scheduled while the previous kernel in the stream is still
+// finishing, so each kernel waits (grid_dep_wait) before its first access to
+// global memory, which makes everything the previous kernel wrote visible,
+// and then lets the next kernel be scheduled (grid_dep_launch).  Without that
+// launch attribute both are no-ops.
+FA_DEV void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+FA_DEV void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---------------------------------------------------------------- TMA
 FA_DEV void prefetch_tmap(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
