@@ -434,10 +434,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       int lim = N - kcol0;
       if (p.causal && qrow - kcol0 + 1 < lim) lim = qrow - kcol0 + 1;
       uint32_t pw[32];  // pw[i]: keys 2i, 2i+1 of this thread's 64 columns
+      const uint64_t sl2x2 = f2_pack(sl2, sl2), nlse2x2 = f2_pack(-lse2, -lse2);
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
-        float a = ex2(fmaf(__uint_as_float(sv[i >> 4][(2 * i) & 31]), sl2, -lse2));
-        float b = ex2(fmaf(__uint_as_float(sv[i >> 4][(2 * i + 1) & 31]), sl2, -lse2));
+        // scale * S * log2 e - lse * log2 e for two keys in one fp32 x2 FMA
+        float a, b;
+        f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[i >> 4][(2 * i) & 31]),
+                                 __uint_as_float(sv[i >> 4][(2 * i + 1) & 31])),
+                         sl2x2, nlse2x2),
+                  a, b);
+        a = ex2(a);
+        b = ex2(b);
         if (need_mask) {
           if (2 * i >= lim) a = 0.f;
           if (2 * i + 1 >= lim) b = 0.f;
@@ -482,6 +489,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       ok = __all_sync(0xffffffffu, wait_bar(bar(L::B_DPF), n & 1, wc));
       if (!ok) break;
       tc_fence_after();
+      const uint64_t dltx2 = f2_pack(dlt_c, dlt_c);
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         uint32_t dp[32];
@@ -500,8 +508,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
               d0 = ((kb[c] >> (8 * g + 2 * j)) & 1u) ? d0 * p.drop.scale : 0.f;
               d1 = ((kb[c] >> (8 * g + 2 * j + 1)) & 1u) ? d1 * p.drop.scale : 0.f;
             }
-            const float x0 = bf16_lo(pp) * (d0 - dlt_c);
-            const float x1 = bf16_hi(pp) * (d1 - dlt_c);
+            // P o (dP - D) for the two keys in fp32 x2
+            float x0, x1;
+            f2_unpack(f2_mul(f2_pack(bf16_lo(pp), bf16_hi(pp)),
+                             f2_sub(f2_pack(d0, d1), dltx2)),
+                      x0, x1);
             w[j] = pack_bf16(x0, x1);
           }
           st_shared_v4(dsbuf + sw128_offset(r, 4 * c + g), w[0], w[1], w[2], w[3]);

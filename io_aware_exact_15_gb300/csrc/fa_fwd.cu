@@ -306,11 +306,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       }
       float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        mx0 = fmaxf(mx0, __uint_as_float(sr[0][j]));
-        mx1 = fmaxf(mx1, __uint_as_float(sr[1][j]));
-        mx2 = fmaxf(mx2, __uint_as_float(sr[2][j]));
-        mx3 = fmaxf(mx3, __uint_as_float(sr[3][j]));
+      for (int j = 0; j < 32; j += 2) {  // two scores per three-input max
+        mx0 = fmax3(mx0, __uint_as_float(sr[0][j]), __uint_as_float(sr[0][j + 1]));
+        mx1 = fmax3(mx1, __uint_as_float(sr[1][j]), __uint_as_float(sr[1][j + 1]));
+        mx2 = fmax3(mx2, __uint_as_float(sr[2][j]), __uint_as_float(sr[2][j + 1]));
+        mx3 = fmax3(mx3, __uint_as_float(sr[3][j]), __uint_as_float(sr[3][j + 1]));
       }
       const float m_new = fmaxf(m, fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2);
       const bool resc = m_new > m + kRescaleLog2;
@@ -321,7 +321,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       }
       const bool rescale_o = cnt > 0 && __any_sync(0xffffffffu, resc);
       const float mu = (m == -INFINITY) ? 0.f : m;
-      float ls0 = 0.f, ls1 = 0.f;
+      const uint64_t sl2x2 = f2_pack(sl2, sl2), nmux2 = f2_pack(-mu, -mu);
+      uint64_t lsa = 0ull, lsb = 0ull;  // row-sum partials, fp32 x2 (0 bits = +0.0)
       PhiloxOut rw;
       // P (bf16, two per 32-bit column) overwrites the first 64 columns of
       // this tile's S, which are already in registers
@@ -333,15 +334,22 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         for (int c4 = 0; c4 < 4; ++c4) {
           float e[8];
 #pragma unroll
-          for (int j = 0; j < 8; ++j) e[j] = ex2(fmaf(__uint_as_float(sr[q][8 * c4 + j]), sl2, -mu));
+          for (int j = 0; j < 8; j += 2) {  // exponent arguments of two keys per FMA
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[q][8 * c4 + j]),
+                                     __uint_as_float(sr[q][8 * c4 + j + 1])),
+                             sl2x2, nmux2),
+                      e[j], e[j + 1]);
+            e[j] = ex2(e[j]);
+            e[j + 1] = ex2(e[j + 1]);
+          }
 #pragma unroll
           for (int j = 0; j < 4; ++j) sr[q][4 * c4 + j] = pack_bf16(e[2 * j], e[2 * j + 1]);
           // l sums the same bf16-rounded weights the PV MMA consumes, so a
           // dominant key's rounding cancels in O / l
-          ls0 += (bf16_lo(sr[q][4 * c4]) + bf16_hi(sr[q][4 * c4])) +
-                 (bf16_lo(sr[q][4 * c4 + 1]) + bf16_hi(sr[q][4 * c4 + 1]));
-          ls1 += (bf16_lo(sr[q][4 * c4 + 2]) + bf16_hi(sr[q][4 * c4 + 2])) +
-                 (bf16_lo(sr[q][4 * c4 + 3]) + bf16_hi(sr[q][4 * c4 + 3]));
+          lsa = f2_add(lsa, f2_pack(bf16_lo(sr[q][4 * c4]), bf16_hi(sr[q][4 * c4])));
+          lsb = f2_add(lsb, f2_pack(bf16_lo(sr[q][4 * c4 + 1]), bf16_hi(sr[q][4 * c4 + 1])));
+          lsa = f2_add(lsa, f2_pack(bf16_lo(sr[q][4 * c4 + 2]), bf16_hi(sr[q][4 * c4 + 2])));
+          lsb = f2_add(lsb, f2_pack(bf16_lo(sr[q][4 * c4 + 3]), bf16_hi(sr[q][4 * c4 + 3])));
           if (DROP) {
             // dropped weights leave the PV product (l keeps them); one
             // generator call covers keys 32 q + 16 (c4 / 2) .. + 15
@@ -371,7 +379,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         tmem_st_wait();
       }
       tmem_st_wait();
-      l += ls0 + ls1;
+      {
+        float a0, a1, b0, b1;
+        f2_unpack(lsa, a0, a1);
+        f2_unpack(lsb, b0, b1);
+        l += (a0 + a1) + (b0 + b1);
+      }
       tc_fence_before();
       mbar_arrive(bar(L::B_PF + s));
       ++cnt;
