@@ -215,21 +215,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // accumulator is latency-bound on the tensor core, so independent
       // chains are issued interleaved step by step where the data allows.
       // X[128 q x 128 k] = A[128 x D] B[128 x D]^T, both K-major
+      // operand descriptors: K-major (qk) or MN-major (tt, dq B), advanced per
+      // k-step from the descriptor of the operand's first byte
+      const uint64_t dk0 = desc_sw128(sb, 16, 1024), dm0 = desc_sw128(sb, L::CHUNK, 1024);
+      auto kmaj = [&](uint32_t a) { return desc_advance(dk0, a - sb); };
+      auto mnmaj = [&](uint32_t a) { return desc_advance(dm0, a - sb); };
       auto qk_step = [&](uint32_t dst, uint32_t a, uint32_t b, int kk) {
         const uint32_t off = (kk >> 2) * L::CHUNK + (kk & 3) * 32;
-        mma_bf16_ss(dst, desc_sw128(a + off, 16, 1024), desc_sw128(b + off, 16, 1024), idSS,
-                    kk > 0);
+        mma_bf16_ss(dst, kmaj(a + off), kmaj(b + off), idSS, kk > 0);
       };
       // Y[128 k x D] += X^T[128 k x 128 q] Z[128 q x D]; X stored [q][k]
       auto tt_step = [&](uint32_t dst, uint32_t x, uint32_t z, bool acc, int kk) {
-        mma_bf16_ss(dst, desc_sw128(x + kk * 2048, L::CHUNK, 1024),
-                    desc_sw128(z + kk * 2048, L::CHUNK, 1024), idTT, (acc || kk > 0) ? 1u : 0u);
+        mma_bf16_ss(dst, mnmaj(x + kk * 2048), mnmaj(z + kk * 2048), idTT,
+                    (acc || kk > 0) ? 1u : 0u);
       };
       // dQ[128 q x D] = dS[128 q x 128 k] K[128 k x D]
       auto dq_step = [&](uint32_t dst, int kk) {
         const uint32_t aoff = (kk >> 2) * L::CHUNK + (kk & 3) * 32;
-        mma_bf16_ss(dst, desc_sw128(sb + L::DS + aoff, 16, 1024),
-                    desc_sw128(sb + L::K + kk * 2048, L::CHUNK, 1024), idDQ, kk > 0);
+        mma_bf16_ss(dst, kmaj(sb + L::DS + aoff), mnmaj(sb + L::K + kk * 2048), idDQ, kk > 0);
       };
       auto issue_qk = [&](uint32_t dst, uint32_t a, uint32_t b) {
 #pragma unroll

@@ -153,12 +153,14 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       constexpr uint32_t idSS = idesc_bf16(128, 128, false, false);  // S, dP
       constexpr uint32_t idDQ = idesc_bf16(128, D, false, true);     // dQ
       // X[128 q x 128 k] = A[128 x D] B[128 x D]^T, both K-major
+      // operand descriptors formed once and advanced per k-step
+      const uint64_t dk0 = desc_sw128(sb, 16, 1024), dm0 = desc_sw128(sb, L::CHUNK, 1024);
       auto issue_qk = [&](uint32_t dst, uint32_t a, uint32_t b) {
+        const uint64_t da = desc_advance(dk0, a - sb), db = desc_advance(dk0, b - sb);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * L::CHUNK + (kk & 3) * 32;
-          mma_bf16_ss(dst, desc_sw128(a + off, 16, 1024), desc_sw128(b + off, 16, 1024), idSS,
-                      kk > 0);
+          mma_bf16_ss(dst, desc_advance(da, off), desc_advance(db, off), idSS, kk > 0);
         }
       };
       // dQ[128 q x D] += dS[128 q x 128 k] K[128 k x D] (K is MN-major here)
@@ -166,9 +168,8 @@ __global__ void __launch_bounds__(kDqThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk) {
           const uint32_t aoff = (kk >> 2) * L::CHUNK + (kk & 3) * 32;
-          mma_bf16_ss(dst, desc_sw128(sb + L::DS + aoff, 16, 1024),
-                      desc_sw128(kaddr + kk * 2048, L::CHUNK, 1024), idDQ,
-                      (acc || kk > 0) ? 1u : 0u);
+          mma_bf16_ss(dst, desc_advance(dk0, L::DS + aoff), desc_advance(dm0, kaddr - sb + kk * 2048),
+                      idDQ, (acc || kk > 0) ? 1u : 0u);
         }
       };
       const uint32_t tS = tmem + L::T_S, tDP = tmem + L::T_DP, tDQ = tmem + L::T_DQ;

@@ -182,24 +182,27 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16(128, 128, false, false);
       constexpr uint32_t idO = idesc_bf16(128, D, false, true);
+      // descriptors are formed once per operand and advanced per k-step
+      const uint64_t dq0 = desc_sw128(sb + L::Q, 16, 1024);
+      const uint64_t dkv0 = desc_sw128(sb + L::KV, 16, 1024);  // K-major ring slot 0
+      const uint64_t dv0 = desc_sw128(sb + L::KV, L::CHUNK, 1024);  // MN-major ring slot 0
       auto issue_s = [&](int s, int kpos) {
-        const uint32_t qa = sb + L::Q + s * L::TILE;
-        const uint32_t kb = sb + L::KV + kpos * L::TILE;
+        const uint64_t qa = desc_advance(dq0, s * L::TILE);
+        const uint64_t kb = desc_advance(dkv0, kpos * L::TILE);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * L::CHUNK + (kk & 3) * 32;
-          mma_bf16_ss(tmem + s * 128, desc_sw128(qa + off, 16, 1024),
-                      desc_sw128(kb + off, 16, 1024), idS, kk > 0);
+          mma_bf16_ss(tmem + s * 128, desc_advance(qa, off), desc_advance(kb, off), idS, kk > 0);
         }
       };
       // O_s += P_s V: P_s sits in TMEM (64 columns, two bf16 per column), V is
       // MN-major in shared memory
       auto issue_pv = [&](int s, int vpos, bool acc) {
-        const uint32_t vb = sb + L::KV + vpos * L::TILE;
+        const uint64_t vb = desc_advance(dv0, vpos * L::TILE);
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
           mma_bf16_ts(tmem + 256 + s * D, tmem + L::T_P + s * L::T_PSTRIDE + kk * 8,
-                      desc_sw128(vb + kk * 2048, L::CHUNK, 1024), idO, (acc || kk > 0) ? 1u : 0u);
+                      desc_advance(vb, kk * 2048), idO, (acc || kk > 0) ? 1u : 0u);
       };
       int kt, mem, kt_n = 0, mem_n = 0;
       uint32_t idx = 0;

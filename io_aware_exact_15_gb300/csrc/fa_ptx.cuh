@@ -230,6 +230,11 @@ FA_DEV uint64_t desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
   return d;
 }
 
+// The descriptor of an operand `bytes` further on (a multiple of 16): the
+// start-address field holds addr / 16 in 14 bits, and every shared-memory
+// address of a CTA is below 2^18, so the field never carries into the next.
+FA_DEV uint64_t desc_advance(uint64_t desc, uint32_t bytes) { return desc + (bytes >> 4); }
+
 // Instruction descriptor for kind::f16 with bf16 A/B and fp32 D.
 // a_mn / b_mn select MN-major (transposed) operands.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool b_mn) {
