@@ -325,7 +325,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       const bool rescale_o = cnt > 0 && __any_sync(0xffffffffu, resc);
       const float mu = (m == -INFINITY) ? 0.f : m;
       const uint64_t sl2x2 = f2_pack(sl2, sl2), nmux2 = f2_pack(-mu, -mu);
-      uint64_t lsa = 0ull, lsb = 0ull;  // row-sum partials, fp32 x2 (0 bits = +0.0)
+      float ls0 = 0.f, ls1 = 0.f, ls2 = 0.f, ls3 = 0.f;  // row-sum partials
       PhiloxOut rw;
       // P (bf16, two per 32-bit column) overwrites the first 64 columns of
       // this tile's S, which are already in registers
@@ -349,10 +349,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           for (int j = 0; j < 4; ++j) sr[q][4 * c4 + j] = pack_bf16(e[2 * j], e[2 * j + 1]);
           // l sums the same bf16-rounded weights the PV MMA consumes, so a
           // dominant key's rounding cancels in O / l
-          lsa = f2_add(lsa, f2_pack(bf16_lo(sr[q][4 * c4]), bf16_hi(sr[q][4 * c4])));
-          lsb = f2_add(lsb, f2_pack(bf16_lo(sr[q][4 * c4 + 1]), bf16_hi(sr[q][4 * c4 + 1])));
-          lsa = f2_add(lsa, f2_pack(bf16_lo(sr[q][4 * c4 + 2]), bf16_hi(sr[q][4 * c4 + 2])));
-          lsb = f2_add(lsb, f2_pack(bf16_lo(sr[q][4 * c4 + 3]), bf16_hi(sr[q][4 * c4 + 3])));
+          acc_bf16x2(ls0, ls1, sr[q][4 * c4]);
+          acc_bf16x2(ls2, ls3, sr[q][4 * c4 + 1]);
+          acc_bf16x2(ls0, ls1, sr[q][4 * c4 + 2]);
+          acc_bf16x2(ls2, ls3, sr[q][4 * c4 + 3]);
           if (DROP) {
             // dropped weights leave the PV product (l keeps them); one
             // generator call covers keys 32 q + 16 (c4 / 2) .. + 15
@@ -382,12 +382,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         tmem_st_wait();
       }
       tmem_st_wait();
-      {
-        float a0, a1, b0, b1;
-        f2_unpack(lsa, a0, a1);
-        f2_unpack(lsb, b0, b1);
-        l += (a0 + a1) + (b0 + b1);
-      }
+      l += (ls0 + ls1) + (ls2 + ls3);
       tc_fence_before();
       mbar_arrive(bar(L::B_PF + s));
       ++cnt;

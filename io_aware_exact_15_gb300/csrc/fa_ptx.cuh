@@ -278,6 +278,15 @@ FA_DEV uint64_t f2_add(uint64_t a, uint64_t b) {
   return r;
 }
 
+// a += lo half, b += hi half of a packed bf16x2 word (each half widened to
+// fp32 exactly, then one fp32 add with round-to-nearest)
+FA_DEV void acc_bf16x2(float& a, float& b, uint32_t w) {
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+      "add.rn.f32.bf16 %0, lo, %0;\n\tadd.rn.f32.bf16 %1, hi, %1;\n\t}"
+      : "+f"(a), "+f"(b)
+      : "r"(w));
+}
+
 // max of three fp32 values in one instruction
 FA_DEV float fmax3(float a, float b, float c) {
   float r;
