@@ -408,9 +408,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           bulk_commit();
         }
       }
-      // the staging rows are this warp's dS rows: their reads must be done
-      if (lane == 0) bulk_wait_read_all();
-      __syncwarp();
+      // the staging rows are this warp's dS rows: the wait for the reads to
+      // finish comes just before the next dS store, so that it overlaps the
+      // dP wait and the dS arithmetic
       return true;
     };
     while (ok && have) {
@@ -517,6 +517,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                              f2_sub(f2_pack(d0, d1), dltx2)),
                       x0, x1);
             w[j] = pack_bf16(x0, x1);
+          }
+          if (c == 0 && g == 0) {  // the previous dQ staging in these rows has been read
+            if (lane == 0) bulk_wait_read_all();
+            __syncwarp();
           }
           st_shared_v4(dsbuf + sw128_offset(r, 4 * c + g), w[0], w[1], w[2], w[3]);
         }
