@@ -185,16 +185,42 @@ def run_gpu(args, rank, world, dist):
     bwb = nbytes - lists_bytes
 
     # device buffers of one step (the double-buffered e2e loop uses two sets)
-    def buffer_set(src=None):
-        if src is not None:
-            return types.SimpleNamespace(**vars(src))
+    # One allocation per direction: a step's inputs (q, k, v, dO and the mask
+    # or sequence offsets) and its outputs (o, lse, dq, dk, dv) are views into
+    # a single buffer, 256-byte aligned, so each moves in one copy.
+    in_specs = [(tuple(t.shape), t.dtype) for t in (qd, kd, vd, dod)]
+    if md is not None:
+        in_specs.append((tuple(md.shape), md.dtype))
+    if cud is not None:
+        in_specs.append((tuple(cud.shape), cud.dtype))
+    out_specs = [(tuple(t.shape), t.dtype) for t in (o, lse, dq, dk, dv)]
+
+    def packed(specs, device=None, pin=False):
+        sizes = [int(np.prod(shape)) * torch.empty((), dtype=dt).element_size()
+                 for shape, dt in specs]
+        offs, total = [], 0
+        for n in sizes:
+            offs.append(total)
+            total += (n + 255) // 256 * 256
+        buf = torch.empty(total, dtype=torch.uint8, device=device)
+        if pin:
+            buf = buf.pin_memory()
+        views = [buf[a:a + n].view(dt).view(shape)
+                 for (shape, dt), a, n in zip(specs, offs, sizes)]
+        return buf, views
+
+    def buffer_set():
         with torch.cuda.stream(stream):
-            bs = types.SimpleNamespace(
-                qd=torch.empty_like(qd), kd=torch.empty_like(kd), vd=torch.empty_like(vd),
-                dod=torch.empty_like(dod), md=None if md is None else torch.empty_like(md),
-                cud=None if cud is None else torch.empty_like(cud), o=torch.empty_like(o),
-                lse=torch.empty_like(lse), dq=torch.empty_like(dq), dk=torch.empty_like(dk),
-                dv=torch.empty_like(dv))
+            din, iv = packed(in_specs, device=dev)
+            dout, ov = packed(out_specs, device=dev)
+        bs = types.SimpleNamespace(din=din, dout=dout, qd=iv[0], kd=iv[1], vd=iv[2], dod=iv[3],
+                                   md=None, cud=None, o=ov[0], lse=ov[1], dq=ov[2], dk=ov[3],
+                                   dv=ov[4])
+        rest = iv[4:]
+        if md is not None:
+            bs.md = rest.pop(0)
+        if cud is not None:
+            bs.cud = rest.pop(0)
         return bs
 
     b0 = types.SimpleNamespace(qd=qd, kd=kd, vd=vd, dod=dod, md=md, cud=cud, o=o, lse=lse,
@@ -336,26 +362,24 @@ def run_gpu(args, rank, world, dist):
     value = world * fb / (ms_max * 1e-3) / 1e12
 
     # end to end through the public API with host buffers (pinned)
-    hq, hk, hv, hdo = (t.pin_memory() for t in (q, k, v, do))
-    ho = torch.empty_like(q).pin_memory()
-    hl = torch.empty(lse_shape, dtype=torch.float32).pin_memory()
-    hdq = torch.empty_like(q).pin_memory()
-    hdk, hdv = torch.empty_like(k).pin_memory(), torch.empty_like(v).pin_memory()
-    hm = torch.from_numpy(np.ascontiguousarray(mask)).pin_memory() if sparse else None
-    hcu = torch.from_numpy(cu).pin_memory() if varlen else None
-    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo))
-    d2h = sum(t.numel() * t.element_size() for t in (ho, hl, hdq, hdk, hdv))
+    hin, hiv = packed(in_specs, pin=True)
+    hout, _ = packed(out_specs, pin=True)
+    host_inputs = [q, k, v, do]
     if sparse:
-        h2d += hm.numel()
+        host_inputs.append(torch.from_numpy(np.ascontiguousarray(mask)))
     if varlen:
-        h2d += hcu.numel() * hcu.element_size()
+        host_inputs.append(torch.from_numpy(cu))
+    for dst, src in zip(hiv, host_inputs):
+        dst.copy_(src)
+    h2d = hin.numel()   # bytes copied per step (payload plus <= 255 B alignment per tensor)
+    d2h = hout.numel()
 
     # Streamed batches: step i's inputs go up on `cin`, its forward + backward
     # run on the compute stream, its outputs come down on `cout`; two buffer
     # sets let the copies of steps i+1 and i-1 overlap the compute of step i.
     # Every step's host -> device and device -> host copies are inside the
     # timed region.
-    sets = [b0, buffer_set()]
+    sets = [buffer_set(), buffer_set()]
     cin = torch.cuda.Stream(device=dev)
     cout = torch.cuda.Stream(device=dev)
     ev_in = [torch.cuda.Event() for _ in range(2)]      # inputs of set s loaded
@@ -369,12 +393,7 @@ def run_gpu(args, rank, world, dist):
         with torch.cuda.stream(cin):
             if used[sidx]:
                 cin.wait_event(ev_done[sidx])  # the set's previous inputs are consumed
-            for dst, src in ((bs.qd, hq), (bs.kd, hk), (bs.vd, hv), (bs.dod, hdo)):
-                dst.copy_(src, non_blocking=True)
-            if sparse:
-                bs.md.copy_(hm, non_blocking=True)
-            if varlen:
-                bs.cud.copy_(hcu, non_blocking=True)
+            bs.din.copy_(hin, non_blocking=True)
             ev_in[sidx].record(cin)
         stream.wait_event(ev_in[sidx])
         if used[sidx]:
@@ -383,8 +402,7 @@ def run_gpu(args, rank, world, dist):
         ev_done[sidx].record(stream)
         with torch.cuda.stream(cout):
             cout.wait_event(ev_done[sidx])
-            for dst, src in ((ho, bs.o), (hl, bs.lse), (hdq, bs.dq), (hdk, bs.dk), (hdv, bs.dv)):
-                dst.copy_(src, non_blocking=True)
+            hout.copy_(bs.dout, non_blocking=True)
             ev_out[sidx].record(cout)
         used[sidx] = True
 
@@ -401,17 +419,12 @@ def run_gpu(args, rank, world, dist):
     ems = a.elapsed_time(b) / Ke
     # the same steps one after another on one stream, for comparison
     def serial_step():
+        bs = sets[0]
         with torch.cuda.stream(stream):
-            for dst, src in ((b0.qd, hq), (b0.kd, hk), (b0.vd, hv), (b0.dod, hdo)):
-                dst.copy_(src, non_blocking=True)
-            if sparse:
-                b0.md.copy_(hm, non_blocking=True)
-            if varlen:
-                b0.cud.copy_(hcu, non_blocking=True)
-        step()
+            bs.din.copy_(hin, non_blocking=True)
+        step(bs=bs)
         with torch.cuda.stream(stream):
-            for dst, src in ((ho, b0.o), (hl, b0.lse), (hdq, b0.dq), (hdk, b0.dk), (hdv, b0.dv)):
-                dst.copy_(src, non_blocking=True)
+            hout.copy_(bs.dout, non_blocking=True)
     serial_step()
     torch.cuda.synchronize(dev)
     a2, b2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -428,9 +441,10 @@ def run_gpu(args, rank, world, dist):
     e2e = {"value": round(world * fb / (ems * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
            "ms_per_step": round(ems, 4), "h2d_bytes_per_step": int(h2d),
            "d2h_bytes_per_step": int(d2h),
-           "path": "per step: pinned host -> device copies of the inputs, forward + backward "
-                   "via the C ABI, device -> host copies of o, lse, dq, dk, dv; streamed with "
-                   "two device buffer sets so the copies of neighbouring steps overlap compute",
+           "path": "per step: one pinned host -> device copy of the packed inputs (q, k, v, dO), "
+                   "forward + backward via the C ABI, one device -> host copy of the packed "
+                   "outputs (o, lse, dq, dk, dv); streamed with two device buffer sets so the "
+                   "copies of neighbouring steps overlap compute",
            "serial_ms_per_step": round(ems_serial, 4)}
 
     src_hash = kernel_source_hash(["fa_bwd.cu", "fa_ptx.cuh", "fa_sched.cuh"])

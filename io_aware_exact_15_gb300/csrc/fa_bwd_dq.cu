@@ -231,6 +231,8 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     const float dlt_c = p.delta[row_idx];
     const bool live = qrow < N && lse_c != -INFINITY;
     const float lse2 = live ? lse_c * kLog2e : 0.f;
+    const uint64_t sl2x2 = f2_pack(sl2, sl2), nlse2x2 = f2_pack(-lse2, -lse2);
+    const uint64_t dltx2 = f2_pack(dlt_c, dlt_c);
     bool ok = true;
     uint32_t n = 0;
     int kt, mem;
@@ -253,8 +255,14 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       uint32_t pw[32];  // pw[i]: keys 2i, 2i+1 of this thread's 64 columns
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
-        float a = ex2(fmaf(__uint_as_float(sv[i >> 4][(2 * i) & 31]), sl2, -lse2));
-        float b = ex2(fmaf(__uint_as_float(sv[i >> 4][(2 * i + 1) & 31]), sl2, -lse2));
+        // exponent arguments of two keys in one fp32 x2 FMA
+        float a, b;
+        f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[i >> 4][(2 * i) & 31]),
+                                 __uint_as_float(sv[i >> 4][(2 * i + 1) & 31])),
+                         sl2x2, nlse2x2),
+                  a, b);
+        a = ex2(a);
+        b = ex2(b);
         if (need_mask) {
           if (2 * i >= lim) a = 0.f;
           if (2 * i + 1 >= lim) b = 0.f;
@@ -279,8 +287,13 @@ __global__ void __launch_bounds__(kDqThreads, 1)
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             const uint32_t pp = pw[16 * c + 4 * g + j];
-            const float x0 = bf16_lo(pp) * (__uint_as_float(dp[8 * g + 2 * j]) - dlt_c);
-            const float x1 = bf16_hi(pp) * (__uint_as_float(dp[8 * g + 2 * j + 1]) - dlt_c);
+            // P o (dP - D) for two keys in fp32 x2
+            float x0, x1;
+            f2_unpack(f2_mul(f2_pack(bf16_lo(pp), bf16_hi(pp)),
+                             f2_sub(f2_pack(__uint_as_float(dp[8 * g + 2 * j]),
+                                            __uint_as_float(dp[8 * g + 2 * j + 1])),
+                                    dltx2)),
+                      x0, x1);
             w[j] = pack_bf16(x0, x1);
           }
           st_shared_v4(dsbuf + sw128_offset(r, 4 * c + g), w[0], w[1], w[2], w[3]);
