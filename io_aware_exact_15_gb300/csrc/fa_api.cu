@@ -306,6 +306,10 @@ fa_status make_dropout(float p_drop, unsigned long long seed, unsigned offset,
   out->seed_lo = static_cast<uint32_t>(seed);
   out->seed_hi = static_cast<uint32_t>(seed >> 32);
   out->offset = offset;
+  for (uint32_t r = 0; r < 10; ++r) {
+    out->rk[2 * r] = out->seed_lo + r * 0x9E3779B9u;
+    out->rk[2 * r + 1] = out->seed_hi + r * 0xBB67AE85u;
+  }
   return FA_OK;
 }
 

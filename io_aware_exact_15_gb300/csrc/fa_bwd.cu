@@ -357,7 +357,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const float sl2 = p.scale * kLog2e;
     const int kbase = kt * kTile;
     const int kcol0 = kbase + 64 * half;  // first key of this thread's columns
-    const DropoutRng rng{p.drop.seed_lo, p.drop.seed_hi, p.drop.offset, p.drop.t * 0x01010101u};
+    const DropoutRng rng{p.drop.rk, p.drop.offset, p.drop.t * 0x01010101u};
     bool ok = true;
     uint32_t n = 0;
     int qt = 0, qt_prev = 0, g = 0, g_prev = 0;

@@ -278,7 +278,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const uint32_t tO = tmem + lane_off + 256 + s * D;
     const uint32_t tP = tmem + lane_off + L::T_P + s * L::T_PSTRIDE;
     const float sl2 = p.scale * kLog2e;
-    DropoutRng rng{p.drop.seed_lo, p.drop.seed_hi, p.drop.offset, p.drop.t * 0x01010101u};
+    const DropoutRng rng{p.drop.rk, p.drop.offset, p.drop.t * 0x01010101u};
     float m = -INFINITY, l = 0.f;
     int cnt = 0;
     bool ok = true;

@@ -48,6 +48,9 @@ struct DropoutParams {
   uint32_t seed_lo = 0, seed_hi = 0, offset = 0;
   uint32_t t = 0;
   float scale = 1.f;
+  // Philox key of round r: (seed_lo + r * 0x9E3779B9, seed_hi + r * 0xBB67AE85),
+  // formed on the host; kernel parameters, read by the rounds as constants
+  uint32_t rk[20] = {};
 };
 
 struct FwdParams {

@@ -17,8 +17,11 @@ struct PhiloxOut {
   uint32_t w[4];
 };
 
-FA_DEV PhiloxOut philox4x32_10(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3, uint32_t k0,
-                               uint32_t k1) {
+// Ten rounds on the counter; rk[2 r], rk[2 r + 1] are the key of round r,
+// i.e. (k0 + r * 0x9E3779B9, k1 + r * 0xBB67AE85) (the Weyl sequence that
+// bumps the key between rounds), formed once on the host.
+FA_DEV PhiloxOut philox4x32_10(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3,
+                               const uint32_t (&rk)[20]) {
 #pragma unroll
   for (int round = 0; round < 10; ++round) {
     // the two 32 x 32 -> 64-bit products of the round
@@ -26,13 +29,10 @@ FA_DEV PhiloxOut philox4x32_10(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c
     const uint64_t b = static_cast<uint64_t>(0xCD9E8D57u) * c2;
     const uint32_t a_hi = static_cast<uint32_t>(a >> 32), a_lo = static_cast<uint32_t>(a);
     const uint32_t b_hi = static_cast<uint32_t>(b >> 32), b_lo = static_cast<uint32_t>(b);
-    c0 = b_hi ^ c1 ^ k0;
+    c0 = b_hi ^ c1 ^ rk[2 * round];
     c1 = b_lo;
-    c2 = a_hi ^ c3 ^ k1;
+    c2 = a_hi ^ c3 ^ rk[2 * round + 1];
     c3 = a_lo;
-    // Weyl sequence on the key between rounds
-    k0 += 0x9E3779B9u;
-    k1 += 0xBB67AE85u;
   }
   PhiloxOut r;
   r.w[0] = c0;
@@ -42,16 +42,17 @@ FA_DEV PhiloxOut philox4x32_10(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c
   return r;
 }
 
-// Dropout stream of one call: key words, offset and threshold.
+// Dropout stream of one call: round keys, offset and threshold.
 struct DropoutRng {
-  uint32_t k0, k1, offset, t4;  // t4: the threshold t in every byte
+  const uint32_t (&rk)[20];
+  uint32_t offset, t4;  // t4: the threshold t in every byte
 
   // 0xFF in byte k of the result iff key 4 * w + k of the 16-key group is kept
   FA_DEV static uint32_t keep_bytes(uint32_t word, uint32_t t4) { return __vcmpgeu4(word, t4); }
 
   // the four words of the 16-key group starting at key 16 * grp of row i
   FA_DEV PhiloxOut group(uint32_t grp, uint32_t i, uint32_t bhc) const {
-    return philox4x32_10(grp, i, bhc, offset, k0, k1);
+    return philox4x32_10(grp, i, bhc, offset, rk);
   }
 };
 
