@@ -20,7 +20,8 @@
 //               (ex2 with the scale folded in) and dS from dP and D, both
 //               written to shared memory as bf16 for the MMAs that read them;
 //               between the two, the previous tile's dQ is read out of TMEM,
-//               staged in the (then idle) dS buffer and added into the fp32
+//               staged (d = 64: in a buffer of its own; d = 128: in the
+//               then idle dS buffer) and added into the fp32
 //               dQ accumulator by TMA reduce-add while the tensor core runs
 //               the next MMAs
 //   warps 2-3   idle
@@ -53,7 +54,12 @@ struct BwdSmem {
   static constexpr int DOR = QR + NQ * TILE;
   static constexpr int P = DOR + NDO * TILE;
   static constexpr int DS = P + PT;
-  static constexpr int BAR = DS + PT;
+  // d = 64 leaves room for a dQ staging buffer of its own (128 x 64 fp32), so
+  // that the wait for the TMA to read it falls a whole step after the reduce
+  // is issued; d = 128 stages in the dS buffer
+  static constexpr bool OWN_STG = (D == 64);
+  static constexpr int STG = DS + PT;
+  static constexpr int BAR = STG + (OWN_STG ? 2 * CHUNK : 0);
   static constexpr int B_KV = 0, B_QF = 1, B_QE = B_QF + NQ, B_DOF = B_QE + NQ,
                        B_DOE = B_DOF + NDO, B_SF = B_DOE + NDO, B_DPF = B_SF + 1,
                        B_PR = B_DPF + 1, B_DSR = B_PR + 1, B_DQF = B_DSR + 1, B_DQE = B_DQF + 1,
@@ -384,15 +390,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tc_fence_before();
       mbar_arrive(bar(L::B_DQE));
       // Reduce-add through the TMA engine: the warp stages its 32 rows x 32
-      // columns (4 KB, 128-byte swizzle) in its own rows of the dS buffer,
-      // which no MMA reads between dQ's completion and the next dS, and lane 0
-      // adds the box into the fp32 accumulator (rows past the tensor are
-      // clipped; rows past this sequence but inside the tensor receive exact
-      // zeros, since their P and dS rows are 0).
-      const uint32_t stage = dsbuf + q4 * 4096;
+      // columns (4 KB, 128-byte swizzle), for d = 64 in its own staging
+      // buffer, for d = 128 in its own rows of the dS buffer, which no MMA
+      // reads between dQ's completion and the next dS, and lane 0 adds the
+      // box into the fp32 accumulator (rows past the tensor are clipped; rows
+      // past this sequence but inside the tensor receive exact zeros, since
+      // their P and dS rows are 0).
+      const uint32_t stage =
+          (L::OWN_STG ? sb + L::STG + half * L::CHUNK : dsbuf) + q4 * 4096;
 #pragma unroll
       for (int c = 0; c < D / 64; ++c) {
-        if (c > 0) {
+        if (c > 0 || L::OWN_STG) {  // the previous box has been read
           if (lane == 0) bulk_wait_read_all();
           __syncwarp();
         }
@@ -408,9 +416,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           bulk_commit();
         }
       }
-      // the staging rows are this warp's dS rows: the wait for the reads to
-      // finish comes just before the next dS store, so that it overlaps the
-      // dP wait and the dS arithmetic
+      // d = 128: the staging rows are this warp's dS rows: the wait for the
+      // reads to finish comes just before the next dS store, so that it
+      // overlaps the dP wait and the dS arithmetic
       return true;
     };
     while (ok && have) {
@@ -518,7 +526,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                       x0, x1);
             w[j] = pack_bf16(x0, x1);
           }
-          if (c == 0 && g == 0) {  // the previous dQ staging in these rows has been read
+          if (!L::OWN_STG && c == 0 && g == 0) {  // the previous dQ staging in these rows has been read
             if (lane == 0) bulk_wait_read_all();
             __syncwarp();
           }
