@@ -75,6 +75,49 @@ struct BwdSmem {
 constexpr int kBwdThreads = 384;
 constexpr float kLog2e = 1.4426950408889634f;
 
+// Geometry of one work unit: one key/value head x one key tile.
+struct BwdUnit {
+  int kt;       // key tile
+  int N;        // sequence length
+  int row0;     // first row of the sequence in its slice
+  int zkv;      // key/value slice
+  int bq0;      // first query slice of the group
+  int bh_base;  // b * H when query slices are heads (variable-length batch)
+  int nT;       // tiles of the sequence
+};
+
+// Unit u -> its geometry.  False when the key tile lies past the end of its
+// (variable-length) sequence; every role of the CTA skips such a unit alike.
+template <bool GQA>
+FA_DEV bool bwd_unit(int u, const BwdParams& p, int Hkv, int G, int ntmax, bool varlen,
+                     BwdUnit& w) {
+  int bkv;
+  bwd_cta_coords(u, p.B * Hkv, ntmax, p.causal != 0, bkv, w.kt);
+  w.N = p.N;
+  w.row0 = 0;
+  w.zkv = bkv;
+  w.bq0 = GQA ? (bkv / Hkv) * p.H + (bkv % Hkv) * G : bkv;
+  w.bh_base = 0;
+  if (varlen) {
+    // variable-length batch: slices are heads, sequences are row ranges
+    // (indices clamped to [0, total], so bad offsets cannot write outside)
+    const int b = bkv / Hkv;
+    const int a = min(max(p.cu_seqlens[b], 0), p.total);
+    const int e = min(max(p.cu_seqlens[b + 1], a), p.total);
+    w.row0 = a;
+    w.N = min(e - a, p.N);
+    w.zkv = bkv % Hkv;
+    w.bq0 = w.zkv * G;
+    w.bh_base = b * p.H;
+  }
+  w.nT = (w.N + kTile - 1) / kTile;
+  return w.kt * kTile < w.N;
+}
+
+// Persistent: CTA c takes the units c, c + gridDim.x, ... in turn.  Per
+// unit, K_j and V_j of the next unit load while the previous unit's last dQ
+// drains and its dV, dK leave TMEM, and the Q / dO rings and every step
+// barrier run on across units.
 // DQ = false: no dQ product and no reduce-adds (dQ comes from the query-tile
 // pass of the deterministic backward)
 template <int D, int KIND, bool DQ = true>
@@ -96,35 +139,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   constexpr bool GQA = KIND != kPlain;
   const int ntmax = (p.N + kTile - 1) / kTile;
-  // one CTA = one key/value head x one key tile; with grouped K/V it walks
+  // a unit = one key/value head x one key tile; with grouped K/V it walks
   // the query tiles of every query head of its group (G = H / Hkv)
   // (the plain instantiation carries no group arithmetic)
   const int Hkv = GQA ? p.Hkv : p.H;
   const int G = GQA ? p.H / p.Hkv : 1;
-  int bkv, kt;
-  bwd_cta_coords(blockIdx.x, p.B * Hkv, ntmax, p.causal != 0, bkv, kt);
-  // Sequence geometry: length N, first row row0 of the sequence in its
-  // slice, the K/V slice zkv and the first query slice bq0 of the group.
+  const int nunits = p.B * Hkv * ntmax;
   constexpr bool DROP = KIND == kGeneralDropout;
-  int N = p.N, row0 = 0, zkv = bkv;
-  int bq0 = GQA ? (bkv / Hkv) * p.H + (bkv % Hkv) * G : bkv;
-  int bh_base = 0;  // b * H when query slices are heads (variable-length batch)
   const bool varlen = KIND >= kGeneral && p.cu_seqlens != nullptr;
-  if (varlen) {
-    // variable-length batch: slices are heads, sequences are row ranges
-    // (indices clamped to [0, total], so bad offsets cannot write outside)
-    const int b = bkv / Hkv;
-    const int a = min(max(p.cu_seqlens[b], 0), p.total);
-    const int e = min(max(p.cu_seqlens[b + 1], a), p.total);
-    row0 = a;
-    N = min(e - a, p.N);
-    zkv = bkv % Hkv;
-    bq0 = zkv * G;
-    bh_base = b * p.H;
-    if (kt * kTile >= N) return;  // no key of this tile here (CTA-uniform)
-  }
   const size_t slice_rows = varlen ? static_cast<size_t>(p.total) : static_cast<size_t>(p.N);
-  const int nT = (N + kTile - 1) / kTile;
+  auto unit_at = [&](int u, BwdUnit& w) {
+    return bwd_unit<GQA>(u, p, Hkv, G, ntmax, varlen, w);
+  };
 
   if (threadIdx.x == 0) {
     mbar_init(bar(L::B_KV), 1);
@@ -156,8 +182,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const WaitCtl wc{abort_flag, p.err, p.wait_ns};
 
-  typename std::conditional<GQA, BwdGroupSchedule, BwdSingleSchedule>::type sch;
-  sch.init(kt, nT, p.causal != 0, p.lists, bq0 % p.H, G);
+  using Sched = typename std::conditional<GQA, BwdGroupSchedule, BwdSingleSchedule>::type;
 
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer
@@ -167,41 +192,62 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       prefetch_tmap(&tv);
       prefetch_tmap(&tdo);
       prefetch_tmap(&tdq);
-      mbar_arrive_expect_tx(bar(L::B_KV), 2 * L::TILE);
-#pragma unroll
-      for (int c = 0; c < L::CH; ++c) {
-        tma_load_3d(sb + L::K + c * L::CHUNK, &tk, bar(L::B_KV), 64 * c, row0 + kt * kTile, zkv);
-        tma_load_3d(sb + L::V + c * L::CHUNK, &tv, bar(L::B_KV), 64 * c, row0 + kt * kTile, zkv);
-      }
-      uint32_t nq = 0, nd = 0;  // Q / dO copies issued
+      uint32_t nq = 0, nd = 0, nkv = 0;  // Q / dO / K-V copies issued
       bool ok = true;
-      int qt, g;
-      while (ok && sch.next(qt, g, p.lists)) {
-        const int qpos = nq % L::NQ, dpos = nd % L::NDO;
-        const uint32_t qround = nq / L::NQ, dround = nd / L::NDO;
-        if (qround > 0 && !wait_bar(bar(L::B_QE + qpos), (qround - 1) & 1, wc)) {
-          ok = false;
-          break;
-        }
-        mbar_arrive_expect_tx(bar(L::B_QF + qpos), L::TILE);
+      BwdUnit un;
+      // K_j, V_j of the current unit once every product of the previous unit
+      // is done (that unit's final commit also follows its own K/V arrival)
+      auto load_kv = [&]() -> bool {
+        if (nkv > 0 && !wait_bar(bar(L::B_FIN), (nkv - 1) & 1, wc)) return false;
+        mbar_arrive_expect_tx(bar(L::B_KV), 2 * L::TILE);
 #pragma unroll
-        for (int c = 0; c < L::CH; ++c)
-          tma_load_3d(sb + L::QR + qpos * L::TILE + c * L::CHUNK, &tq, bar(L::B_QF + qpos), 64 * c,
-                      row0 + qt * kTile, bq0 + g);
-        ++nq;
-        if (dround > 0 && !wait_bar(bar(L::B_DOE + dpos), (dround - 1) & 1, wc)) {
-          ok = false;
-          break;
+        for (int c = 0; c < L::CH; ++c) {
+          tma_load_3d(sb + L::K + c * L::CHUNK, &tk, bar(L::B_KV), 64 * c,
+                      un.row0 + un.kt * kTile, un.zkv);
+          tma_load_3d(sb + L::V + c * L::CHUNK, &tv, bar(L::B_KV), 64 * c,
+                      un.row0 + un.kt * kTile, un.zkv);
         }
-        mbar_arrive_expect_tx(bar(L::B_DOF + dpos), L::TILE);
+        ++nkv;
+        return true;
+      };
+      for (int u = blockIdx.x; ok && u < nunits; u += gridDim.x) {
+        if (!unit_at(u, un)) continue;
+        Sched sch;
+        sch.init(un.kt, un.nT, p.causal != 0, p.lists, un.bq0 % p.H, G);
+        bool kv = false;  // the unit's first Q / dO copies go out before its K/V
+        int qt, g;
+        while (ok && sch.next(qt, g, p.lists)) {
+          const int qpos = nq % L::NQ, dpos = nd % L::NDO;
+          const uint32_t qround = nq / L::NQ, dround = nd / L::NDO;
+          if (qround > 0 && !wait_bar(bar(L::B_QE + qpos), (qround - 1) & 1, wc)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(bar(L::B_QF + qpos), L::TILE);
 #pragma unroll
-        for (int c = 0; c < L::CH; ++c)
-          tma_load_3d(sb + L::DOR + dpos * L::TILE + c * L::CHUNK, &tdo, bar(L::B_DOF + dpos),
-                      64 * c, row0 + qt * kTile, bq0 + g);
-        ++nd;
+          for (int c = 0; c < L::CH; ++c)
+            tma_load_3d(sb + L::QR + qpos * L::TILE + c * L::CHUNK, &tq, bar(L::B_QF + qpos), 64 * c,
+                        un.row0 + qt * kTile, un.bq0 + g);
+          ++nq;
+          if (dround > 0 && !wait_bar(bar(L::B_DOE + dpos), (dround - 1) & 1, wc)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(bar(L::B_DOF + dpos), L::TILE);
+#pragma unroll
+          for (int c = 0; c < L::CH; ++c)
+            tma_load_3d(sb + L::DOR + dpos * L::TILE + c * L::CHUNK, &tdo, bar(L::B_DOF + dpos),
+                        64 * c, un.row0 + qt * kTile, un.bq0 + g);
+          ++nd;
+          if (!kv) {
+            kv = true;
+            if (!(ok = load_kv())) break;
+          }
+        }
+        if (ok && !kv) ok = load_kv();
       }
       // let copies still in flight land before the CTA can exit
-      drain_bar(bar(L::B_KV), 0, p.wait_ns);
+      if (nkv > 0) drain_bar(bar(L::B_KV), (nkv - 1) & 1, p.wait_ns);
       if (!ok) {
         const uint32_t fq = nq > static_cast<uint32_t>(L::NQ) ? nq - L::NQ : 0;
         for (uint32_t j = fq; j < nq; ++j)
@@ -254,94 +300,109 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       };
       const uint32_t tS = tmem + L::T_S, tDP = tmem + L::T_DP, tDV = tmem + L::T_DV,
                      tDK = tmem + L::T_DK, tDQ = tmem + L::T_DQ;
-      int qt, qt_n, g_unused;
-      bool ok = wait_bar(bar(L::B_KV), 0, wc);
-      bool have = sch.next(qt, g_unused, p.lists);
-      uint32_t n = 0;
-      if (ok && have) {
-        ok = wait_bar(bar(L::B_QF + 0), 0, wc);
-        if (ok) {
-          tc_fence_after();
-          issue_qk(tS, sb + L::QR, sb + L::K);
-          mma_commit(bar(L::B_SF));
-          ok = wait_bar(bar(L::B_DOF + 0), 0, wc);
-        }
-        if (ok) {
-          tc_fence_after();
-          issue_qk(tDP, sb + L::DOR, sb + L::V);
-          mma_commit(bar(L::B_DPF));
-        }
-      }
-      while (ok && have) {
-        const bool have_n = sch.next(qt_n, g_unused, p.lists);
-        const uint32_t qpos = n % L::NQ, dpos = n % L::NDO;
-        const uint32_t n1 = n + 1;
-        // dV += P^T dO_i once P is in shared memory, interleaved with the
-        // next S when its Q tile is already in (the S columns were read)
-        if (!(ok = wait_bar(bar(L::B_PR), n & 1, wc))) break;
-        tc_fence_after();
-        const uint32_t qn = sb + L::QR + (n1 % L::NQ) * L::TILE;
-        const uint32_t dov = sb + L::DOR + dpos * L::TILE;
-        if (have_n && mbar_try(bar(L::B_QF + n1 % L::NQ), (n1 / L::NQ) & 1)) {
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk) {
-            tt_step(tDV, sb + L::P, dov, n > 0, kk);
-            if (kk < D / 16) qk_step(tS, qn, sb + L::K, kk);
-          }
-          mma_commit(bar(L::B_DOE + dpos));
-          mma_commit(bar(L::B_SF));
-        } else {
-          issue_tt(tDV, sb + L::P, dov, n > 0);
-          mma_commit(bar(L::B_DOE + dpos));
-          if (have_n) {
-            if (!(ok = wait_bar(bar(L::B_QF + n1 % L::NQ), (n1 / L::NQ) & 1, wc))) break;
+      uint32_t n = 0, ku = 0;  // steps and units so far
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < nunits; u += gridDim.x) {
+        BwdUnit un;
+        if (!unit_at(u, un)) continue;
+        Sched sch;
+        sch.init(un.kt, un.nT, p.causal != 0, p.lists, un.bq0 % p.H, G);
+        int qt, qt_n, g_unused;
+        ok = wait_bar(bar(L::B_KV), ku & 1, wc);
+        bool have = ok && sch.next(qt, g_unused, p.lists);
+        uint32_t nu = 0;  // steps of this unit
+        if (ok && have) {
+          ok = wait_bar(bar(L::B_QF + n % L::NQ), (n / L::NQ) & 1, wc);
+          if (ok) {
             tc_fence_after();
-            issue_qk(tS, qn, sb + L::K);
+            issue_qk(tS, sb + L::QR + (n % L::NQ) * L::TILE, sb + L::K);
             mma_commit(bar(L::B_SF));
+            // d = 128: the previous unit's last dQ shares the dP columns
+            if (DQ && D != 64 && n > 0) ok = wait_bar(bar(L::B_DQE), (n - 1) & 1, wc);
           }
-        }
-        // dK += dS^T Q_i and dQ_i = dS K once dS is in shared memory,
-        // interleaved when the dQ columns are free
-        if (!(ok = wait_bar(bar(L::B_DSR), n & 1, wc))) break;
-        tc_fence_after();
-        const uint32_t qv = sb + L::QR + qpos * L::TILE;
-        if (!DQ) {
-          issue_tt(tDK, sb + L::DS, qv, n > 0);
-          mma_commit(bar(L::B_QE + qpos));
-        } else if (D != 64 || n == 0 || mbar_try(bar(L::B_DQE), (n - 1) & 1)) {
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk) {
-            tt_step(tDK, sb + L::DS, qv, n > 0, kk);
-            dq_step(tDQ, kk);
-          }
-          mma_commit(bar(L::B_QE + qpos));
-          mma_commit(bar(L::B_DQF));
-        } else {
-          issue_tt(tDK, sb + L::DS, qv, n > 0);
-          mma_commit(bar(L::B_QE + qpos));
-          if (!(ok = wait_bar(bar(L::B_DQE), (n - 1) & 1, wc))) break;
-          tc_fence_after();
-          issue_dq(tDQ);
-          mma_commit(bar(L::B_DQF));
-        }
-        if (have_n) {
-          if (DQ && D != 64) {  // dQ_i shares the dP columns: wait until it is read out
-            if (!(ok = wait_bar(bar(L::B_DQE), n & 1, wc))) break;
+          if (ok) ok = wait_bar(bar(L::B_DOF + n % L::NDO), (n / L::NDO) & 1, wc);
+          if (ok) {
             tc_fence_after();
+            issue_qk(tDP, sb + L::DOR + (n % L::NDO) * L::TILE, sb + L::V);
+            mma_commit(bar(L::B_DPF));
           }
-          if (!(ok = wait_bar(bar(L::B_DOF + n1 % L::NDO), (n1 / L::NDO) & 1, wc))) break;
-          tc_fence_after();
-          issue_qk(tDP, sb + L::DOR + (n1 % L::NDO) * L::TILE, sb + L::V);
-          mma_commit(bar(L::B_DPF));
         }
-        qt = qt_n;
-        have = have_n;
-        n = n1;
+        while (ok && have) {
+          const bool have_n = sch.next(qt_n, g_unused, p.lists);
+          const uint32_t qpos = n % L::NQ, dpos = n % L::NDO;
+          const uint32_t n1 = n + 1;
+          // dV += P^T dO_i once P is in shared memory, interleaved with the
+          // next S when its Q tile is already in (the S columns were read)
+          if (!(ok = wait_bar(bar(L::B_PR), n & 1, wc))) break;
+          tc_fence_after();
+          const uint32_t qn = sb + L::QR + (n1 % L::NQ) * L::TILE;
+          const uint32_t dov = sb + L::DOR + dpos * L::TILE;
+          if (have_n && mbar_try(bar(L::B_QF + n1 % L::NQ), (n1 / L::NQ) & 1)) {
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < kTile / 16; ++kk) {
+              tt_step(tDV, sb + L::P, dov, nu > 0, kk);
+              if (kk < D / 16) qk_step(tS, qn, sb + L::K, kk);
+            }
+            mma_commit(bar(L::B_DOE + dpos));
+            mma_commit(bar(L::B_SF));
+          } else {
+            issue_tt(tDV, sb + L::P, dov, nu > 0);
+            mma_commit(bar(L::B_DOE + dpos));
+            if (have_n) {
+              if (!(ok = wait_bar(bar(L::B_QF + n1 % L::NQ), (n1 / L::NQ) & 1, wc))) break;
+              tc_fence_after();
+              issue_qk(tS, qn, sb + L::K);
+              mma_commit(bar(L::B_SF));
+            }
+          }
+          // dK += dS^T Q_i and dQ_i = dS K once dS is in shared memory,
+          // interleaved when the dQ columns are free
+          if (!(ok = wait_bar(bar(L::B_DSR), n & 1, wc))) break;
+          tc_fence_after();
+          const uint32_t qv = sb + L::QR + qpos * L::TILE;
+          if (!DQ) {
+            issue_tt(tDK, sb + L::DS, qv, nu > 0);
+            mma_commit(bar(L::B_QE + qpos));
+          } else if (D != 64 || n == 0 || mbar_try(bar(L::B_DQE), (n - 1) & 1)) {
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < kTile / 16; ++kk) {
+              tt_step(tDK, sb + L::DS, qv, nu > 0, kk);
+              dq_step(tDQ, kk);
+            }
+            mma_commit(bar(L::B_QE + qpos));
+            mma_commit(bar(L::B_DQF));
+          } else {
+            issue_tt(tDK, sb + L::DS, qv, nu > 0);
+            mma_commit(bar(L::B_QE + qpos));
+            if (!(ok = wait_bar(bar(L::B_DQE), (n - 1) & 1, wc))) break;
+            tc_fence_after();
+            issue_dq(tDQ);
+            mma_commit(bar(L::B_DQF));
+          }
+          if (have_n) {
+            if (DQ && D != 64) {  // dQ_i shares the dP columns: wait until it is read out
+              if (!(ok = wait_bar(bar(L::B_DQE), n & 1, wc))) break;
+              tc_fence_after();
+            }
+            if (!(ok = wait_bar(bar(L::B_DOF + n1 % L::NDO), (n1 / L::NDO) & 1, wc))) break;
+            tc_fence_after();
+            issue_qk(tDP, sb + L::DOR + (n1 % L::NDO) * L::TILE, sb + L::V);
+            mma_commit(bar(L::B_DPF));
+          }
+          qt = qt_n;
+          have = have_n;
+          n = n1;
+          ++nu;
+        }
+        // every product of the unit issued: dV_j, dK_j complete and K_j, V_j
+        // free once this lands (also committed on a failed wait, so that the
+        // phase count stays that of the other roles)
+        mma_commit(bar(L::B_FIN));
+        ++ku;
       }
-      mma_commit(bar(L::B_FIN));
-      drain_bar(bar(L::B_FIN), 0, p.wait_ns);
+      if (ku > 0) drain_bar(bar(L::B_FIN), (ku - 1) & 1, p.wait_ns);
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------ P, dS, dQ warps
@@ -361,21 +422,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t pbuf = sb + L::P + half * L::CHUNK;
     const uint32_t dsbuf = sb + L::DS + half * L::CHUNK;
     const float sl2 = p.scale * kLog2e;
-    const int kbase = kt * kTile;
-    const int kcol0 = kbase + 64 * half;  // first key of this thread's columns
     const DropoutRng rng{p.drop.rk, p.drop.offset, p.drop.t * 0x01010101u};
     bool ok = true;
-    uint32_t n = 0;
-    int qt = 0, qt_prev = 0, g = 0, g_prev = 0;
-    bool have = sch.next(qt, g, p.lists);
+    uint32_t n = 0, ku = 0;  // steps and units so far
+    BwdUnit un{};
+    int kbase = 0, kcol0 = 0;  // first key of the tile / of this thread's columns
     auto load_stats = [&](int t, int gg, float& l_, float& d_) {
       const int row = t * kTile + r;
-      const size_t idx = static_cast<size_t>(bq0 + gg) * slice_rows + row0 + (row < N ? row : 0);
+      const size_t idx =
+          static_cast<size_t>(un.bq0 + gg) * slice_rows + un.row0 + (row < un.N ? row : 0);
       l_ = p.lse[idx];
       d_ = p.delta[idx];
     };
-    float lse_c = 0.f, dlt_c = 0.f;
-    if (have) load_stats(qt, g, lse_c, dlt_c);
     // dQ of query tile t (step m): TMEM -> registers, release the columns,
     // then add this thread's D/2 columns into the fp32 accumulator
     auto drain_dq = [&](uint32_t m, int t, int gg) -> bool {
@@ -411,8 +469,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         fence_async_smem();
         __syncwarp();
         if (lane == 0) {
-          tma_reduce_add_3d(&tdq, stage, (D / 2) * half + 32 * c, row0 + t * kTile + 32 * q4,
-                            bq0 + gg);
+          tma_reduce_add_3d(&tdq, stage, (D / 2) * half + 32 * c,
+                            un.row0 + t * kTile + 32 * q4, un.bq0 + gg);
           bulk_commit();
         }
       }
@@ -421,169 +479,187 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // overlaps the dP wait and the dS arithmetic
       return true;
     };
-    while (ok && have) {
-      int qt_n = 0, g_n = 0;
-      const bool have_n = sch.next(qt_n, g_n, p.lists);
-      float lse_n = 0.f, dlt_n = 0.f;
-      if (have_n) load_stats(qt_n, g_n, lse_n, dlt_n);  // prefetch the next tile's statistics
-      const int qrow = qt * kTile + r;
-      const bool live = qrow < N && lse_c != -INFINITY;
-      const float lse2 = live ? lse_c * kLog2e : 0.f;
-      // P = exp2(S * scale * log2e - lse * log2e); masked entries 0
-      ok = __all_sync(0xffffffffu, wait_bar(bar(L::B_SF), n & 1, wc));
-      if (!ok) break;
-      tc_fence_after();
-      uint32_t sv[2][32];
-      tmem_ld32(tS, sv[0]);
-      tmem_ld32(tS + 32, sv[1]);
-      tmem_ld_wait();
-      reg_fence(sv[0]);
-      reg_fence(sv[1]);
-      const bool need_mask = (kcol0 + 64 > N) || (p.causal && kcol0 + 63 > qt * kTile);
-      // keys kcol0 + i with i >= lim are masked (past N, or after this row
-      // when causal)
-      int lim = N - kcol0;
-      if (p.causal && qrow - kcol0 + 1 < lim) lim = qrow - kcol0 + 1;
-      uint32_t pw[32];  // pw[i]: keys 2i, 2i+1 of this thread's 64 columns
-      const uint64_t sl2x2 = f2_pack(sl2, sl2), nlse2x2 = f2_pack(-lse2, -lse2);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        // scale * S * log2 e - lse * log2 e for two keys in one fp32 x2 FMA
-        float a, b;
-        f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[i >> 4][(2 * i) & 31]),
-                                 __uint_as_float(sv[i >> 4][(2 * i + 1) & 31])),
-                         sl2x2, nlse2x2),
-                  a, b);
-        a = ex2(a);
-        b = ex2(b);
-        if (need_mask) {
-          if (2 * i >= lim) a = 0.f;
-          if (2 * i + 1 >= lim) b = 0.f;
-        }
-        pw[i] = live ? pack_bf16(a, b) : 0u;
-      }
-      // keep bits of this thread's 64 keys (bit k of kb[c]: key 32 c + k)
-      uint32_t kb[2] = {0u, 0u};
-      if (DROP) {
-        // the dV product takes the dropped weights z * P; dS needs P and z
-#pragma unroll
-        for (int g4 = 0; g4 < 4; ++g4) {
-          const PhiloxOut rw = rng.group((kcol0 >> 4) + g4, qrow, bh_base + bq0 + g);
-          uint32_t mk[4];
-#pragma unroll
-          for (int w = 0; w < 4; ++w) mk[w] = DropoutRng::keep_bytes(rw.w[w], rng.t4);
-#pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            const uint32_t* pp = &pw[8 * g4 + 4 * hh];
-            st_shared_v4(pbuf + sw128_offset(r, 2 * g4 + hh), pp[0] & pair_mask(mk[2 * hh], 0),
-                         pp[1] & pair_mask(mk[2 * hh], 1), pp[2] & pair_mask(mk[2 * hh + 1], 0),
-                         pp[3] & pair_mask(mk[2 * hh + 1], 1));
-          }
-          kb[g4 >> 1] |= (keep_nibble(mk[0]) | (keep_nibble(mk[1]) << 4) |
-                          (keep_nibble(mk[2]) << 8) | (keep_nibble(mk[3]) << 12))
-                         << (16 * (g4 & 1));
-        }
-      } else {
-#pragma unroll
-        for (int u = 0; u < 8; ++u)
-          st_shared_v4(pbuf + sw128_offset(r, u), pw[4 * u], pw[4 * u + 1], pw[4 * u + 2],
-                       pw[4 * u + 3]);
-      }
-      fence_async_smem();
-      tc_fence_before();
-      mbar_arrive(bar(L::B_PR));
-      if (DQ && n > 0 && !drain_dq(n - 1, qt_prev, g_prev)) {
-        ok = false;
-        break;
-      }
-      // dS = P o (dP - D_i)
-      ok = __all_sync(0xffffffffu, wait_bar(bar(L::B_DPF), n & 1, wc));
-      if (!ok) break;
-      tc_fence_after();
-      const uint64_t dltx2 = f2_pack(dlt_c, dlt_c);
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t dp[32];
-        tmem_ld32(tDP + 32 * c, dp);
+    for (int u = blockIdx.x; ok && u < nunits; u += gridDim.x) {
+      if (!unit_at(u, un)) continue;
+      Sched sch;
+      sch.init(un.kt, un.nT, p.causal != 0, p.lists, un.bq0 % p.H, G);
+      kbase = un.kt * kTile;
+      kcol0 = kbase + 64 * half;
+      const int N = un.N;
+      uint32_t nu = 0;  // steps of this unit
+      int qt = 0, qt_prev = 0, g = 0, g_prev = 0;
+      bool have = sch.next(qt, g, p.lists);
+      float lse_c = 0.f, dlt_c = 0.f;
+      if (have) load_stats(qt, g, lse_c, dlt_c);
+      while (ok && have) {
+        int qt_n = 0, g_n = 0;
+        const bool have_n = sch.next(qt_n, g_n, p.lists);
+        float lse_n = 0.f, dlt_n = 0.f;
+        if (have_n) load_stats(qt_n, g_n, lse_n, dlt_n);  // prefetch the next tile's statistics
+        const int qrow = qt * kTile + r;
+        const bool live = qrow < N && lse_c != -INFINITY;
+        const float lse2 = live ? lse_c * kLog2e : 0.f;
+        // P = exp2(S * scale * log2e - lse * log2e); masked entries 0
+        ok = __all_sync(0xffffffffu, wait_bar(bar(L::B_SF), n & 1, wc));
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t sv[2][32];
+        tmem_ld32(tS, sv[0]);
+        tmem_ld32(tS + 32, sv[1]);
         tmem_ld_wait();
-        reg_fence(dp);
+        reg_fence(sv[0]);
+        reg_fence(sv[1]);
+        const bool need_mask = (kcol0 + 64 > N) || (p.causal && kcol0 + 63 > qt * kTile);
+        // keys kcol0 + i with i >= lim are masked (past N, or after this row
+        // when causal)
+        int lim = N - kcol0;
+        if (p.causal && qrow - kcol0 + 1 < lim) lim = qrow - kcol0 + 1;
+        uint32_t pw[32];  // pw[i]: keys 2i, 2i+1 of this thread's 64 columns
+        const uint64_t sl2x2 = f2_pack(sl2, sl2), nlse2x2 = f2_pack(-lse2, -lse2);
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          uint32_t w[4];
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const uint32_t pp = pw[16 * c + 4 * g + j];
-            float d0 = __uint_as_float(dp[8 * g + 2 * j]);
-            float d1 = __uint_as_float(dp[8 * g + 2 * j + 1]);
-            if (DROP) {  // dP = z dP~ / (1 - p')
-              d0 = ((kb[c] >> (8 * g + 2 * j)) & 1u) ? d0 * p.drop.scale : 0.f;
-              d1 = ((kb[c] >> (8 * g + 2 * j + 1)) & 1u) ? d1 * p.drop.scale : 0.f;
-            }
-            // P o (dP - D) for the two keys in fp32 x2
-            float x0, x1;
-            f2_unpack(f2_mul(f2_pack(bf16_lo(pp), bf16_hi(pp)),
-                             f2_sub(f2_pack(d0, d1), dltx2)),
-                      x0, x1);
-            w[j] = pack_bf16(x0, x1);
+        for (int i = 0; i < 32; ++i) {
+          // scale * S * log2 e - lse * log2 e for two keys in one fp32 x2 FMA
+          float a, b;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[i >> 4][(2 * i) & 31]),
+                                   __uint_as_float(sv[i >> 4][(2 * i + 1) & 31])),
+                           sl2x2, nlse2x2),
+                    a, b);
+          a = ex2(a);
+          b = ex2(b);
+          if (need_mask) {
+            if (2 * i >= lim) a = 0.f;
+            if (2 * i + 1 >= lim) b = 0.f;
           }
-          if (!L::OWN_STG && c == 0 && g == 0) {  // the previous dQ staging in these rows has been read
-            if (lane == 0) bulk_wait_read_all();
-            __syncwarp();
-          }
-          st_shared_v4(dsbuf + sw128_offset(r, 4 * c + g), w[0], w[1], w[2], w[3]);
+          pw[i] = live ? pack_bf16(a, b) : 0u;
         }
-      }
-      fence_async_smem();
-      tc_fence_before();
-      mbar_arrive(bar(L::B_DSR));
-      qt_prev = qt;
-      g_prev = g;
-      qt = qt_n;
-      g = g_n;
-      have = have_n;
-      lse_c = lse_n;
-      dlt_c = dlt_n;
-      ++n;
-    }
-    if (DQ && ok && n > 0) ok = drain_dq(n - 1, qt_prev, g_prev);
-    if (lane == 0) bulk_wait_all();  // every dQ reduce of this warp has landed
-    // ---------------------------------------------------- epilogue: dV, dK
-    // warps 4-7 write dV_j, warps 8-11 write scale * dK_j (thread = key row)
-    if (ok) ok = __all_sync(0xffffffffu, wait_bar(bar(L::B_FIN), 0, wc));
-    tc_fence_after();
-    const int key = kbase + r;
-    if (ok) {  // warp-uniform: every lane takes part in the TMEM reads
-      const bool dv_side = half == 0;
-      const uint32_t tcol = dv_side ? L::T_DV : L::T_DK;
-      const float mul = dv_side ? (DROP ? p.drop.scale : 1.f) : p.scale;
-      uint8_t* dst = static_cast<uint8_t*>(dv_side ? p.dv : p.dk) +
-                     (static_cast<size_t>(zkv) * slice_rows + row0 + (key < N ? key : 0)) *
-                         static_cast<size_t>(D) * 2;
-#pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t a[32];
-        if (n > 0) {
-          tmem_ld32(tmem + lane_off + tcol + 32 * c, a);
-          tmem_ld_wait();
-          reg_fence(a);
+        // keep bits of this thread's 64 keys (bit k of kb[c]: key 32 c + k)
+        uint32_t kb[2] = {0u, 0u};
+        if (DROP) {
+          // the dV product takes the dropped weights z * P; dS needs P and z
+#pragma unroll
+          for (int g4 = 0; g4 < 4; ++g4) {
+            const PhiloxOut rw = rng.group((kcol0 >> 4) + g4, qrow, un.bh_base + un.bq0 + g);
+            uint32_t mk[4];
+#pragma unroll
+            for (int w = 0; w < 4; ++w) mk[w] = DropoutRng::keep_bytes(rw.w[w], rng.t4);
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+              const uint32_t* pp = &pw[8 * g4 + 4 * hh];
+              st_shared_v4(pbuf + sw128_offset(r, 2 * g4 + hh), pp[0] & pair_mask(mk[2 * hh], 0),
+                           pp[1] & pair_mask(mk[2 * hh], 1), pp[2] & pair_mask(mk[2 * hh + 1], 0),
+                           pp[3] & pair_mask(mk[2 * hh + 1], 1));
+            }
+            kb[g4 >> 1] |= (keep_nibble(mk[0]) | (keep_nibble(mk[1]) << 4) |
+                            (keep_nibble(mk[2]) << 8) | (keep_nibble(mk[3]) << 12))
+                           << (16 * (g4 & 1));
+          }
         } else {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) a[j] = 0u;
+          for (int u = 0; u < 8; ++u)
+            st_shared_v4(pbuf + sw128_offset(r, u), pw[4 * u], pw[4 * u + 1], pw[4 * u + 2],
+                         pw[4 * u + 3]);
         }
-        if (key < N) {
-          uint4* o4 = reinterpret_cast<uint4*>(dst + c * 64);
+        fence_async_smem();
+        tc_fence_before();
+        mbar_arrive(bar(L::B_PR));
+        if (DQ && nu > 0 && !drain_dq(n - 1, qt_prev, g_prev)) {
+          ok = false;
+          break;
+        }
+        // dS = P o (dP - D_i)
+        ok = __all_sync(0xffffffffu, wait_bar(bar(L::B_DPF), n & 1, wc));
+        if (!ok) break;
+        tc_fence_after();
+        const uint64_t dltx2 = f2_pack(dlt_c, dlt_c);
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            uint4 w;
-            w.x = pack_bf16(__uint_as_float(a[8 * v + 0]) * mul, __uint_as_float(a[8 * v + 1]) * mul);
-            w.y = pack_bf16(__uint_as_float(a[8 * v + 2]) * mul, __uint_as_float(a[8 * v + 3]) * mul);
-            w.z = pack_bf16(__uint_as_float(a[8 * v + 4]) * mul, __uint_as_float(a[8 * v + 5]) * mul);
-            w.w = pack_bf16(__uint_as_float(a[8 * v + 6]) * mul, __uint_as_float(a[8 * v + 7]) * mul);
-            o4[v] = w;
+        for (int c = 0; c < 2; ++c) {
+          uint32_t dp[32];
+          tmem_ld32(tDP + 32 * c, dp);
+          tmem_ld_wait();
+          reg_fence(dp);
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            uint32_t w[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const uint32_t pp = pw[16 * c + 4 * g + j];
+              float d0 = __uint_as_float(dp[8 * g + 2 * j]);
+              float d1 = __uint_as_float(dp[8 * g + 2 * j + 1]);
+              if (DROP) {  // dP = z dP~ / (1 - p')
+                d0 = ((kb[c] >> (8 * g + 2 * j)) & 1u) ? d0 * p.drop.scale : 0.f;
+                d1 = ((kb[c] >> (8 * g + 2 * j + 1)) & 1u) ? d1 * p.drop.scale : 0.f;
+              }
+              // P o (dP - D) for the two keys in fp32 x2
+              float x0, x1;
+              f2_unpack(f2_mul(f2_pack(bf16_lo(pp), bf16_hi(pp)),
+                               f2_sub(f2_pack(d0, d1), dltx2)),
+                        x0, x1);
+              w[j] = pack_bf16(x0, x1);
+            }
+            if (!L::OWN_STG && c == 0 && g == 0) {  // the previous dQ staging in these rows has been read
+              if (lane == 0) bulk_wait_read_all();
+              __syncwarp();
+            }
+            st_shared_v4(dsbuf + sw128_offset(r, 4 * c + g), w[0], w[1], w[2], w[3]);
+          }
+        }
+        fence_async_smem();
+        tc_fence_before();
+        mbar_arrive(bar(L::B_DSR));
+        qt_prev = qt;
+        g_prev = g;
+        qt = qt_n;
+        g = g_n;
+        have = have_n;
+        lse_c = lse_n;
+        dlt_c = dlt_n;
+        ++n;
+        ++nu;
+      }
+      if (DQ && ok && nu > 0) ok = drain_dq(n - 1, qt_prev, g_prev);
+      // ---------------------------------------------------- epilogue: dV, dK
+      // warps 4-7 write dV_j, warps 8-11 write scale * dK_j (thread = key row);
+      // the next unit's first dV, dK products (issued after this thread's next
+      // P / dS arrivals) overwrite the columns read here
+      if (ok) ok = __all_sync(0xffffffffu, wait_bar(bar(L::B_FIN), ku & 1, wc));
+      tc_fence_after();
+      const int key = kbase + r;
+      if (ok) {  // warp-uniform: every lane takes part in the TMEM reads
+        const bool dv_side = half == 0;
+        const uint32_t tcol = dv_side ? L::T_DV : L::T_DK;
+        const float mul = dv_side ? (DROP ? p.drop.scale : 1.f) : p.scale;
+        uint8_t* dst = static_cast<uint8_t*>(dv_side ? p.dv : p.dk) +
+                       (static_cast<size_t>(un.zkv) * slice_rows + un.row0 + (key < N ? key : 0)) *
+                           static_cast<size_t>(D) * 2;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t a[32];
+          if (nu > 0) {
+            tmem_ld32(tmem + lane_off + tcol + 32 * c, a);
+            tmem_ld_wait();
+            reg_fence(a);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) a[j] = 0u;
+          }
+          if (key < N) {
+            uint4* o4 = reinterpret_cast<uint4*>(dst + c * 64);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              uint4 o;
+              o.x = pack_bf16(__uint_as_float(a[8 * v + 0]) * mul, __uint_as_float(a[8 * v + 1]) * mul);
+              o.y = pack_bf16(__uint_as_float(a[8 * v + 2]) * mul, __uint_as_float(a[8 * v + 3]) * mul);
+              o.z = pack_bf16(__uint_as_float(a[8 * v + 4]) * mul, __uint_as_float(a[8 * v + 5]) * mul);
+              o.w = pack_bf16(__uint_as_float(a[8 * v + 6]) * mul, __uint_as_float(a[8 * v + 7]) * mul);
+              o4[v] = o;
+            }
           }
         }
       }
+      tc_fence_before();
+      ++ku;
     }
+    if (lane == 0) bulk_wait_all();  // every dQ reduce of this warp has landed
   }
   tc_fence_before();
   __syncthreads();
@@ -602,7 +678,14 @@ cudaError_t launch_bwd_d(const BwdParams& p, const CUtensorMap& tq, const CUtens
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
   if (e != cudaSuccess) return e;
   const int nT = (p.N + kTile - 1) / kTile;
-  const long long ctas = static_cast<long long>(nT) * p.B * (p.Hkv > 0 ? p.Hkv : p.H);
+  const long long units = static_cast<long long>(nT) * p.B * (p.Hkv > 0 ? p.Hkv : p.H);
+  // persistent: one CTA per SM (the CTA holds the SM's TMEM and most of its
+  // shared memory), each walking units blockIdx.x, blockIdx.x + grid, ...
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+    return e;
+  const long long ctas = units < sms ? units : sms;
   return launch_pdl(fa_bwd_kernel<D, KIND, DQ>, dim3(static_cast<unsigned>(ctas)),
                     dim3(kBwdThreads), L::ALLOC, stream, tq, tk, tv, tdo, tdq, p);
 }
