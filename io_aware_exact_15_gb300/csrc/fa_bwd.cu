@@ -427,10 +427,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     uint32_t n = 0, ku = 0;  // steps and units so far
     BwdUnit un{};
     int kbase = 0, kcol0 = 0;  // first key of the tile / of this thread's columns
-    auto load_stats = [&](int t, int gg, float& l_, float& d_) {
+    auto load_stats = [&](const BwdUnit& w, int t, int gg, float& l_, float& d_) {
       const int row = t * kTile + r;
       const size_t idx =
-          static_cast<size_t>(un.bq0 + gg) * slice_rows + un.row0 + (row < un.N ? row : 0);
+          static_cast<size_t>(w.bq0 + gg) * slice_rows + w.row0 + (row < w.N ? row : 0);
       l_ = p.lse[idx];
       d_ = p.delta[idx];
     };
@@ -479,23 +479,33 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // overlaps the dP wait and the dS arithmetic
       return true;
     };
-    for (int u = blockIdx.x; ok && u < nunits; u += gridDim.x) {
-      if (!unit_at(u, un)) continue;
-      Sched sch;
+    // the first unit at or after u that has keys (nunits if none)
+    auto seek = [&](int u, BwdUnit& w) {
+      while (u < nunits && !unit_at(u, w)) u += gridDim.x;
+      return u;
+    };
+    // current unit: its schedule, next query tile and that tile's statistics
+    int u = seek(blockIdx.x, un);
+    Sched sch;
+    int qt = 0, g = 0;
+    bool have = false;
+    float lse_c = 0.f, dlt_c = 0.f;
+    if (u < nunits) {
       sch.init(un.kt, un.nT, p.causal != 0, p.lists, un.bq0 % p.H, G);
+      have = sch.next(qt, g, p.lists);
+      if (have) load_stats(un, qt, g, lse_c, dlt_c);
+    }
+    while (ok && u < nunits) {
       kbase = un.kt * kTile;
       kcol0 = kbase + 64 * half;
       const int N = un.N;
       uint32_t nu = 0;  // steps of this unit
-      int qt = 0, qt_prev = 0, g = 0, g_prev = 0;
-      bool have = sch.next(qt, g, p.lists);
-      float lse_c = 0.f, dlt_c = 0.f;
-      if (have) load_stats(qt, g, lse_c, dlt_c);
+      int qt_prev = 0, g_prev = 0;
       while (ok && have) {
         int qt_n = 0, g_n = 0;
         const bool have_n = sch.next(qt_n, g_n, p.lists);
         float lse_n = 0.f, dlt_n = 0.f;
-        if (have_n) load_stats(qt_n, g_n, lse_n, dlt_n);  // prefetch the next tile's statistics
+        if (have_n) load_stats(un, qt_n, g_n, lse_n, dlt_n);  // prefetch the next tile's statistics
         const int qrow = qt * kTile + r;
         const bool live = qrow < N && lse_c != -INFINITY;
         const float lse2 = live ? lse_c * kLog2e : 0.f;
@@ -617,47 +627,81 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         ++nu;
       }
       if (DQ && ok && nu > 0) ok = drain_dq(n - 1, qt_prev, g_prev);
+      // the next unit's schedule and first statistics, loaded while the
+      // epilogue runs
+      BwdUnit un_n{};
+      const int u_n = seek(u + gridDim.x, un_n);
+      Sched sch_n;
+      int qt_u = 0, g_u = 0;
+      bool have_u = false;
+      float lse_u = 0.f, dlt_u = 0.f;
+      if (u_n < nunits) {
+        sch_n.init(un_n.kt, un_n.nT, p.causal != 0, p.lists, un_n.bq0 % p.H, G);
+        have_u = sch_n.next(qt_u, g_u, p.lists);
+        if (have_u) load_stats(un_n, qt_u, g_u, lse_u, dlt_u);
+      }
       // ---------------------------------------------------- epilogue: dV, dK
-      // warps 4-7 write dV_j, warps 8-11 write scale * dK_j (thread = key row);
-      // the next unit's first dV, dK products (issued after this thread's next
-      // P / dS arrivals) overwrite the columns read here
+      // warps 4-7 write dV_j, warps 8-11 write scale * dK_j; the next unit's
+      // first dV, dK products (issued after this thread's next P / dS
+      // arrivals) overwrite the columns read here
       if (ok) ok = __all_sync(0xffffffffu, wait_bar(bar(L::B_FIN), ku & 1, wc));
       tc_fence_after();
-      const int key = kbase + r;
       if (ok) {  // warp-uniform: every lane takes part in the TMEM reads
         const bool dv_side = half == 0;
         const uint32_t tcol = dv_side ? L::T_DV : L::T_DK;
         const float mul = dv_side ? (DROP ? p.drop.scale : 1.f) : p.scale;
+        const int krow0 = kbase + 32 * q4;  // key of this warp's first row
+        const int nrows = min(32, N - krow0);
         uint8_t* dst = static_cast<uint8_t*>(dv_side ? p.dv : p.dk) +
-                       (static_cast<size_t>(un.zkv) * slice_rows + un.row0 + (key < N ? key : 0)) *
+                       (static_cast<size_t>(un.zkv) * slice_rows + un.row0 + krow0) *
                            static_cast<size_t>(D) * 2;
+        // Each thread packs 64 columns of its key row (128 bytes) into this
+        // warp's 32 rows of the P buffer (the unit's last dV product, which
+        // read it, has completed); then each store writes 4 whole rows.
+        const uint32_t stg = pbuf + q4 * 4096;
 #pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t a[32];
+        for (int c = 0; c < D / 64; ++c) {
+          uint32_t a[2][32];
           if (nu > 0) {
-            tmem_ld32(tmem + lane_off + tcol + 32 * c, a);
+            tmem_ld32(tmem + lane_off + tcol + 64 * c, a[0]);
+            tmem_ld32(tmem + lane_off + tcol + 64 * c + 32, a[1]);
             tmem_ld_wait();
-            reg_fence(a);
+            reg_fence(a[0]);
+            reg_fence(a[1]);
           } else {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) a[j] = 0u;
+            for (int j = 0; j < 32; ++j) a[0][j] = a[1][j] = 0u;
           }
-          if (key < N) {
-            uint4* o4 = reinterpret_cast<uint4*>(dst + c * 64);
 #pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              uint4 o;
-              o.x = pack_bf16(__uint_as_float(a[8 * v + 0]) * mul, __uint_as_float(a[8 * v + 1]) * mul);
-              o.y = pack_bf16(__uint_as_float(a[8 * v + 2]) * mul, __uint_as_float(a[8 * v + 3]) * mul);
-              o.z = pack_bf16(__uint_as_float(a[8 * v + 4]) * mul, __uint_as_float(a[8 * v + 5]) * mul);
-              o.w = pack_bf16(__uint_as_float(a[8 * v + 6]) * mul, __uint_as_float(a[8 * v + 7]) * mul);
-              o4[v] = o;
-            }
+          for (int v = 0; v < 8; ++v) {
+            const uint32_t* x = &a[v >> 2][8 * (v & 3)];
+            st_shared_v4(stg + sw128_offset(lane, v),
+                         pack_bf16(__uint_as_float(x[0]) * mul, __uint_as_float(x[1]) * mul),
+                         pack_bf16(__uint_as_float(x[2]) * mul, __uint_as_float(x[3]) * mul),
+                         pack_bf16(__uint_as_float(x[4]) * mul, __uint_as_float(x[5]) * mul),
+                         pack_bf16(__uint_as_float(x[6]) * mul, __uint_as_float(x[7]) * mul));
           }
+          __syncwarp();
+#pragma unroll
+          for (int it = 0; it < 8; ++it) {
+            const int j = 4 * it + (lane >> 3), cc = lane & 7;
+            const uint4 v = ld_shared_v4(stg + sw128_offset(j, cc));
+            if (j < nrows)
+              *reinterpret_cast<uint4*>(dst + static_cast<size_t>(j) * D * 2 + c * 128 + cc * 16) = v;
+          }
+          __syncwarp();
         }
       }
       tc_fence_before();
       ++ku;
+      u = u_n;
+      un = un_n;
+      sch = sch_n;
+      qt = qt_u;
+      g = g_u;
+      have = have_u;
+      lse_c = lse_u;
+      dlt_c = dlt_u;
     }
     if (lane == 0) bulk_wait_all();  // every dQ reduce of this warp has landed
   }
