@@ -75,9 +75,9 @@ cudaError_t launch_build_lists(const uint8_t* mask, int mask_heads, int nT, int*
 }
 
 // ------------------------------------------------------------------ backward helpers
-// D_i = sum_c dO_ic O_ic in fp32 and dQ_acc = 0.  Each thread takes items of
-// 8 consecutive elements of a row (16-byte loads of O and dO, 32 bytes of
-// zeros); the D/8 threads of a row reduce with shuffles.  Every thread keeps
+// dQ_acc = 0 and D_i = sum_c dO_ic O_ic in fp32.  For D each thread takes
+// items of 8 consecutive elements of a row (16-byte loads of O and dO); the
+// D/8 threads of a row reduce with shuffles.  Every thread keeps
 // kUnroll grid-stride items in flight, and the grid is sized so that each
 // thread has about that many.
 constexpr int kUnroll = 4;
@@ -88,11 +88,20 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const uint4* __restrict
                                                          float* __restrict__ delta,
                                                          float4* __restrict__ dq_acc,
                                                          long long rows) {
-  grid_dep_wait();  // the previous kernel's writes are visible from here on
   grid_dep_launch();
   constexpr int TPR = D / 8;  // threads per row: 8 or 16
   const long long total = rows * TPR;
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  // dQ_acc = 0 first: no kernel before this one can still be using the
+  // accumulator (the kernels that read or add into it signal their
+  // dependents only on completion), so this runs while the forward finishes
+  if (dq_acc) {  // null when dQ does not go through the accumulator
+    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+         t < 2 * total; t += stride)
+      dq_acc[t] = z;
+  }
+  grid_dep_wait();  // the previous kernel's writes (O) are visible from here on
   // the loop condition is warp-uniform (the warp's first item), so every
   // lane takes part in the shuffles
   for (long long t0 = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -116,10 +125,6 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const uint4* __restrict
                   bf16_lo(a[u].y) * bf16_lo(b[u].y) + bf16_hi(a[u].y) * bf16_hi(b[u].y) +
                   bf16_lo(a[u].z) * bf16_lo(b[u].z) + bf16_hi(a[u].z) * bf16_hi(b[u].z) +
                   bf16_lo(a[u].w) * bf16_lo(b[u].w) + bf16_hi(a[u].w) * bf16_hi(b[u].w);
-      if (dq_acc && t < total) {  // null when dQ does not go through the accumulator
-        dq_acc[2 * t] = make_float4(0.f, 0.f, 0.f, 0.f);
-        dq_acc[2 * t + 1] = make_float4(0.f, 0.f, 0.f, 0.f);
-      }
 #pragma unroll
       for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
       if (t < total && (t % TPR) == 0) delta[t / TPR] = acc;
@@ -153,7 +158,8 @@ __global__ void __launch_bounds__(256) fa_dq_convert_kernel(const float4* __rest
                                                             uint4* __restrict__ dq, long long n8,
                                                             float scale) {
   grid_dep_wait();  // the previous kernel's writes are visible from here on
-  grid_dep_launch();
+  // no early grid_dep_launch: the next kernel may be a preprocess that zeroes
+  // this accumulator before its own wait
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
   for (long long i0 = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i0 < n8;
        i0 += kUnroll * stride) {

@@ -45,8 +45,8 @@ struct BwdSmem {
   static constexpr int CH = D / 64;
   static constexpr int CHUNK = kTile * 128;
   static constexpr int TILE = CH * CHUNK;
-  static constexpr int NQ = (D == 64) ? 3 : 2;
-  static constexpr int NDO = (D == 64) ? 3 : 1;
+  static constexpr int NQ = 2;                  // Q ring (a third slot measured slower)
+  static constexpr int NDO = (D == 64) ? 2 : 1;  // dO ring
   static constexpr int PT = 2 * CHUNK;  // 128 x 128 bf16
   static constexpr int K = 0;
   static constexpr int V = K + TILE;
@@ -126,8 +126,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                   const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
                   const __grid_constant__ CUtensorMap tdq, const BwdParams p) {
   using L = BwdSmem<D>;
-  grid_dep_wait();  // the previous kernel's writes are visible from here on
-  grid_dep_launch();
+  // with dQ reduce-adds, no early grid_dep_launch: the next kernel may be a
+  // preprocess that zeroes the accumulator before its own wait
+  if (!DQ) grid_dep_launch();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -179,6 +180,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  grid_dep_wait();  // the previous kernel's writes are visible from here on
   const uint32_t tmem = *tmem_slot;
   const WaitCtl wc{abort_flag, p.err, p.wait_ns};
 

@@ -89,7 +89,11 @@ FA_DEV void drain_bar(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
 // finishing, so each kernel waits (grid_dep_wait) before its first access to
 // global memory, which makes everything the previous kernel wrote visible,
 // and then lets the next kernel be scheduled (grid_dep_launch).  Without that
-// launch attribute both are no-ops.
+// launch attribute both are no-ops.  Two exceptions: the backward preprocess
+// zeroes the dQ accumulator before its wait (that work depends on nothing
+// the forward writes and can overlap its last wave), and so the kernels that
+// read or add into that accumulator (the backward main kernel, the dQ
+// conversion) let the next kernel start only when they have finished.
 FA_DEV void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 FA_DEV void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
