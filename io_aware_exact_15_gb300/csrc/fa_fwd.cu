@@ -391,34 +391,49 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     if (ok) ok = __all_sync(0xffffffffu, wait_bar(bar(L::B_OF), 0, wc));
     tc_fence_after();
     if (ok && active) {
-      uint8_t* orow = static_cast<uint8_t*>(p.o) +
-                      (static_cast<size_t>(zq) * slice_rows + row0 + qrow) * static_cast<size_t>(D) * 2;
+      const int qrow0 = qt * kTile + q4 * 32;  // this warp's first query row
+      const int nrows = min(32, N - qrow0);
+      uint8_t* obase = static_cast<uint8_t*>(p.o) +
+                       (static_cast<size_t>(zq) * slice_rows + row0 + qrow0) *
+                           static_cast<size_t>(D) * 2;
       const bool store = qrow < N;
       const bool has = cnt > 0 && l > 0.f;
       // inverted dropout scales the kept weights by 1 / (1 - p')
       const float inv = has ? (DROP ? p.drop.scale : 1.f) / l : 0.f;
+      // Each thread packs 64 columns of its O row (128 bytes) into this
+      // warp's rows of Q_s (free: the tile's last S product has completed),
+      // then each store writes 4 whole 128-byte row pieces.
+      const uint32_t stg = sb + L::Q + s * L::TILE + q4 * 4096;
 #pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t o[32];
+      for (int c = 0; c < D / 64; ++c) {
+        uint32_t o[2][32];
         if (cnt > 0) {
-          tmem_ld32(tO + 32 * c, o);
+          tmem_ld32(tO + 64 * c, o[0]);
+          tmem_ld32(tO + 64 * c + 32, o[1]);
           tmem_ld_wait();
-          reg_fence(o);
+          reg_fence(o[0]);
+          reg_fence(o[1]);
         } else {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) o[j] = 0u;
+          for (int j = 0; j < 32; ++j) o[0][j] = o[1][j] = 0u;
         }
-        if (store) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + c * 64);
+        const uint32_t st = stg + c * L::CHUNK;
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            uint4 w;
-            w.x = pack_bf16(__uint_as_float(o[8 * v + 0]) * inv, __uint_as_float(o[8 * v + 1]) * inv);
-            w.y = pack_bf16(__uint_as_float(o[8 * v + 2]) * inv, __uint_as_float(o[8 * v + 3]) * inv);
-            w.z = pack_bf16(__uint_as_float(o[8 * v + 4]) * inv, __uint_as_float(o[8 * v + 5]) * inv);
-            w.w = pack_bf16(__uint_as_float(o[8 * v + 6]) * inv, __uint_as_float(o[8 * v + 7]) * inv);
-            dst[v] = w;
-          }
+        for (int v = 0; v < 8; ++v) {
+          const uint32_t* x = &o[v >> 2][8 * (v & 3)];
+          st_shared_v4(st + sw128_offset(lane, v),
+                       pack_bf16(__uint_as_float(x[0]) * inv, __uint_as_float(x[1]) * inv),
+                       pack_bf16(__uint_as_float(x[2]) * inv, __uint_as_float(x[3]) * inv),
+                       pack_bf16(__uint_as_float(x[4]) * inv, __uint_as_float(x[5]) * inv),
+                       pack_bf16(__uint_as_float(x[6]) * inv, __uint_as_float(x[7]) * inv));
+        }
+        __syncwarp();
+#pragma unroll
+        for (int it = 0; it < 8; ++it) {
+          const int j = 4 * it + (lane >> 3), cc = lane & 7;
+          const uint4 v = ld_shared_v4(st + sw128_offset(j, cc));
+          if (j < nrows)
+            *reinterpret_cast<uint4*>(obase + static_cast<size_t>(j) * D * 2 + c * 128 + cc * 16) = v;
         }
       }
       if (store)
