@@ -114,7 +114,7 @@ FA_DEV bool bwd_unit(int u, const BwdParams& p, int Hkv, int G, int ntmax, bool 
   return w.kt * kTile < w.N;
 }
 
-// Persistent: CTA c takes the units c, c + gridDim.x, ... in turn.  Per
+// Persistent: each CTA takes one unit of every round of gridDim.x units.  Per
 // unit, K_j and V_j of the next unit load while the previous unit's last dQ
 // drains and its dV, dK leave TMEM, and the Q / dO rings and every step
 // barrier run on across units.
@@ -149,6 +149,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   constexpr bool DROP = KIND == kGeneralDropout;
   const bool varlen = KIND >= kGeneral && p.cu_seqlens != nullptr;
   const size_t slice_rows = varlen ? static_cast<size_t>(p.total) : static_cast<size_t>(p.N);
+  // k-th unit of this CTA: rounds of gridDim.x units, walked left to right in
+  // even rounds and right to left in odd ones.  Units come longest first
+  // (causal), so each CTA pairs a long unit with a short one.
+  auto unit_of = [&](int k) {
+    const int base = k * static_cast<int>(gridDim.x);
+    return base + ((k & 1) ? static_cast<int>(gridDim.x - 1 - blockIdx.x)
+                           : static_cast<int>(blockIdx.x));
+  };
   auto unit_at = [&](int u, BwdUnit& w) {
     return bwd_unit<GQA>(u, p, Hkv, G, ntmax, varlen, w);
   };
@@ -212,7 +220,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         ++nkv;
         return true;
       };
-      for (int u = blockIdx.x; ok && u < nunits; u += gridDim.x) {
+      for (int k = 0, u; ok && (u = unit_of(k)) < nunits; ++k) {
         if (!unit_at(u, un)) continue;
         Sched sch;
         sch.init(un.kt, un.nT, p.causal != 0, p.lists, un.bq0 % p.H, G);
@@ -304,7 +312,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                      tDK = tmem + L::T_DK, tDQ = tmem + L::T_DQ;
       uint32_t n = 0, ku = 0;  // steps and units so far
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < nunits; u += gridDim.x) {
+      for (int k = 0, u; ok && (u = unit_of(k)) < nunits; ++k) {
         BwdUnit un;
         if (!unit_at(u, un)) continue;
         Sched sch;
@@ -482,12 +490,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       return true;
     };
     // the first unit at or after u that has keys (nunits if none)
-    auto seek = [&](int u, BwdUnit& w) {
-      while (u < nunits && !unit_at(u, w)) u += gridDim.x;
-      return u;
+    // the first of this CTA's units from the k-th on that has keys (its
+    // ordinal; unit_of(result) >= nunits if none)
+    auto seek = [&](int k, BwdUnit& w) {
+      while (unit_of(k) < nunits && !unit_at(unit_of(k), w)) ++k;
+      return k;
     };
     // current unit: its schedule, next query tile and that tile's statistics
-    int u = seek(blockIdx.x, un);
+    int kc = seek(0, un);
+    int u = unit_of(kc);
     Sched sch;
     int qt = 0, g = 0;
     bool have = false;
@@ -632,7 +643,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // the next unit's schedule and first statistics, loaded while the
       // epilogue runs
       BwdUnit un_n{};
-      const int u_n = seek(u + gridDim.x, un_n);
+      const int k_n = seek(kc + 1, un_n);
+      const int u_n = unit_of(k_n);
       Sched sch_n;
       int qt_u = 0, g_u = 0;
       bool have_u = false;
@@ -696,6 +708,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       tc_fence_before();
       ++ku;
+      kc = k_n;
       u = u_n;
       un = un_n;
       sch = sch_n;

@@ -308,9 +308,13 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     if (ok) ok = __all_sync(0xffffffffu, wait_bar(bar(L::B_FIN), 0, wc));
     tc_fence_after();
     if (ok) {  // warp-uniform: every lane takes part in the TMEM reads
-      uint8_t* dst = static_cast<uint8_t*>(p.dq) +
-                     (row_idx * D + (D / 2) * half) * 2;
-#pragma unroll 1
+      // This thread's D/2 columns of its row are packed into the Q tile (no
+      // MMA reads it any more), in the row's half of the 128-byte-swizzled
+      // layout; then each store writes whole row pieces of 32 rows.
+      constexpr int U = D / 16;  // 16-byte units per thread row (D/2 bf16)
+      const uint32_t qbuf = sb + L::Q + (D == 128 ? half * L::CHUNK : 0);
+      const int u0 = (D == 64) ? 4 * half : 0;  // first unit of this half in the row
+#pragma unroll
       for (int c = 0; c < D / 64; ++c) {
         uint32_t a[32];
         if (n > 0) {
@@ -321,22 +325,29 @@ __global__ void __launch_bounds__(kDqThreads, 1)
 #pragma unroll
           for (int j = 0; j < 32; ++j) a[j] = 0u;
         }
-        if (qrow < N) {
-          uint4* o4 = reinterpret_cast<uint4*>(dst + c * 64);
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            uint4 w;
-            w.x = pack_bf16(__uint_as_float(a[8 * v + 0]) * p.scale,
-                            __uint_as_float(a[8 * v + 1]) * p.scale);
-            w.y = pack_bf16(__uint_as_float(a[8 * v + 2]) * p.scale,
-                            __uint_as_float(a[8 * v + 3]) * p.scale);
-            w.z = pack_bf16(__uint_as_float(a[8 * v + 4]) * p.scale,
-                            __uint_as_float(a[8 * v + 5]) * p.scale);
-            w.w = pack_bf16(__uint_as_float(a[8 * v + 6]) * p.scale,
-                            __uint_as_float(a[8 * v + 7]) * p.scale);
-            o4[v] = w;
-          }
-        }
+        for (int v = 0; v < 4; ++v)
+          st_shared_v4(qbuf + sw128_offset(r, u0 + 4 * c + v),
+                       pack_bf16(__uint_as_float(a[8 * v + 0]) * p.scale,
+                                 __uint_as_float(a[8 * v + 1]) * p.scale),
+                       pack_bf16(__uint_as_float(a[8 * v + 2]) * p.scale,
+                                 __uint_as_float(a[8 * v + 3]) * p.scale),
+                       pack_bf16(__uint_as_float(a[8 * v + 4]) * p.scale,
+                                 __uint_as_float(a[8 * v + 5]) * p.scale),
+                       pack_bf16(__uint_as_float(a[8 * v + 6]) * p.scale,
+                                 __uint_as_float(a[8 * v + 7]) * p.scale));
+      }
+      __syncwarp();
+      const int qrow0 = qt * kTile + q4 * 32;  // this warp's first row
+      uint8_t* dst = static_cast<uint8_t*>(p.dq) +
+                     ((static_cast<size_t>(bh) * N + qrow0) * D + (D / 2) * half) * 2;
+      constexpr int RPI = 32 / U;  // rows per store instruction
+#pragma unroll
+      for (int it = 0; it < 32 / RPI; ++it) {
+        const int j = it * RPI + lane / U, v = lane % U;
+        const uint4 w = ld_shared_v4(qbuf + sw128_offset(q4 * 32 + j, u0 + v));
+        if (qrow0 + j < N)
+          *reinterpret_cast<uint4*>(dst + static_cast<size_t>(j) * D * 2 + v * 16) = w;
       }
     }
   }
