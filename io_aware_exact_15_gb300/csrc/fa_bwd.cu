@@ -8,12 +8,12 @@
 //   dS = P o (dP - D_i),
 //   dV_j += P^T dO_i,  dK_j += dS^T Q_i,  dQ_i += dS K_j  (dQ, dK scaled later).
 //
-// GB300 design (one CTA = one key/value head x one 128-key tile; K_j, V_j
+// GB300 design (a unit = one key/value head x one 128-key tile; K_j, V_j
 // stay in shared memory while the CTA walks the query tiles of every query
 // head that reads this key/value head, so grouped K/V needs no atomics for
-// dK and dV):
-//   warp 0      TMA producer: K_j, V_j once; Q_i through an NQ-slot ring and
-//               dO_i through an NDO-slot ring (128-byte swizzle)
+// dK and dV; persistent CTAs, one per SM, take the units in turn):
+//   warp 0      TMA producer: K_j, V_j once per unit; Q_i through an NQ-slot
+//               ring and dO_i through an NDO-slot ring (128-byte swizzle)
 //   warp 1      allocates 512 TMEM columns; lane 0 issues the five MMAs
 //   warps 4-11  one thread per query row and half of the key columns (warps
 //               4-7: keys 0-63, warps 8-11: keys 64-127): P from S and lse
@@ -25,7 +25,8 @@
 //               dQ accumulator by TMA reduce-add while the tensor core runs
 //               the next MMAs
 //   warps 2-3   idle
-// At the end warps 4-7 write dV_j and warps 8-11 write scale * dK_j.
+// At the end of a unit warps 4-7 write dV_j and warps 8-11 write scale * dK_j
+// (whole rows, through their rows of the P buffer).
 // TMEM: S [0,128) dP [128,256) dV [256,256+d) dK [256+d,256+2d);
 //       dQ at [384,448) for d = 64 and over the dP columns for d = 128.
 #include <math.h>
