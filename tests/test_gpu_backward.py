@@ -44,6 +44,34 @@ def test_backward_small_full(N, d, causal):
     parity.check_grad(dv, dv_r, "dV", what)
 
 
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("d", [64, 128])
+def test_backward_split_entry_points(d, causal):
+    # preprocess -> main -> dq_convert, called one by one, gives the
+    # gradients of fa_backward
+    dev = device()
+    B, H, N = 2, 3, 513
+    q, k, v, do = W.make_qkv(B, H, N, d, seed=5 + d + causal)
+    scale = 1.0 / d ** 0.5
+    qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
+    o = torch.empty_like(qd)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    assert fa.fa_forward(qd, kd, vd, o, lse, B, H, N, d, scale, causal) == fa.FA_OK
+    dq, dk, dv = (torch.full_like(qd, float("nan")) for _ in range(3))
+    nbytes = fa.fa_backward_workspace_size(B, H, N, d)
+    ws = torch.full((nbytes,), 0xFF, dtype=torch.uint8, device=dev)
+    assert fa.fa_backward_preprocess(o, dod, B, H, N, d, ws, nbytes) == fa.FA_OK
+    assert fa.fa_backward_main(qd, kd, vd, dod, lse, dk, dv, B, H, N, d, scale, causal, ws,
+                               nbytes) == fa.FA_OK
+    assert fa.fa_backward_dq_convert(dq, B, H, N, d, scale, ws, nbytes) == fa.FA_OK
+    status_ok()
+    what = f"d={d} causal={causal}"
+    dq_r, dk_r, dv_r = parity.oracle_backward(q, k, v, do, scale, causal)
+    parity.check_grad(dq.cpu(), dq_r, "dQ", what)
+    parity.check_grad(dk.cpu(), dk_r, "dK", what)
+    parity.check_grad(dv.cpu(), dv_r, "dV", what)
+
+
 def test_backward_single_key_closed_form():
     # N = 1: O = V, dV = dO and dQ = dK = 0 exactly
     dev = device()
