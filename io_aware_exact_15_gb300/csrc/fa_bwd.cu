@@ -447,6 +447,40 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     };
     // dQ of query tile t (step m): TMEM -> registers, release the columns,
     // then add this thread's D/2 columns into the fp32 accumulator
+    // d = 128: the second 32 columns of this thread's dQ row wait in
+    // registers (dq1) until the step's dS is out, then leave through the
+    // warp's rows of the P buffer once the dV product has read it; the next
+    // P store waits for that read, about a step later.
+    constexpr bool SPLIT = (D == 128) && DQ;
+    uint32_t dq1[32];
+    int t1 = 0, g1 = 0;
+    bool dq1_live = false;
+    auto stage_dq1 = [&]() {
+      const uint32_t st1 = pbuf + q4 * 4096;
+      // the previous half staged here may still be in flight: at a unit's
+      // end two stagings follow each other with no P store between them
+      if (lane == 0) bulk_wait_read_all();
+      __syncwarp();
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        st_shared_v4(st1 + sw128_offset(lane, u), dq1[4 * u], dq1[4 * u + 1], dq1[4 * u + 2],
+                     dq1[4 * u + 3]);
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_reduce_add_3d(&tdq, st1, (D / 2) * half + 32, un.row0 + t1 * kTile + 32 * q4,
+                          un.bq0 + g1);
+        bulk_commit();
+      }
+      dq1_live = false;
+    };
+    // the P rows of this warp may be written once the TMA has read them
+    auto p_rows_free = [&]() {
+      if (SPLIT) {
+        if (lane == 0) bulk_wait_read_all();
+        __syncwarp();
+      }
+    };
     auto drain_dq = [&](uint32_t m, int t, int gg) -> bool {
       if (!__all_sync(0xffffffffu, wait_bar(bar(L::B_DQF), m & 1, wc))) return false;
       tc_fence_after();
@@ -467,8 +501,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // their P and dS rows are 0).
       const uint32_t stage =
           (L::OWN_STG ? sb + L::STG + half * L::CHUNK : dsbuf) + q4 * 4096;
+      if (SPLIT) {  // second half later, from the P rows
 #pragma unroll
-      for (int c = 0; c < D / 64; ++c) {
+        for (int j = 0; j < 32; ++j) dq1[j] = dq[1][j];
+        t1 = t;
+        g1 = gg;
+        dq1_live = true;
+      }
+#pragma unroll
+      for (int c = 0; c < (SPLIT ? 1 : D / 64); ++c) {
         if (c > 0 || L::OWN_STG) {  // the previous box has been read
           if (lane == 0) bulk_wait_read_all();
           __syncwarp();
@@ -558,6 +599,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         // keep bits of this thread's 64 keys (bit k of kb[c]: key 32 c + k)
         uint32_t kb[2] = {0u, 0u};
+        p_rows_free();
         if (DROP) {
           // the dV product takes the dropped weights z * P; dS needs P and z
 #pragma unroll
@@ -630,6 +672,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         fence_async_smem();
         tc_fence_before();
         mbar_arrive(bar(L::B_DSR));
+        if (SPLIT && dq1_live) {  // dV(n) has read P(n): its rows take dQ(n-1)'s second half
+          if (!__all_sync(0xffffffffu,
+                          wait_bar(bar(L::B_DOE + n % L::NDO), (n / L::NDO) & 1, wc))) {
+            ok = false;
+            break;
+          }
+          stage_dq1();
+        }
         qt_prev = qt;
         g_prev = g;
         qt = qt_n;
@@ -641,6 +691,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         ++nu;
       }
       if (DQ && ok && nu > 0) ok = drain_dq(n - 1, qt_prev, g_prev);
+      if (SPLIT && ok && dq1_live) {  // after the unit's last dV (step n - 1)
+        ok = __all_sync(0xffffffffu, wait_bar(bar(L::B_DOE + (n - 1) % L::NDO),
+                                              ((n - 1) / L::NDO) & 1, wc));
+        if (ok) stage_dq1();
+      }
       // the next unit's schedule and first statistics, loaded while the
       // epilogue runs
       BwdUnit un_n{};
@@ -674,6 +729,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         // warp's 32 rows of the P buffer (the unit's last dV product, which
         // read it, has completed); then each store writes 4 whole rows.
         const uint32_t stg = pbuf + q4 * 4096;
+        p_rows_free();
 #pragma unroll 1
         for (int c = 0; c < D / 64; ++c) {
           uint32_t a[2][32];
