@@ -20,8 +20,9 @@
 //               (ex2 with the scale folded in) and dS from dP and D, both
 //               written to shared memory as bf16 for the MMAs that read them;
 //               between the two, the previous tile's dQ is read out of TMEM,
-//               staged (d = 64: in a buffer of its own; d = 128: in the
-//               then idle dS buffer) and added into the fp32
+//               staged (d = 64: in a buffer of its own; d = 128: the first
+//               half in the then idle dS buffer, the second after the dS
+//               store in the warp's P rows) and added into the fp32
 //               dQ accumulator by TMA reduce-add while the tensor core runs
 //               the next MMAs
 //   warps 2-3   idle
@@ -484,12 +485,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     auto drain_dq = [&](uint32_t m, int t, int gg) -> bool {
       if (!__all_sync(0xffffffffu, wait_bar(bar(L::B_DQF), m & 1, wc))) return false;
       tc_fence_after();
-      uint32_t dq[D / 64][32];
+      // SPLIT: the second 32 columns go straight into dq1
+      constexpr int NCH = SPLIT ? 1 : D / 64;
+      uint32_t dq[NCH][32];
 #pragma unroll
-      for (int c = 0; c < D / 64; ++c) tmem_ld32(tDQ + 32 * c, dq[c]);
+      for (int c = 0; c < NCH; ++c) tmem_ld32(tDQ + 32 * c, dq[c]);
+      if (SPLIT) tmem_ld32(tDQ + 32, dq1);
       tmem_ld_wait();
 #pragma unroll
-      for (int c = 0; c < D / 64; ++c) reg_fence(dq[c]);
+      for (int c = 0; c < NCH; ++c) reg_fence(dq[c]);
+      if (SPLIT) reg_fence(dq1);
       tc_fence_before();
       mbar_arrive(bar(L::B_DQE));
       // Reduce-add through the TMA engine: the warp stages its 32 rows x 32
@@ -502,14 +507,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const uint32_t stage =
           (L::OWN_STG ? sb + L::STG + half * L::CHUNK : dsbuf) + q4 * 4096;
       if (SPLIT) {  // second half later, from the P rows
-#pragma unroll
-        for (int j = 0; j < 32; ++j) dq1[j] = dq[1][j];
         t1 = t;
         g1 = gg;
         dq1_live = true;
       }
 #pragma unroll
-      for (int c = 0; c < (SPLIT ? 1 : D / 64); ++c) {
+      for (int c = 0; c < NCH; ++c) {
         if (c > 0 || L::OWN_STG) {  // the previous box has been read
           if (lane == 0) bulk_wait_read_all();
           __syncwarp();
