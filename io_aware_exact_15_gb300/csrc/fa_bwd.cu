@@ -499,11 +499,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_arrive(bar(L::B_DQE));
       // Reduce-add through the TMA engine: the warp stages its 32 rows x 32
       // columns (4 KB, 128-byte swizzle), for d = 64 in its own staging
-      // buffer, for d = 128 in its own rows of the dS buffer, which no MMA
-      // reads between dQ's completion and the next dS, and lane 0 adds the
-      // box into the fp32 accumulator (rows past the tensor are clipped; rows
-      // past this sequence but inside the tensor receive exact zeros, since
-      // their P and dS rows are 0).
+      // buffer, for d = 128 (the first 32 of its 64 columns) in its own rows
+      // of the dS buffer, which no MMA reads between dQ's completion and the
+      // next dS, and lane 0 adds the box into the fp32 accumulator (rows past
+      // the tensor are clipped; rows past this sequence but inside the tensor
+      // receive exact zeros, since their P and dS rows are 0).
       const uint32_t stage =
           (L::OWN_STG ? sb + L::STG + half * L::CHUNK : dsbuf) + q4 * 4096;
       if (SPLIT) {  // second half later, from the P rows
@@ -513,7 +513,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
 #pragma unroll
       for (int c = 0; c < NCH; ++c) {
-        if (c > 0 || L::OWN_STG) {  // the previous box has been read
+        if (c > 0 || L::OWN_STG) {  // the box staged here before has been read
           if (lane == 0) bulk_wait_read_all();
           __syncwarp();
         }
@@ -534,7 +534,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // overlaps the dP wait and the dS arithmetic
       return true;
     };
-    // the first unit at or after u that has keys (nunits if none)
     // the first of this CTA's units from the k-th on that has keys (its
     // ordinal; unit_of(result) >= nunits if none)
     auto seek = [&](int k, BwdUnit& w) {
