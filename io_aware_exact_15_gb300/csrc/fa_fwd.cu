@@ -109,6 +109,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   const size_t slice_rows = varlen ? static_cast<size_t>(p.total) : static_cast<size_t>(p.N);
   const int nT = (N + kTile - 1) / kTile;
 
+  FwdSchedule sch;
+  sch.init(pair, nT, p.causal != 0, p.lists, head, single);
+
+  // Thread 0 (the producer's lane) initialises the barriers and sends Q and
+  // the first K/V pair at once, before the block-wide barrier and the TMEM
+  // allocation, so that the first loads start as early as they can.
+  bool pre_kv = false;  // thread 0: the first key tile's K and V are in flight
   if (threadIdx.x == 0) {
     mbar_init(bar(L::B_Q), 1);
     for (int s = 0; s < L::NS; ++s) {
@@ -122,6 +129,30 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     mbar_init(bar(L::B_OF), 1);
     *abort_flag = 0;
     fence_mbar_init();
+    prefetch_tmap(&tq);
+    prefetch_tmap(&tk);
+    prefetch_tmap(&tv);
+    const int y0 = sch.qt[0] * kTile;
+    const int y1 = (sch.act[1] ? sch.qt[1] : sch.qt[0]) * kTile;
+    mbar_arrive_expect_tx(bar(L::B_Q), 2 * L::TILE);
+#pragma unroll
+    for (int c = 0; c < L::CH; ++c) {
+      tma_load_3d(sb + L::Q + c * L::CHUNK, &tq, bar(L::B_Q), 64 * c, row0 + y0, zq);
+      tma_load_3d(sb + L::Q + L::TILE + c * L::CHUNK, &tq, bar(L::B_Q), 64 * c, row0 + y1, zq);
+    }
+    FwdSchedule first = sch;  // the first key tile, without advancing sch
+    int kt0, mem0;
+    if (first.next(kt0, mem0)) {
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {  // ring slots 0 and 1
+        mbar_arrive_expect_tx(bar(L::B_KVF + t), L::TILE);
+#pragma unroll
+        for (int c = 0; c < L::CH; ++c)
+          tma_load_3d(sb + L::KV + t * L::TILE + c * L::CHUNK, t == 0 ? &tk : &tv,
+                      bar(L::B_KVF + t), 64 * c, row0 + kt0 * kTile, zkv);
+      }
+      pre_kv = true;
+    }
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), 512);
@@ -133,27 +164,19 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const WaitCtl wc{abort_flag, p.err, p.wait_ns};
 
-  FwdSchedule sch;
-  sch.init(pair, nT, p.causal != 0, p.lists, head, single);
-
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer
     if (lane == 0) {
-      prefetch_tmap(&tq);
-      prefetch_tmap(&tk);
-      prefetch_tmap(&tv);
-      const int y0 = sch.qt[0] * kTile;
-      const int y1 = (sch.act[1] ? sch.qt[1] : sch.qt[0]) * kTile;
-      mbar_arrive_expect_tx(bar(L::B_Q), 2 * L::TILE);
-#pragma unroll
-      for (int c = 0; c < L::CH; ++c) {
-        tma_load_3d(sb + L::Q + c * L::CHUNK, &tq, bar(L::B_Q), 64 * c, row0 + y0, zq);
-        tma_load_3d(sb + L::Q + L::TILE + c * L::CHUNK, &tq, bar(L::B_Q), 64 * c, row0 + y1, zq);
-      }
-      uint32_t idx = 0;
+      // Q and the first K/V pair went out before the block-wide barrier
+      uint32_t idx = pre_kv ? 2 : 0;
       bool ok = true;
+      bool skip = pre_kv;
       int kt, mem;
       while (ok && sch.next(kt, mem)) {
+        if (skip) {
+          skip = false;
+          continue;
+        }
         for (int t = 0; t < 2; ++t) {
           const int pos = idx % L::NS;
           const uint32_t round = idx / L::NS;
