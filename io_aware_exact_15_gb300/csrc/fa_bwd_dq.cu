@@ -78,6 +78,14 @@ __global__ void __launch_bounds__(kDqThreads, 1)
   fwd_cta_coords(blockIdx.x, BH, nT, p.causal != 0, bh, qt);  // causal: longest rows first
   const int head = bh % p.H;
 
+  // key tiles of query tile qt: 0 .. qt (causal), all, or its CSR list
+  FwdSchedule sch;
+  sch.init(qt, nT, p.causal != 0, p.lists, head, true);
+
+  // Thread 0 (the producer's lane) initialises the barriers and sends Q, dO
+  // and the first K/V pair at once, before the block-wide barrier and the
+  // TMEM allocation.
+  bool pre_kv = false;  // thread 0: the first key tile's K and V are in flight
   if (threadIdx.x == 0) {
     mbar_init(bar(L::B_QDO), 1);
     for (int s = 0; s < L::NS; ++s) {
@@ -91,6 +99,28 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     mbar_init(bar(L::B_FIN), 1);
     *abort_flag = 0;
     fence_mbar_init();
+    prefetch_tmap(&tq);
+    prefetch_tmap(&tk);
+    prefetch_tmap(&tv);
+    prefetch_tmap(&tdo);
+    mbar_arrive_expect_tx(bar(L::B_QDO), 2 * L::TILE);
+#pragma unroll
+    for (int c = 0; c < L::CH; ++c) {
+      tma_load_3d(sb + L::Q + c * L::CHUNK, &tq, bar(L::B_QDO), 64 * c, qt * kTile, bh);
+      tma_load_3d(sb + L::DO + c * L::CHUNK, &tdo, bar(L::B_QDO), 64 * c, qt * kTile, bh);
+    }
+    FwdSchedule first = sch;  // the first key tile, without advancing sch
+    int kt0, mem0;
+    if (first.next(kt0, mem0)) {  // ring slot 0
+      mbar_arrive_expect_tx(bar(L::B_KVF), 2 * L::TILE);
+#pragma unroll
+      for (int c = 0; c < L::CH; ++c) {
+        tma_load_3d(sb + L::KV + c * L::CHUNK, &tk, bar(L::B_KVF), 64 * c, kt0 * kTile, bh);
+        tma_load_3d(sb + L::KV + L::TILE + c * L::CHUNK, &tv, bar(L::B_KVF), 64 * c,
+                    kt0 * kTile, bh);
+      }
+      pre_kv = true;
+    }
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), 512);
@@ -102,27 +132,19 @@ __global__ void __launch_bounds__(kDqThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const WaitCtl wc{abort_flag, p.err, p.wait_ns};
 
-  // key tiles of query tile qt: 0 .. qt (causal), all, or its CSR list
-  FwdSchedule sch;
-  sch.init(qt, nT, p.causal != 0, p.lists, head, true);
-
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer
     if (lane == 0) {
-      prefetch_tmap(&tq);
-      prefetch_tmap(&tk);
-      prefetch_tmap(&tv);
-      prefetch_tmap(&tdo);
-      mbar_arrive_expect_tx(bar(L::B_QDO), 2 * L::TILE);
-#pragma unroll
-      for (int c = 0; c < L::CH; ++c) {
-        tma_load_3d(sb + L::Q + c * L::CHUNK, &tq, bar(L::B_QDO), 64 * c, qt * kTile, bh);
-        tma_load_3d(sb + L::DO + c * L::CHUNK, &tdo, bar(L::B_QDO), 64 * c, qt * kTile, bh);
-      }
-      uint32_t idx = 0;
+      // Q, dO and the first K/V pair went out before the block-wide barrier
+      uint32_t idx = pre_kv ? 1 : 0;
       bool ok = true;
+      bool skip = pre_kv;
       int kt, mem;
       while (ok && sch.next(kt, mem)) {
+        if (skip) {
+          skip = false;
+          continue;
+        }
         const int pos = idx % L::NS;
         const uint32_t round = idx / L::NS;
         if (round > 0 && !wait_bar(bar(L::B_KVE + pos), (round - 1) & 1, wc)) {
