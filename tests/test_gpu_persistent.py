@@ -1,0 +1,67 @@
+"""The persistent backward under load: shapes with more key-tile units than
+SMs (so every CTA walks several units and crosses unit boundaries), each run
+several times.  dK and dV must equal the deterministic key-tile pass bit for
+bit (same products in the same order), dQ must agree with the deterministic
+dQ pass within the gradient tolerance, and repeated runs must give the same
+dK, dV and (to rounding) dQ: a missing or doubled reduce-add, or a staging
+buffer overwritten before the TMA read it, shows up as a whole key tile's
+contribution to one slice of dQ."""
+import pytest
+
+from gpu_common import device, status_ok, torch
+import parity
+
+import fa_workloads as W
+import io_aware_exact_15_gb300 as fa
+
+pytestmark = pytest.mark.gpu
+
+RUNS = 3
+
+
+def _forward(qd, kd, vd, scale, causal):
+    B, H, N, d = qd.shape
+    o = torch.empty_like(qd)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=qd.device)
+    assert fa.fa_forward(qd, kd, vd, o, lse, B, H, N, d, scale, causal) == fa.FA_OK
+    return o, lse
+
+
+def _backward(fn, qd, kd, vd, o, dod, lse, scale, causal):
+    B, H, N, d = qd.shape
+    dq, dk, dv = (torch.full_like(qd, float("nan")) for _ in range(3))
+    nbytes = fa.fa_backward_workspace_size(B, H, N, d)
+    ws = torch.full((nbytes,), 0xFF, dtype=torch.uint8, device=qd.device)
+    assert fn(qd, kd, vd, o, dod, lse, dq, dk, dv, B, H, N, d, scale, causal, ws,
+              nbytes) == fa.FA_OK
+    status_ok()
+    return dq, dk, dv
+
+
+# (B, H, N, d): 256 to 1024 key-tile units for the 152-SM grid
+SHAPES = [(2, 8, 2048, 128), (4, 16, 512, 64), (2, 16, 1024, 64), (1, 8, 4096, 128)]
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("B,H,N,d", SHAPES)
+def test_multi_unit_backward_consistent(B, H, N, d, causal):
+    dev = device()
+    q, k, v, do = W.make_qkv(B, H, N, d, seed=900 + N + d + B + causal)
+    scale = 1.0 / d ** 0.5
+    qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
+    o, lse = _forward(qd, kd, vd, scale, causal)
+    dq_det, dk_det, dv_det = _backward(fa.fa_backward_deterministic, qd, kd, vd, o, dod, lse,
+                                       scale, causal)
+    ref = parity.f64(dq_det.cpu())
+    what = f"B{B} H{H} N{N} d{d} causal={causal}"
+    first = None
+    for run in range(RUNS):
+        dq, dk, dv = _backward(fa.fa_backward, qd, kd, vd, o, dod, lse, scale, causal)
+        assert torch.equal(dk, dk_det), f"{what} run {run}: dK differs from the key-tile pass"
+        assert torch.equal(dv, dv_det), f"{what} run {run}: dV differs from the key-tile pass"
+        parity.check_grad(dq.cpu(), ref, "dQ", f"{what} run {run} vs deterministic dQ")
+        if first is None:
+            first = dq
+        else:  # the reduce-adds commute only to rounding
+            assert (dq.float() - first.float()).abs().max().item() <= \
+                1e-2 * first.float().abs().max().item(), f"{what} run {run}: dQ drifted"
