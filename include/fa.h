@@ -69,8 +69,11 @@ fa_status fa_forward(const void* q, const void* k, const void* v, void* o, float
                      int N, int d, float scale, int causal, cudaStream_t stream);
 
 /* Bytes of workspace fa_backward needs: D (fp32 [B,H,N]) and the fp32 dQ
- * accumulator ([B,H,N,d]), each 256-byte aligned.  O(B*H*N*d), never
- * O(N^2). */
+ * accumulator ([B,H,N,d]), each 256-byte aligned; for d = 128 with more
+ * than 64 key tiles (B*H*ceil(N/128)) also min(tiles/2, 96) slots of
+ * 128 KiB plus 8 bytes each (at most 12 MiB): fp32 dK, dV partial sums
+ * of key tiles whose query-tile walk the last round of the persistent
+ * backward splits between two SMs.  O(B*H*N*d), never O(N^2). */
 size_t fa_backward_workspace_size(int B, int H, int N, int d);
 
 /*
@@ -119,7 +122,7 @@ fa_status fa_backward_dq_convert(void* dq, int B, int H, int N, int d, float sca
  *            held from library load until process exit.  Problems whose
  *            fa_backward_workspace_size(B, H, N, d) exceeds 2^25 bytes return
  *            FA_ERR_WORKSPACE with nothing launched (d = 64: about 129k rows
- *            B*H*N; d = 128: about 65k rows).
+ *            B*H*N; d = 128: about 40k rows).
  *   Sharing: every call on a device uses the same array, which keeps the last
  *            call's contents; each call clears what must start at zero (the
  *            dQ accumulator) itself.  Calls whose kernels overlap on the GPU

@@ -115,25 +115,46 @@ fa_status check_ptr4(const void* p) {
     if ((x) != cudaSuccess) return FA_ERR_CUDA;   \
   } while (0)
 
+int num_tiles(int N) { return (N + kTile - 1) / kTile; }
+
 struct BwdWorkspace {
   float* delta;
   float* dq_acc;
+  float* part;     // split-last-round partials: [nslot][2][128][d] fp32
+  int* part_cnt;   // [2 * nslot]
+  int nslot;
 };
+
+// Slots for the split last round (the d = 128 kernel only): the last round
+// splits only when it holds at most half the grid, so at most units / 2 (and
+// 96, half of 192 SMs).
+int split_slots(int B, int H, int N, int d) {
+  if (d != 128) return 0;
+  const long long units = static_cast<long long>(B) * H * num_tiles(N);
+  return units > 64 ? static_cast<int>(units / 2 < 96 ? units / 2 : 96) : 0;
+}
 
 size_t bwd_ws_bytes(int B, int H, int N, int d) {
   const size_t rows = static_cast<size_t>(B) * H * N;
-  return align256(rows * sizeof(float)) + align256(rows * d * sizeof(float));
+  const size_t ns = static_cast<size_t>(split_slots(B, H, N, d));
+  return align256(rows * sizeof(float)) + align256(rows * d * sizeof(float)) +
+         align256(ns * 2 * kTile * d * sizeof(float)) + align256(2 * ns * sizeof(int));
 }
 
-BwdWorkspace bwd_ws(void* ws, int B, int H, int N) {
+BwdWorkspace bwd_ws(void* ws, int B, int H, int N, int d) {
   const size_t rows = static_cast<size_t>(B) * H * N;
   BwdWorkspace w;
-  w.delta = static_cast<float*>(ws);
-  w.dq_acc = reinterpret_cast<float*>(static_cast<char*>(ws) + align256(rows * sizeof(float)));
+  char* base = static_cast<char*>(ws);
+  w.delta = reinterpret_cast<float*>(base);
+  base += align256(rows * sizeof(float));
+  w.dq_acc = reinterpret_cast<float*>(base);
+  base += align256(rows * d * sizeof(float));
+  w.nslot = split_slots(B, H, N, d);
+  w.part = reinterpret_cast<float*>(base);
+  base += align256(static_cast<size_t>(w.nslot) * 2 * kTile * d * sizeof(float));
+  w.part_cnt = reinterpret_cast<int*>(base);
   return w;
 }
-
-int num_tiles(int N) { return (N + kTile - 1) / kTile; }
 
 size_t lists_bytes(int N, int mask_heads) {
   const size_t nT = static_cast<size_t>(num_tiles(N));
@@ -243,6 +264,11 @@ fa_status backward_main_impl(const void* q, const void* k, const void* v, const 
   p.cu_seqlens = vl.cu_seqlens;
   p.total = vl.total;
   p.drop = drop;
+  if (!lists && w.nslot > 0) {  // the split last round (not with a block mask)
+    p.part = w.part;
+    p.part_cnt = w.part_cnt;
+    p.nslot = w.nslot;
+  }
   p.err = err;
   p.wait_ns = wait_limit_ns();
   FA_CUDA(fa::launch_backward_main(p, tq, tk, tv, tdo, tdq, stream));
@@ -391,9 +417,9 @@ fa_status fa_backward_preprocess(const void* o, const void* dO, int B, int H, in
   FA_TRY(check_ptr16(o));
   FA_TRY(check_ptr16(dO));
   FA_TRY(check_ws(workspace, workspace_bytes, bwd_ws_bytes(B, H, N, d)));
-  const BwdWorkspace w = bwd_ws(workspace, B, H, N);
-  FA_CUDA(fa::launch_bwd_preprocess(o, dO, w.delta, w.dq_acc, static_cast<long long>(B) * H * N, d,
-                                    stream));
+  const BwdWorkspace w = bwd_ws(workspace, B, H, N, d);
+  FA_CUDA(fa::launch_bwd_preprocess(o, dO, w.delta, w.dq_acc, w.part_cnt, 2LL * w.nslot,
+                                    static_cast<long long>(B) * H * N, d, stream));
   return FA_OK;
 }
 
@@ -407,7 +433,7 @@ fa_status fa_backward_main(const void* q, const void* k, const void* v, const vo
   FA_TRY(check_ptr4(lse));
   FA_TRY(check_ws(workspace, workspace_bytes, bwd_ws_bytes(B, H, N, d)));
   return backward_main_impl(q, k, v, dO, lse, dk, dv, B, H, H, N, d, scale, causal,
-                            bwd_ws(workspace, B, H, N), nullptr, stream);
+                            bwd_ws(workspace, B, H, N, d), nullptr, stream);
 }
 
 fa_status fa_backward_dq_convert(void* dq, int B, int H, int N, int d, float scale,
@@ -415,7 +441,7 @@ fa_status fa_backward_dq_convert(void* dq, int B, int H, int N, int d, float sca
   FA_TRY(check_shape(B, H, N, d, scale));
   FA_TRY(check_ptr16(dq));
   FA_TRY(check_ws(workspace, workspace_bytes, bwd_ws_bytes(B, H, N, d)));
-  const BwdWorkspace w = bwd_ws(workspace, B, H, N);
+  const BwdWorkspace w = bwd_ws(workspace, B, H, N, d);
   FA_CUDA(fa::launch_dq_convert(w.dq_acc, dq, static_cast<long long>(B) * H * N * d, scale, stream));
   return FA_OK;
 }
@@ -441,7 +467,7 @@ fa_status fa_backward_gqa(const void* q, const void* k, const void* v, const voi
   FA_TRY(check_ws(workspace, workspace_bytes, bwd_ws_bytes(B, H, N, d)));
   FA_TRY(fa_backward_preprocess(o, dO, B, H, N, d, workspace, workspace_bytes, stream));
   FA_TRY(backward_main_impl(q, k, v, dO, lse, dk, dv, B, H, Hkv, N, d, scale, causal,
-                            bwd_ws(workspace, B, H, N), nullptr, stream));
+                            bwd_ws(workspace, B, H, N, d), nullptr, stream));
   return fa_backward_dq_convert(dq, B, H, N, d, scale, workspace, workspace_bytes, stream);
 }
 
@@ -486,7 +512,7 @@ fa_status fa_backward_varlen(const void* q, const void* k, const void* v, const 
   vl.cu_seqlens = cu_seqlens;
   vl.total = total;
   FA_TRY(backward_main_impl(q, k, v, dO, lse, dk, dv, B, H, Hkv, max_seqlen, d, scale, causal,
-                            bwd_ws(workspace, 1, H, total), nullptr, stream, vl, drop));
+                            bwd_ws(workspace, 1, H, total, d), nullptr, stream, vl, drop));
   return fa_backward_dq_convert(dq, 1, H, total, d, scale, workspace, workspace_bytes, stream);
 }
 
@@ -502,7 +528,7 @@ fa_status fa_backward_deterministic(const void* q, const void* k, const void* v,
   if (!err) return st;
   float* delta = static_cast<float*>(workspace);
   // D only: the dQ accumulator is not used
-  FA_CUDA(fa::launch_bwd_preprocess(o, dO, delta, nullptr, static_cast<long long>(rows), d,
+  FA_CUDA(fa::launch_bwd_preprocess(o, dO, delta, nullptr, nullptr, 0, static_cast<long long>(rows), d,
                                     stream));
   CUtensorMap tq, tk, tv, tdo, tdq;
   // tdq is never dereferenced by the key-tile pass without its dQ product;
@@ -564,7 +590,7 @@ fa_status fa_backward_dropout(const void* q, const void* k, const void* v, const
   FA_TRY(check_ws(workspace, workspace_bytes, bwd_ws_bytes(B, H, N, d)));
   FA_TRY(fa_backward_preprocess(o, dO, B, H, N, d, workspace, workspace_bytes, stream));
   FA_TRY(backward_main_impl(q, k, v, dO, lse, dk, dv, B, H, H, N, d, scale, causal,
-                            bwd_ws(workspace, B, H, N), nullptr, stream, Varlen(), drop));
+                            bwd_ws(workspace, B, H, N, d), nullptr, stream, Varlen(), drop));
   return fa_backward_dq_convert(dq, B, H, N, d, scale, workspace, workspace_bytes, stream);
 }
 
@@ -608,7 +634,7 @@ fa_status fa_blocksparse_backward(const void* q, const void* k, const void* v, c
   const size_t bws_bytes = workspace_bytes - lb;
   FA_TRY(fa_backward_preprocess(o, dO, B, H, N, d, bws, bws_bytes, stream));
   FA_TRY(backward_main_impl(q, k, v, dO, lse, dk, dv, B, H, H, N, d, scale, causal,
-                            bwd_ws(bws, B, H, N), &L, stream));
+                            bwd_ws(bws, B, H, N, d), &L, stream));
   return fa_backward_dq_convert(dq, B, H, N, d, scale, bws, bws_bytes, stream);
 }
 

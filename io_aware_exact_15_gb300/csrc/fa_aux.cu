@@ -87,6 +87,7 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const uint4* __restrict
                                                          const uint4* __restrict__ dO,
                                                          float* __restrict__ delta,
                                                          float4* __restrict__ dq_acc,
+                                                         int* __restrict__ zero_i, long long nzero,
                                                          long long rows) {
   grid_dep_launch();
   constexpr int TPR = D / 8;  // threads per row: 8 or 16
@@ -101,6 +102,9 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const uint4* __restrict
          t < 2 * total; t += stride)
       dq_acc[t] = z;
   }
+  for (long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; t < nzero;
+       t += stride)
+    zero_i[t] = 0;  // counters of the backward's split last round
   grid_dep_wait();  // the previous kernel's writes (O) are visible from here on
   // the loop condition is warp-uniform (the warp's first item), so every
   // lane takes part in the shuffles
@@ -141,16 +145,17 @@ static int stream_blocks(long long items, int per_sm) {
 }
 
 cudaError_t launch_bwd_preprocess(const void* o, const void* dO, float* delta, float* dq_acc,
-                                  long long rows, int d, cudaStream_t stream) {
+                                  int* zero_i, long long nzero, long long rows, int d,
+                                  cudaStream_t stream) {
   const int blocks = stream_blocks(rows * (d / 8), 8);
   const uint4* o4 = static_cast<const uint4*>(o);
   const uint4* do4 = static_cast<const uint4*>(dO);
   float4* acc4 = reinterpret_cast<float4*>(dq_acc);
   if (d == 64)
     return launch_pdl(fa_bwd_pre_kernel<64>, dim3(blocks), dim3(256), 0, stream, o4, do4, delta,
-                      acc4, rows);
+                      acc4, zero_i, nzero, rows);
   return launch_pdl(fa_bwd_pre_kernel<128>, dim3(blocks), dim3(256), 0, stream, o4, do4, delta,
-                    acc4, rows);
+                    acc4, zero_i, nzero, rows);
 }
 
 // dq = bf16(scale * dq_acc), 8 elements per item, kUnroll items in flight

@@ -65,7 +65,8 @@ struct BwdSmem {
   static constexpr int B_KV = 0, B_QF = 1, B_QE = B_QF + NQ, B_DOF = B_QE + NQ,
                        B_DOE = B_DOF + NDO, B_SF = B_DOE + NDO, B_DPF = B_SF + 1,
                        B_PR = B_DPF + 1, B_DSR = B_PR + 1, B_DQF = B_DSR + 1, B_DQE = B_DQF + 1,
-                       B_FIN = B_DQE + 1, NBAR = B_FIN + 1;
+                       B_FIN = B_DQE + 1, B_SPL = B_FIN + 1, B_EPI = B_SPL + 1,
+                       NBAR = B_EPI + 1;
   static constexpr int MISC = BAR + NBAR * 8;
   static constexpr int ALLOC = MISC + 16 + 1024;
   static_assert(ALLOC <= 232448, "shared memory budget");
@@ -76,6 +77,18 @@ struct BwdSmem {
 
 constexpr int kBwdThreads = 384;
 constexpr float kLog2e = 1.4426950408889634f;
+
+// A unit's query-tile walk, or a stretch of it: at most `left` more steps.
+template <class S>
+struct BwdPartSchedule {
+  S s;
+  int left;
+  FA_DEV bool next(int& qt, int& g, const TileLists& L) {
+    if (left <= 0) return false;
+    --left;
+    return s.next(qt, g, L);
+  }
+};
 
 // Geometry of one work unit: one key/value head x one key tile.
 struct BwdUnit {
@@ -162,6 +175,51 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   auto unit_at = [&](int u, BwdUnit& w) {
     return bwd_unit<GQA>(u, p, Hkv, G, ntmax, varlen, w);
   };
+  // Split last round: when the last round's units fill at most half the
+  // grid, each runs as two halves of its query-tile walk on two CTAs.  Only
+  // for units of at least 8 steps (the last round's: G x nT dense, G x 1
+  // causal, whose last units are the diagonal key tiles): a shorter half
+  // pays the unit boundary and the hand-off for too little work (measured:
+  // B8 H16 N512 d64, 4-step units, 54 -> 60 us).  Compiled for d = 128
+  // only: in the d = 64 kernel the mere run-time option cost the B8 H16
+  // N512 backward 52 -> 57 us, though it never split there.
+  const int nround = (nunits + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x);
+  const int last0 = (nround - 1) * static_cast<int>(gridDim.x);  // first unit of the last round
+  const int mlast = nunits - last0;
+  const bool split = D == 128 && p.part != nullptr && p.lists.col_ptr == nullptr && !varlen && nround > 1 &&
+                     2 * mlast <= static_cast<int>(gridDim.x) && mlast <= p.nslot &&
+                     G * (p.causal ? 1 : ntmax) >= 8;
+  // k-th item of this CTA: unit u and half uh (-1: the whole unit); false
+  // when the CTA has no k-th item
+  auto item_of = [&](int k, int& u, int& uh) {
+    uh = -1;
+    if (!split || k < nround - 1) {
+      u = unit_of(k);
+      return u < nunits;
+    }
+    if (k > nround - 1) return false;
+    const int pos = (k & 1) ? static_cast<int>(gridDim.x - 1 - blockIdx.x)
+                            : static_cast<int>(blockIdx.x);
+    if (pos >= 2 * mlast) return false;
+    u = last0 + pos / 2;
+    uh = pos & 1;
+    return true;
+  };
+  // the query-tile walk of item (unit w, half uh): half 0 takes the first
+  // half of the unit's steps, half 1 the rest (no block mask here, so a
+  // unit has G x (nT, or nT - kt when causal) steps)
+  using Sched0 = typename std::conditional<GQA, BwdGroupSchedule, BwdSingleSchedule>::type;
+  auto start = [&](const BwdUnit& w, int uh, BwdPartSchedule<Sched0>& ps) {
+    ps.s.init(w.kt, w.nT, p.causal != 0, p.lists, w.bq0 % p.H, G);
+    ps.left = INT_MAX;
+    if (uh >= 0) {
+      const int ns = G * (p.causal ? w.nT - w.kt : w.nT);
+      int qt, gg;
+      if (uh == 1)
+        for (int i = 0; i < ns / 2; ++i) ps.s.next(qt, gg, p.lists);
+      ps.left = uh ? ns - ns / 2 : ns / 2;
+    }
+  };
 
   if (threadIdx.x == 0) {
     mbar_init(bar(L::B_KV), 1);
@@ -180,6 +238,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(bar(L::B_DQF), 1);
     mbar_init(bar(L::B_DQE), 256);
     mbar_init(bar(L::B_FIN), 1);
+    mbar_init(bar(L::B_SPL), 256);
+    mbar_init(bar(L::B_EPI), 256);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -194,7 +254,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const WaitCtl wc{abort_flag, p.err, p.wait_ns};
 
-  using Sched = typename std::conditional<GQA, BwdGroupSchedule, BwdSingleSchedule>::type;
+  using Sched = BwdPartSchedule<Sched0>;
 
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer
@@ -222,10 +282,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         ++nkv;
         return true;
       };
-      for (int k = 0, u; ok && (u = unit_of(k)) < nunits; ++k) {
+      for (int k = 0, u, uh; ok && item_of(k, u, uh); ++k) {
         if (!unit_at(u, un)) continue;
         Sched sch;
-        sch.init(un.kt, un.nT, p.causal != 0, p.lists, un.bq0 % p.H, G);
+        start(un, uh, sch);
         bool kv = false;  // the unit's first Q / dO copies go out before its K/V
         int qt, g;
         while (ok && sch.next(qt, g, p.lists)) {
@@ -314,11 +374,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                      tDK = tmem + L::T_DK, tDQ = tmem + L::T_DQ;
       uint32_t n = 0, ku = 0;  // steps and units so far
       bool ok = true;
-      for (int k = 0, u; ok && (u = unit_of(k)) < nunits; ++k) {
+      for (int k = 0, u, uh; ok && item_of(k, u, uh); ++k) {
         BwdUnit un;
         if (!unit_at(u, un)) continue;
         Sched sch;
-        sch.init(un.kt, un.nT, p.causal != 0, p.lists, un.bq0 % p.H, G);
+        start(un, uh, sch);
         int qt, qt_n, g_unused;
         ok = wait_bar(bar(L::B_KV), ku & 1, wc);
         bool have = ok && sch.next(qt, g_unused, p.lists);
@@ -410,7 +470,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         // every product of the unit issued: dV_j, dK_j complete and K_j, V_j
         // free once this lands (also committed on a failed wait, so that the
-        // phase count stays that of the other roles)
+        // phase count stays that of the other roles).  A unit with no step
+        // issued nothing the compute warps gate, so its commit could land
+        // right after the previous unit's, two phases ahead of a compute warp
+        // still to wait for that one: it waits until they have.
+        if (nu == 0 && ku > 0 && !wait_bar(bar(L::B_EPI), (ku - 1) & 1, wc)) ok = false;
         mma_commit(bar(L::B_FIN));
         ++ku;
       }
@@ -536,25 +600,27 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // overlaps the dP wait and the dS arithmetic
       return true;
     };
-    // the first of this CTA's units from the k-th on that has keys (its
-    // ordinal; unit_of(result) >= nunits if none)
-    auto seek = [&](int k, BwdUnit& w) {
-      while (unit_of(k) < nunits && !unit_at(unit_of(k), w)) ++k;
-      return k;
+    // the first of this CTA's items from the k-th on whose unit has keys
+    // (k, u, uh updated); false if none
+    auto seek = [&](int& k, int& u, int& uh, BwdUnit& w) {
+      for (;; ++k) {
+        if (!item_of(k, u, uh)) return false;
+        if (unit_at(u, w)) return true;
+      }
     };
-    // current unit: its schedule, next query tile and that tile's statistics
-    int kc = seek(0, un);
-    int u = unit_of(kc);
+    // current item: its schedule, next query tile and that tile's statistics
+    int kc = 0, u = 0, uh = -1;
+    bool cur = seek(kc, u, uh, un);
     Sched sch;
     int qt = 0, g = 0;
     bool have = false;
     float lse_c = 0.f, dlt_c = 0.f;
-    if (u < nunits) {
-      sch.init(un.kt, un.nT, p.causal != 0, p.lists, un.bq0 % p.H, G);
+    if (cur) {
+      start(un, uh, sch);
       have = sch.next(qt, g, p.lists);
       if (have) load_stats(un, qt, g, lse_c, dlt_c);
     }
-    while (ok && u < nunits) {
+    while (ok && cur) {
       kbase = un.kt * kTile;
       kcol0 = kbase + 64 * half;
       const int N = un.N;
@@ -703,14 +769,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // the next unit's schedule and first statistics, loaded while the
       // epilogue runs
       BwdUnit un_n{};
-      const int k_n = seek(kc + 1, un_n);
-      const int u_n = unit_of(k_n);
+      int k_n = kc + 1, u_n = 0, uh_n = -1;
+      const bool cur_n = seek(k_n, u_n, uh_n, un_n);
       Sched sch_n;
       int qt_u = 0, g_u = 0;
       bool have_u = false;
       float lse_u = 0.f, dlt_u = 0.f;
-      if (u_n < nunits) {
-        sch_n.init(un_n.kt, un_n.nT, p.causal != 0, p.lists, un_n.bq0 % p.H, G);
+      if (cur_n) {
+        start(un_n, uh_n, sch_n);
         have_u = sch_n.next(qt_u, g_u, p.lists);
         if (have_u) load_stats(un_n, qt_u, g_u, lse_u, dlt_u);
       }
@@ -719,6 +785,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // first dV, dK products (issued after this thread's next P / dS
       // arrivals) overwrite the columns read here
       if (ok) ok = __all_sync(0xffffffffu, wait_bar(bar(L::B_FIN), ku & 1, wc));
+      mbar_arrive(bar(L::B_EPI));  // this unit's commit has been seen
       tc_fence_after();
       if (ok) {  // warp-uniform: every lane takes part in the TMEM reads
         const bool dv_side = half == 0;
@@ -734,8 +801,37 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         // read it, has completed); then each store writes 4 whole rows.
         const uint32_t stg = pbuf + q4 * 4096;
         p_rows_free();
+        // Half of a split unit: the first half to finish (order 0) parks its
+        // fp32 rows in the unit's slot and raises the slot's ready flag; the
+        // second (order 1) adds them to its own and writes the unit's rows.
+        int order = -1;
+        float* prow = nullptr;  // this thread's row in the slot
+        int* ready = nullptr;
+        if (uh >= 0) {
+          const int slot = u - last0;
+          ready = p.part_cnt + p.nslot + slot;
+          prow = p.part + (static_cast<size_t>(slot) * 2 + (dv_side ? 0 : 1)) * kTile * D +
+                 static_cast<size_t>(r) * D;
+          volatile int* sorder = reinterpret_cast<volatile int*>(smem + L::MISC + 8);
+          if (threadIdx.x == 128) *sorder = atomicAdd(p.part_cnt + slot, 1);
+          mbar_arrive(bar(L::B_SPL));  // phase 0: the order is published
+          ok = __all_sync(0xffffffffu, wait_bar(bar(L::B_SPL), 0, wc));
+          order = *sorder;
+          if (ok && order == 1) {  // the other half's rows are in the slot
+            bool seen = false;
+            const uint64_t t0 = global_ns();
+            while (!(seen = ld_acquire_gpu(ready) != 0) && !*wc.abort &&
+                   global_ns() - t0 <= wc.limit_ns) {
+            }
+            if (!seen) {
+              *wc.abort = 1;
+              atomicCAS(wc.err, kDevOk, kDevTimeout);
+            }
+            ok = __all_sync(0xffffffffu, seen);
+          }
+        }
 #pragma unroll 1
-        for (int c = 0; c < D / 64; ++c) {
+        for (int c = 0; ok && c < D / 64; ++c) {
           uint32_t a[2][32];
           if (nu > 0) {
             tmem_ld32(tmem + lane_off + tcol + 64 * c, a[0]);
@@ -746,6 +842,28 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           } else {
 #pragma unroll
             for (int j = 0; j < 32; ++j) a[0][j] = a[1][j] = 0u;
+          }
+          if (order == 0) {  // park 64 columns of this row, no output
+            float4* pr = reinterpret_cast<float4*>(prow + 64 * c);
+#pragma unroll
+            for (int v = 0; v < 16; ++v)
+              pr[v] = make_float4(__uint_as_float(a[v >> 3][4 * (v & 7)]),
+                                  __uint_as_float(a[v >> 3][4 * (v & 7) + 1]),
+                                  __uint_as_float(a[v >> 3][4 * (v & 7) + 2]),
+                                  __uint_as_float(a[v >> 3][4 * (v & 7) + 3]));
+            continue;
+          }
+          if (order == 1) {  // add the parked half
+            const float4* pr = reinterpret_cast<const float4*>(prow + 64 * c);
+#pragma unroll
+            for (int v = 0; v < 16; ++v) {
+              const float4 o = __ldcg(pr + v);
+              uint32_t* x = &a[v >> 3][4 * (v & 7)];
+              x[0] = __float_as_uint(__uint_as_float(x[0]) + o.x);
+              x[1] = __float_as_uint(__uint_as_float(x[1]) + o.y);
+              x[2] = __float_as_uint(__uint_as_float(x[2]) + o.z);
+              x[3] = __float_as_uint(__uint_as_float(x[3]) + o.w);
+            }
           }
 #pragma unroll
           for (int v = 0; v < 8; ++v) {
@@ -766,11 +884,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           }
           __syncwarp();
         }
+        if (ok && order == 0) {  // phase 1: every row parked, then the flag
+          mbar_arrive(bar(L::B_SPL));
+          if (threadIdx.x == 128) {
+            if (wait_bar(bar(L::B_SPL), 1, wc)) {
+              __threadfence();
+              st_release_gpu(ready, 1);
+            }
+          }
+        }
       }
       tc_fence_before();
       ++ku;
       kc = k_n;
       u = u_n;
+      uh = uh_n;
+      cur = cur_n;
       un = un_n;
       sch = sch_n;
       qt = qt_u;

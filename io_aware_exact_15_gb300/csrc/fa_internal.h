@@ -86,6 +86,14 @@ struct BwdParams {
   int total = 0;
   DropoutParams drop;
   int skip_dq = 0;  // 1: no dQ product (dQ comes from the query-tile pass)
+  // Split last round: when the last round of units fills at most half the
+  // grid, each of its units runs as two halves of its query tiles; the first
+  // half to finish parks its fp32 dV, dK ([2][128][d] per slot) in part, the
+  // second adds them to its own.  part_cnt: [nslot] arrival counts then
+  // [nslot] ready flags, zero on entry.  Null / 0: no split.
+  float* part = nullptr;
+  int* part_cnt = nullptr;
+  int nslot = 0;
   int* err = nullptr;
   uint64_t wait_ns = 0;
 };
@@ -129,6 +137,7 @@ cudaError_t launch_backward_dq(const DqParams& p, const CUtensorMap& tq, const C
                                cudaStream_t stream);
 
 cudaError_t launch_bwd_preprocess(const void* o, const void* dO, float* delta, float* dq_acc,
+                                  int* zero_i, long long nzero,
                                   long long rows, int d, cudaStream_t stream);
 cudaError_t launch_dq_convert(const float* dq_acc, void* dq, long long n, float scale,
                               cudaStream_t stream);

@@ -123,6 +123,16 @@ FA_DEV void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memo
 FA_DEV void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 // this thread's bulk groups have completed
 FA_DEV void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// release store / acquire load at GPU scope (flags between CTAs)
+FA_DEV void st_release_gpu(int* p, int v) {
+  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+FA_DEV int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
 // generic-proxy shared-memory writes -> visible to the async proxy (MMA/TMA)
 FA_DEV void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 

@@ -48,6 +48,14 @@ def test_workspace_sizes():
     w1 = fa.fa_backward_workspace_size(1, 1, 4096, 128)
     w2 = fa.fa_backward_workspace_size(1, 1, 8192, 128)
     assert abs(w2 - 2 * w1) <= 512
+    # d = 128 beyond 64 key tiles: min(tiles / 2, 96) split slots of two
+    # 128 x d fp32 partial sums and two int counters each
+    for (B, H, N), ns in (((2, 8, 2048), 96), ((1, 5, 2048), 40), ((1, 4, 2048), 0)):
+        rows = B * H * N
+        assert fa.fa_backward_workspace_size(B, H, N, 128) == \
+            a256(4 * rows) + a256(4 * rows * 128) + a256(ns * 2 * 128 * 128 * 4) + a256(8 * ns)
+    rows = 2 * 8 * 2048
+    assert fa.fa_backward_workspace_size(2, 8, 2048, 64) == a256(4 * rows) + a256(4 * rows * 64)
 
 
 ALIGNED = 1 << 20          # fake, never dereferenced: every case fails validation first

@@ -85,3 +85,30 @@ def test_gqa_long_sequence_sampled_rows():
     parity.check_grad(dq[:, :, rows], dq_r, "dQ", "gqa 2k")
     parity.check_grad(dk[:, :, rows], dk_r, "dK", "gqa 2k")
     parity.check_grad(dv[:, :, rows], dv_r, "dV", "gqa 2k")
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_gqa_split_last_round_sampled_rows(causal):
+    # 2 x 4 key/value heads x 20 key tiles = 160 units on the 152-SM grid:
+    # dense, the 8 units of the last round (4 x 20 steps each) run as two
+    # halves each (the d = 128 kernel; d = 64 never splits); causal ones
+    # (4 steps) do not split.  The key rows checked
+    # include every row of the key tiles those units own
+    dev = device()
+    B, H, Hkv, N, d = 2, 16, 4, 2560, 128
+    q, k, v, do = make(B, H, Hkv, N, d, seed=31 + causal)
+    scale = 1.0 / d ** 0.5
+    o, lse, dq, dk, dv = run(q, k, v, do, scale, causal, dev)
+    # last-round units: causal walks key tile 19 of every head first-to-last
+    # (units 152..159 are (kt 19, heads 0..7)); dense ones are key tiles 12..19
+    # of the last key/value head
+    last = list(range(19 * 128, 20 * 128)) if causal else list(range(12 * 128, 13 * 128))
+    krows = np.unique(np.concatenate([np.array(last), W.sample_rows(N, 64, seed=5)]))
+    qrows = W.sample_rows(N, 64, seed=6)
+    f = parity.f64
+    dq_r, dk_r, dv_r = oracle.backward(f(q), f(k), f(v), f(do), scale, causal=causal, qrows=qrows,
+                                       krows=krows)
+    what = f"gqa split causal={causal}"
+    parity.check_grad(dq[:, :, qrows], dq_r, "dQ", what)
+    parity.check_grad(dk[:, :, krows], dk_r, "dK", what)
+    parity.check_grad(dv[:, :, krows], dv_r, "dV", what)
