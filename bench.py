@@ -54,6 +54,23 @@ def kernel_source_hash(files):
     return h.hexdigest()[:12]
 
 
+def max_over_ranks(x, dist, device):
+    """The largest x over all ranks (x itself on one rank): the job's time is
+    that of its slowest rank."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(world, flops_per_rank_step, ms_per_step):
+    """Whole-job throughput: every rank runs its own replica of the step
+    (weak scaling), all of them within the slowest rank's step time."""
+    return world * flops_per_rank_step / (ms_per_step * 1e-3) / 1e12
+
+
 def ncu_traffic(kernel_key, src_hash):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
     on the current kernel source; else None."""
@@ -354,12 +371,8 @@ def run_gpu(args, rank, world, dist):
     conv_ms = statistics.fmean(p[3] for p in per)
     if combined:  # p[2] bracketed preprocess + main (+ dQ pass or convert)
         main_ms = main_ms - pre_ms - (0.0 if det else conv_ms)
-    ms_max = ms
-    if dist is not None:
-        t = torch.tensor([ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_max = float(t.item())
-    value = world * fb / (ms_max * 1e-3) / 1e12
+    ms_max = max_over_ranks(ms, dist, dev)
+    value = whole_job_tflops(world, fb, ms_max)
 
     # end to end through the public API with host buffers (pinned)
     hin, hiv = packed(in_specs, pin=True)
@@ -434,11 +447,8 @@ def run_gpu(args, rank, world, dist):
     b2.record(stream)
     torch.cuda.synchronize(dev)
     ems_serial = a2.elapsed_time(b2) / Ke
-    if dist is not None:
-        t = torch.tensor([ems], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ems = float(t.item())
-    e2e = {"value": round(world * fb / (ems * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+    ems = max_over_ranks(ems, dist, dev)
+    e2e = {"value": round(whole_job_tflops(world, fb, ems), 3), "unit": "TFLOP/s",
            "ms_per_step": round(ems, 4), "h2d_bytes_per_step": int(h2d),
            "d2h_bytes_per_step": int(d2h),
            "path": "per step: one pinned host -> device copy of the packed inputs (q, k, v, dO), "

@@ -112,3 +112,24 @@ def test_gqa_split_last_round_sampled_rows(causal):
     parity.check_grad(dq[:, :, qrows], dq_r, "dQ", what)
     parity.check_grad(dk[:, :, krows], dk_r, "dK", what)
     parity.check_grad(dv[:, :, krows], dv_r, "dV", what)
+
+
+def test_gqa_causal_split_last_round_eight_heads_per_group():
+    # 4 x 2 key/value heads x 20 key tiles = 160 units, causal, 8 query heads
+    # per key/value head: the last round holds the 8 diagonal units of key
+    # tile 19, 8 steps each (one per query head), which run as two halves of
+    # 4 steps on two CTAs.  Every row of key tile 19 is checked.
+    dev = device()
+    B, H, Hkv, N, d = 4, 16, 2, 2560, 128
+    q, k, v, do = make(B, H, Hkv, N, d, seed=77)
+    scale = 1.0 / d ** 0.5
+    o, lse, dq, dk, dv = run(q, k, v, do, scale, True, dev)
+    krows = np.unique(np.concatenate([np.arange(19 * 128, 20 * 128), W.sample_rows(N, 32, seed=8)]))
+    qrows = W.sample_rows(N, 48, seed=9)
+    f = parity.f64
+    dq_r, dk_r, dv_r = oracle.backward(f(q), f(k), f(v), f(do), scale, causal=True, qrows=qrows,
+                                       krows=krows)
+    what = "gqa causal split, 8 heads per group"
+    parity.check_grad(dq[:, :, qrows], dq_r, "dQ", what)
+    parity.check_grad(dk[:, :, krows], dk_r, "dK", what)
+    parity.check_grad(dv[:, :, krows], dv_r, "dV", what)
