@@ -558,14 +558,20 @@ def cpu_baseline(w, budget_s=12.0):
     sample, total, per_unit = oracle_job(w)
     nthreads = os.cpu_count() or 1
     n = calibrate_units(sample, total, nthreads, budget_s)
+    passes = 1
+    if n >= total:  # the whole workload takes less than the budget: repeat it
+        t0 = time.perf_counter()
+        sample(n, nthreads)
+        passes = max(1, int(budget_s / max(time.perf_counter() - t0, 1e-3)))
     t0 = time.perf_counter()
-    sample(n, nthreads)
+    for _ in range(passes):
+        sample(n, nthreads)
     dt = time.perf_counter() - t0
     unit = "heads of the packed batch" if w.varlen else "(batch, head) slices"
-    return {"value": round(per_unit * n / dt / 1e12, 9), "unit": "TFLOP/s",
+    return {"value": round(per_unit * n * passes / dt / 1e12, 9), "unit": "TFLOP/s",
             "cores": nthreads, "kind": "oracle",
             "sample": f"fp64 C oracle forward+backward on {n} of {total} {unit} "
-                      f"of {w.name}, {dt:.2f} s wall"}
+                      f"of {w.name}, {passes} pass(es), {dt:.2f} s wall"}
 
 
 def run_reference(args, rank, world):
