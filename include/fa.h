@@ -101,7 +101,11 @@ fa_status fa_backward_preprocess(const void* o, const void* dO, int B, int H, in
 
 /* Backward step 2: the fused recompute kernel.  Reads D from the workspace,
  * writes dk and dv, and adds unscaled dS K into the workspace's dQ
- * accumulator. */
+ * accumulator.  Run it once after each fa_backward_preprocess of the same
+ * problem on the same workspace: the preprocess also clears the counters
+ * with which split key tiles of the last round hand over their partial
+ * dK, dV sums, and a second run on the same workspace would find them
+ * used. */
 fa_status fa_backward_main(const void* q, const void* k, const void* v, const void* dO,
                            const float* lse, void* dk, void* dv, int B, int H, int N, int d,
                            float scale, int causal, void* workspace, size_t workspace_bytes,
