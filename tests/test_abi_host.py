@@ -58,6 +58,20 @@ def test_workspace_sizes():
     assert fa.fa_backward_workspace_size(2, 8, 2048, 64) == a256(4 * rows) + a256(4 * rows * 64)
 
 
+def test_noalloc_scratch_row_limits():
+    """The scratch of fa_backward_noalloc (32 MiB) holds the workspace of
+    about 129k rows B*H*N at d = 64 and about 40k at d = 128 (whose
+    workspace adds the split last round's partial sums): the largest N, in
+    steps of one 128-row tile, of a single head whose workspace fits."""
+    def max_rows(d):
+        n = 128
+        while fa.fa_backward_workspace_size(1, 1, n + 128, d) <= 32 << 20:
+            n += 128
+        return n
+    assert 125_000 <= max_rows(64) <= 131_072
+    assert 39_000 <= max_rows(128) <= 41_000
+
+
 ALIGNED = 1 << 20          # fake, never dereferenced: every case fails validation first
 MIS = ALIGNED + 8
 
