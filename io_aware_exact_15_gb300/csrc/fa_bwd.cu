@@ -181,14 +181,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   // causal, whose last units are the diagonal key tiles): a shorter half
   // pays the unit boundary and the hand-off for too little work (measured:
   // B8 H16 N512 d64, 4-step units, 54 -> 60 us).  Compiled for d = 128
-  // with its dQ product only: in the d = 64 kernel the mere run-time option
-  // cost the B8 H16 N512 backward 52 -> 57 us, though it never split there,
-  // and the key-tile pass of the deterministic backward (no dQ) never
-  // splits either.
+  // only: in the d = 64 kernel the mere run-time option cost the B8 H16
+  // N512 backward 52 -> 57 us, though it never split there.
   const int nround = (nunits + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x);
   const int last0 = (nround - 1) * static_cast<int>(gridDim.x);  // first unit of the last round
   const int mlast = nunits - last0;
-  const bool split = D == 128 && DQ && p.part != nullptr && p.lists.col_ptr == nullptr && !varlen && nround > 1 &&
+  const bool split = D == 128 && p.part != nullptr && p.lists.col_ptr == nullptr && !varlen && nround > 1 &&
                      2 * mlast <= static_cast<int>(gridDim.x) && mlast <= p.nslot &&
                      G * (p.causal ? 1 : ntmax) >= 8;
   // k-th item of this CTA: unit u and half uh (-1: the whole unit); false
