@@ -3,15 +3,18 @@
 One step = the whole hot path over one batch: fa_forward (tile schedule,
 TMA loads, S = QK^T, mask, online softmax, O += PV, epilogue) then the
 backward (preprocess, recompute kernel, dQ conversion), all through the C
-ABI.  Default workload: BERT-large-shaped self-attention, B=8 H=16 N=512
-d=64, non-causal, bf16 inputs drawn N(0,1) from a seeded generator.
+ABI.  Default workload: the largest single-GPU shape of the long-sequence
+sweep, B=1 H=16 N=16384 d=128, non-causal (the long-range workload's shape
+without its causal mask), bf16 inputs drawn N(0,1) from a seeded generator
+with 1% of the keys scaled by 8.  --workload bert_large times the
+BERT-large-shaped step (B=8 H=16 N=512 d=64).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
     python bench.py --impl reference ...   # the fp64 CPU oracle, timed
 
-Inputs of this workload (~34 MB) fit in L2, so L2 is flushed (a 256 MiB
-device write) before every timed step; the flush is outside the per-step
-CUDA events.  Under torchrun every rank runs its own replica (weak
+L2 is flushed (a 256 MiB device write) before every timed step, outside the
+per-step CUDA events; the default workload's inputs (268 MB) are also larger
+than L2, the BERT-shaped ones (34 MB) are not.  Under torchrun every rank runs its own replica (weak
 scaling); the reported time is the max over ranks.
 """
 from __future__ import annotations
@@ -30,6 +33,7 @@ import types
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
+DEFAULT_WORKLOAD = "longseq_dense_n16384_d128"
 METRIC = "attention TFLOP/s fwd and fwd+bwd (bf16, 1×GB300) and % of dense BF16 peak"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -52,6 +56,16 @@ def kernel_source_hash(files):
         with open(os.path.join(ROOT, "io_aware_exact_15_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:12]
+
+
+def bwd_compulsory_bytes(rows_q, rows_kv, d, deterministic=False):
+    """Bytes the backward main kernel must move at least once: Q, dO (bf16)
+    and lse, D (fp32) per query row; K, V read and dK, dV written (bf16) per
+    key/value row; the fp32 dQ accumulator read and written once per query
+    row (the deterministic pass writes bf16 dQ instead)."""
+    per_q = 2 * d * 2 + 2 * 4 + (2 * d if deterministic else 2 * 4 * d)
+    per_kv = 2 * d * 2 + 2 * d * 2
+    return int(rows_q * per_q + rows_kv * per_kv)
 
 
 def max_over_ranks(x, dist, device):
@@ -461,6 +475,10 @@ def run_gpu(args, rank, world, dist):
     main_flops = 2.5 * ff
     achieved = main_flops / (main_ms * 1e-3) / 1e12
     peak = peaks["bf16_tflops"]
+    traffic = ncu_traffic(f"fa_bwd_kernel:{args.workload}", src_hash)
+    rows_q = H * T if varlen else B * H * N
+    rows_kv = Hkv * T if varlen else B * Hkv * N
+    comp = bwd_compulsory_bytes(rows_q, rows_kv, d, det)
     kname = ("fa_bwd_kernel without dQ + fa_bwd_dq_kernel (deterministic backward; algorithmic "
              "FLOPs count the five products once)" if det else
              "fa_bwd_kernel (recompute: S, dP, dV, dK, dQ MMAs)")
@@ -468,13 +486,25 @@ def run_gpu(args, rank, world, dist):
                 "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
                 "frac": round(achieved / peak, 4),
                 "peak_source": f"{peaks['source']} bf16 burst",
-                "traffic": ncu_traffic(f"fa_bwd_kernel:{args.workload}", src_hash),
+                "traffic": traffic,
+                "hbm": {"compulsory_bytes": comp,
+                        "compulsory_gbs": round(comp / (main_ms * 1e-3) / 1e9, 1),
+                        "traffic_gbs": (round(traffic / (main_ms * 1e-3) / 1e9, 1)
+                                        if traffic else None),
+                        "peak_gbs": peaks["hbm_gbs"],
+                        "what": "inputs read once and outputs written once (Q, K, V, dO, lse, "
+                                "D, dK, dV; the fp32 dQ accumulator read and written once), "
+                                "and the ncu DRAM bytes, per launch over avg_launch_ms"},
                 "main_time": ("deterministic backward minus the separately timed preprocess: "
                               "key-tile pass + query-tile dQ pass together" if det else
                               "combined backward minus separately timed preprocess and convert"
                               if combined else "CUDA events around the kernel's launch"),
                 "algorithmic_flops_per_launch": main_flops,
-                "avg_launch_ms": round(main_ms, 5)}
+                "avg_launch_ms": round(main_ms, 5),
+                "timing_note": "per-kernel events sit between launches and stop programmatic "
+                               "dependent launch from overlapping a kernel with its neighbours: "
+                               "avg_launch_ms is an upper bound on the kernel's time inside "
+                               "the unsplit step, so frac is a lower bound"}
     fwd_tf = ff / (fwd_ms * 1e-3) / 1e12
     result = {
         "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world,
@@ -542,7 +572,8 @@ def oracle_job(w):
 
 
 def calibrate_units(sample, total, nthreads, budget_s):
-    """Units whose oracle forward + backward take about budget_s seconds."""
+    """Units whose oracle forward + backward take about budget_s seconds, and
+    the last calibration run (units, seconds)."""
     n = 1
     while True:
         t0 = time.perf_counter()
@@ -551,27 +582,45 @@ def calibrate_units(sample, total, nthreads, budget_s):
         if n >= total or dt >= 0.2 * budget_s:
             break
         n = min(total, n * 4)
-    return max(1, min(total, int(n * budget_s / max(dt, 1e-3))))
+    return max(1, min(total, int(n * budget_s / max(dt, 1e-3)))), (n, dt)
 
 
-def cpu_baseline(w, budget_s=12.0):
+def cpu_baseline(w, budget_s=12.0, single_thread_s=4.0):
+    """The oracle on all host threads over a sample of the workload, and on
+    one thread over a sample of the BERT-large-shaped workload."""
+    import fa_workloads as W
     sample, total, per_unit = oracle_job(w)
     nthreads = os.cpu_count() or 1
-    n = calibrate_units(sample, total, nthreads, budget_s)
+    n, (n_cal, dt_cal) = calibrate_units(sample, total, nthreads, budget_s)
     passes = 1
-    if n >= total:  # the whole workload takes less than the budget: repeat it
+    if n == n_cal and dt_cal >= 0.5 * budget_s:
+        dt = dt_cal  # one unit already takes the budget: keep that run
+    else:
+        if n >= total:  # the whole workload takes less than the budget: repeat it
+            t0 = time.perf_counter()
+            sample(n, nthreads)
+            passes = max(1, int(budget_s / max(time.perf_counter() - t0, 1e-3)))
         t0 = time.perf_counter()
-        sample(n, nthreads)
-        passes = max(1, int(budget_s / max(time.perf_counter() - t0, 1e-3)))
-    t0 = time.perf_counter()
-    for _ in range(passes):
-        sample(n, nthreads)
-    dt = time.perf_counter() - t0
+        for _ in range(passes):
+            sample(n, nthreads)
+        dt = time.perf_counter() - t0
     unit = "heads of the packed batch" if w.varlen else "(batch, head) slices"
-    return {"value": round(per_unit * n * passes / dt / 1e12, 9), "unit": "TFLOP/s",
-            "cores": nthreads, "kind": "oracle",
-            "sample": f"fp64 C oracle forward+backward on {n} of {total} {unit} "
-                      f"of {w.name}, {passes} pass(es), {dt:.2f} s wall"}
+    out = {"value": round(per_unit * n * passes / dt / 1e12, 9), "unit": "TFLOP/s",
+           "cores": nthreads, "kind": "oracle",
+           "sample": f"fp64 C oracle forward+backward on {n} of {total} {unit} "
+                     f"of {w.name}, {passes} pass(es), {dt:.2f} s wall"}
+    wb = W.WORKLOADS["bert_large"]
+    s1, total1, per1 = oracle_job(wb)
+    n1, (nc1, dc1) = calibrate_units(s1, total1, 1, single_thread_s)
+    t0 = time.perf_counter()
+    s1(n1, 1)
+    d1 = time.perf_counter() - t0
+    out["single_thread"] = {
+        "value": round(per1 * n1 / d1 / 1e12, 9), "unit": "TFLOP/s", "cores": 1,
+        "workload": wb.name,
+        "sample": f"fp64 C oracle forward+backward on {n1} of {total1} (batch, head) slices "
+                  f"of {wb.name} on one thread, {d1:.2f} s wall"}
+    return out
 
 
 def run_reference(args, rank, world):
@@ -584,7 +633,7 @@ def run_reference(args, rank, world):
     sample, total, per_unit = oracle_job(w)
     nthreads = os.cpu_count() or 1
     per_step_budget = max(1.0, 150.0 / max(1, args.steps + args.warmup))
-    n = calibrate_units(sample, total, nthreads, per_step_budget)
+    n, _ = calibrate_units(sample, total, nthreads, per_step_budget)
     for _ in range(args.warmup):
         sample(n, nthreads)
     times = []
@@ -661,21 +710,70 @@ def run_tile_sweep(args):
         raise RuntimeError("device status after the sweep")
 
 
+def run_host_overhead(args, calls=200, batches=10):
+    """Host time of one C-ABI call (argument checks, cached tensor maps,
+    launches), measured around the raw ctypes calls on a problem small
+    enough that the GPU keeps up; a host-only library call gives the floor
+    of the ctypes call itself."""
+    import torch
+
+    import io_aware_exact_15_gb300 as fa
+
+    lib = fa.load()
+    dev = torch.device("cuda", 0)
+    out = {}
+    for (B, H, N, d) in ((1, 1, 128, 64), (8, 16, 512, 64)):
+        q, k, v, o, do, dq, dk, dv = (torch.zeros((B, H, N, d), dtype=torch.bfloat16, device=dev)
+                                      for _ in range(8))
+        lse = torch.zeros((B, H, N), dtype=torch.float32, device=dev)
+        nb = fa.fa_backward_workspace_size(B, H, N, d)
+        ws = torch.empty(nb, dtype=torch.uint8, device=dev)
+        s_ = torch.cuda.current_stream().cuda_stream
+        p = lambda t: t.data_ptr()
+        fargs = (p(q), p(k), p(v), p(o), p(lse), B, H, N, d, 0.125, 0, s_)
+        bargs = (p(q), p(k), p(v), p(o), p(do), p(lse), p(dq), p(dk), p(dv), B, H, N, d, 0.125, 0,
+                 p(ws), nb, s_)
+        cases = {"fa_forward": (lib.fa_forward, fargs), "fa_backward": (lib.fa_backward, bargs),
+                 "ctypes_floor": (lib.fa_backward_workspace_size, (B, H, N, d))}
+        res = {}
+        for name, (fn, a) in cases.items():
+            for _ in range(20):
+                fn(*a)
+            torch.cuda.synchronize()
+            tot = 0.0
+            for _ in range(batches):
+                t0 = time.perf_counter()
+                for _ in range(calls):
+                    fn(*a)
+                tot += time.perf_counter() - t0
+                torch.cuda.synchronize()
+            res[name] = round(1e6 * tot / (calls * batches), 2)
+        out[f"B{B} H{H} N{N} d{d}"] = res
+    if fa.fa_get_device_status() != fa.FA_OK:
+        raise RuntimeError("device status after the host-overhead loop")
+    print(json.dumps({"host_us_per_call": out}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=3000)
-    ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--workload", default="bert_large")
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--deterministic", action="store_true",
                     help="time fa_backward_deterministic instead of fa_backward")
     ap.add_argument("--tile-sweep", action="store_true",
                     help="time the forward per tile configuration (block-size experiment)")
+    ap.add_argument("--host-overhead", action="store_true",
+                    help="time the host side of one fa_forward / fa_backward call")
     args = ap.parse_args()
     if args.tile_sweep:
         run_tile_sweep(args)
+        return
+    if args.host_overhead:
+        run_host_overhead(args)
         return
     if args.warmup < 3:
         args.warmup = 3

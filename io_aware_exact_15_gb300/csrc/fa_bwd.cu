@@ -923,17 +923,16 @@ cudaError_t launch_bwd_d(const BwdParams& p, const CUtensorMap& tq, const CUtens
                          const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq,
                          cudaStream_t stream) {
   using L = BwdSmem<D>;
-  cudaError_t e = cudaFuncSetAttribute(fa_bwd_kernel<D, KIND, DQ>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
+  static std::atomic<unsigned long long> attr_done{0};
+  cudaError_t e = smem_attr_once(
+      attr_done, reinterpret_cast<const void*>(fa_bwd_kernel<D, KIND, DQ>), L::ALLOC);
   if (e != cudaSuccess) return e;
   const int nT = (p.N + kTile - 1) / kTile;
   const long long units = static_cast<long long>(nT) * p.B * (p.Hkv > 0 ? p.Hkv : p.H);
   // persistent: one CTA per SM (the CTA holds the SM's TMEM and most of its
   // shared memory), each walking units blockIdx.x, blockIdx.x + grid, ...
-  int dev = 0, sms = 0;
-  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
-    return e;
+  const int sms = sm_count();
+  if (sms <= 0) return cudaErrorInvalidDevice;
   const long long ctas = units < sms ? units : sms;
   return launch_pdl(fa_bwd_kernel<D, KIND, DQ>, dim3(static_cast<unsigned>(ctas)),
                     dim3(kBwdThreads), L::ALLOC, stream, tq, tk, tv, tdo, tdq, p);

@@ -385,8 +385,9 @@ template <int D>
 cudaError_t launch_dq_d(const DqParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                         const CUtensorMap& tv, const CUtensorMap& tdo, cudaStream_t stream) {
   using L = DqSmem<D>;
-  cudaError_t e = cudaFuncSetAttribute(fa_bwd_dq_kernel<D>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
+  static std::atomic<unsigned long long> attr_done{0};
+  cudaError_t e =
+      smem_attr_once(attr_done, reinterpret_cast<const void*>(fa_bwd_dq_kernel<D>), L::ALLOC);
   if (e != cudaSuccess) return e;
   const int nT = (p.N + kTile - 1) / kTile;
   const long long ctas = static_cast<long long>(nT) * p.B * p.H;

@@ -476,8 +476,9 @@ template <int D, int KIND, int NS_ = 0>
 cudaError_t launch_fwd_d(const FwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                          const CUtensorMap& tv, cudaStream_t stream) {
   using L = FwdSmem<D, NS_>;
-  cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<D, KIND, NS_>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
+  static std::atomic<unsigned long long> attr_done{0};
+  cudaError_t e = smem_attr_once(
+      attr_done, reinterpret_cast<const void*>(fa_fwd_kernel<D, KIND, NS_>), L::ALLOC);
   if (e != cudaSuccess) return e;
   const int nT = (p.N + kTile - 1) / kTile;
   const int npairs = (NS_ != 0 && p.single_tile) ? nT : (nT + 1) / 2;

@@ -5,7 +5,39 @@
 #include <cuda_runtime_api.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace fa {
+
+// Dynamic shared memory above 48 KB has to be allowed per kernel, in each
+// device's context.  `done` is the kernel's own record, one bit per device
+// already set up; a device index of 64 or more is set up on every launch.
+inline cudaError_t smem_attr_once(std::atomic<unsigned long long>& done, const void* kernel,
+                                  int bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = dev < 64 ? 1ull << dev : 0ull;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
+
+// SM count of the current device, read once per device (0 on error).
+inline int sm_count() {
+  static std::atomic<int> cached[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev < 64) {
+    const int c = cached[dev].load(std::memory_order_relaxed);
+    if (c > 0) return c;
+  }
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  if (dev < 64) cached[dev].store(sms, std::memory_order_relaxed);
+  return sms;
+}
 
 // Launch with programmatic stream serialization (the kernel starts with
 // grid_dep_wait, see fa_ptx.cuh), so that its scheduling overlaps the tail of

@@ -88,3 +88,60 @@ def keep_scale(p):
     """1 / (1 - p') of dropout probability p (p' = rint(256 p) / 256)."""
     t = int(np.rint(256.0 * float(np.float32(p))))
     return 256.0 / (256 - t)
+
+
+# ------------------------------------------------------------------ row and head samples
+ORACLE_BUDGET = 2.0e11  # oracle flops per shape for the backward's heads
+
+
+def check_rows(N, seed):
+    """256 seeded rows and one seeded row in every 128-row tile (sorted,
+    distinct), so that every query and key tile of a head is represented."""
+    import fa_workloads as W
+    rows = set(W.sample_rows(N, 256, seed).tolist())
+    rng = np.random.default_rng(seed)
+    for t in range((N + 127) // 128):
+        lo, hi = 128 * t, min(N, 128 * t + 128)
+        rows.add(int(rng.integers(lo, hi)))
+    return np.array(sorted(rows), dtype=np.int64)
+
+
+def last_round_heads(B, H, N, causal, sms, Hkv=None):
+    """(batch, key/value head) pairs holding a unit of the persistent
+    backward's last round: one CTA per SM takes units blockIdx.x,
+    blockIdx.x + grid, ...; a unit is one key/value head x one key tile,
+    numbered head-major (dense) or key-tile-major (causal)."""
+    Hk = H if Hkv is None else Hkv
+    nT = (N + 127) // 128
+    BH = B * Hk
+    units = BH * nT
+    grid = min(units, sms)
+    rounds = (units + grid - 1) // grid
+    first = (rounds - 1) * grid
+    bhs = sorted({(u // nT) if not causal else (u % BH) for u in range(first, units)})
+    return [divmod(bh, Hk) for bh in bhs]
+
+
+def backward_heads(w, sms, budget=ORACLE_BUDGET):
+    """Heads on which a backward is compared with the oracle: all of them
+    when their oracle cost (4 N^2 d flops per head, half when causal) fits
+    `budget`, else that many: the first and last head, the first and last
+    head of the backward's last round, and seeded others."""
+    B, H, N, d = w.B, w.H, w.N, w.d
+    per_head = 4.0 * N * N * d / (2 if w.causal else 1)
+    n = int(min(B * H, max(4, budget // per_head)))
+    if n >= B * H:
+        return [(b, h) for b in range(B) for h in range(H)]
+    last = last_round_heads(B, H, N, w.causal, sms)
+    heads = []
+    for x in [(0, 0), (B - 1, H - 1), last[0], last[-1]]:
+        if x not in heads:
+            heads.append(x)
+    rng = np.random.default_rng(w.seed + N + d)
+    for bh in rng.permutation(B * H):
+        if len(heads) >= n:
+            break
+        x = divmod(int(bh), H)
+        if x not in heads:
+            heads.append(x)
+    return sorted(heads)

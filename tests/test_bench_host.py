@@ -15,13 +15,16 @@ import fa_workloads as W  # noqa: E402
 
 
 def test_cpu_baseline_object_on_a_short_budget():
-    r = bench.cpu_baseline(W.WORKLOADS["single_head_fwd"], budget_s=0.5)
-    assert set(r) == {"value", "unit", "cores", "kind", "sample"}
+    r = bench.cpu_baseline(W.WORKLOADS["single_head_fwd"], budget_s=0.5, single_thread_s=0.3)
+    assert set(r) == {"value", "unit", "cores", "kind", "sample", "single_thread"}
     assert r["kind"] == "oracle" and r["unit"] == "TFLOP/s"
     assert r["cores"] == (os.cpu_count() or 1)
     assert r["value"] > 0
     # one slice, finished well inside the budget: repeated whole passes
     assert "1 of 1" in r["sample"] and "pass(es)" in r["sample"]
+    st = r["single_thread"]
+    assert st["cores"] == 1 and st["value"] > 0 and st["workload"] == "bert_large"
+    assert "of 128 (batch, head) slices of bert_large on one thread" in st["sample"]
 
 
 def test_calibration_stays_within_the_workload():
@@ -30,8 +33,21 @@ def test_calibration_stays_within_the_workload():
     def sample(n, nthreads):
         calls.append(n)
 
-    n = bench.calibrate_units(sample, 7, 1, 0.05)
+    n, (n_last, dt_last) = bench.calibrate_units(sample, 7, 1, 0.05)
     assert 1 <= n <= 7 and all(1 <= c <= 7 for c in calls)
+    assert n_last == calls[-1] and dt_last >= 0
+
+
+def test_compulsory_bytes_of_the_backward():
+    # B1 H16 N16384 d128: Q, dO, K, V read, dK, dV written (bf16), lse and
+    # D read (fp32), the fp32 dQ accumulator read and written once
+    rows = 16 * 16384
+    got = bench.bwd_compulsory_bytes(rows, rows, 128)
+    assert got == rows * (6 * 128 * 2 + 2 * 4 + 2 * 4 * 128)
+    # grouped K/V: key/value rows are a quarter of the query rows
+    assert bench.bwd_compulsory_bytes(rows, rows // 4, 128) < got
+    # the deterministic pass writes bf16 dQ instead of touching fp32
+    assert bench.bwd_compulsory_bytes(rows, rows, 128, True) < got
 
 
 def test_traffic_record_needs_the_current_kernel_source():

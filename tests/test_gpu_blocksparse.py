@@ -70,20 +70,21 @@ def test_blocksparse_all_ones_equals_dense():
 
 
 def test_blocksparse_64k_sampled_rows():
+    # every head, 256 seeded rows plus one row in each of the 512 tiles (the
+    # oracle's per-head cost is the sparse forward statistics, ~5.7 % of
+    # the dense 4 N^2 d)
     dev = device()
     w = W.WORKLOADS["blocksparse_64k"]
     q, k, v, do, mask = W.make_inputs(w)
     o, lse, dq, dk, dv = run_sparse(q, k, v, do, w.scale, w.causal, mask, dev)
-    rows = W.sample_rows(w.N, 256, seed=w.seed + 29)
+    rows = parity.check_rows(w.N, seed=w.seed + 29)
     o_ref, lse_ref = parity.oracle_forward(q, k, v, w.scale, w.causal, mask=mask, rows=rows)
     parity.check_forward(o[:, :, rows], lse[:, :, rows], o_ref, lse_ref, "blocksparse_64k")
-    heads = [(0, 0), (0, w.H - 1)]
     dq_r, dk_r, dv_r = parity.oracle_backward(q, k, v, do, w.scale, w.causal, mask=mask,
-                                              qrows=rows, krows=rows, heads=heads)
-    sel = lambda t: torch.stack([t[b, h] for (b, h) in heads])[None][:, :, rows]
-    parity.check_grad(sel(dq), dq_r, "dQ", "blocksparse_64k")
-    parity.check_grad(sel(dk), dk_r, "dK", "blocksparse_64k")
-    parity.check_grad(sel(dv), dv_r, "dV", "blocksparse_64k")
+                                              qrows=rows, krows=rows)
+    parity.check_grad(dq[:, :, rows], dq_r, "dQ", "blocksparse_64k")
+    parity.check_grad(dk[:, :, rows], dk_r, "dK", "blocksparse_64k")
+    parity.check_grad(dv[:, :, rows], dv_r, "dV", "blocksparse_64k")
 
 
 # ---------------------------------------------------------------- integer work

@@ -45,9 +45,11 @@ def test_dropout_small_full(N, p, d, causal):
     dq_r, dk_r, dv_r = oracle.backward(f(q), f(k), f(v), f(do), scale, causal=causal,
                                        dropout=drop)
     # N = 1: dQ = dK = 0 exactly by cancellation; bound by the cancelling
-    # terms' scale (D comes from the bf16-rounded O = z v / (1 - p'))
-    fq = parity.cancel_floor(scale, o, do, k) if N == 1 else parity.GRAD_FLOOR
-    fk = parity.cancel_floor(scale, o, do, q) if N == 1 else parity.GRAD_FLOOR
+    # terms' scale (D comes from the bf16-rounded O = z v / (1 - p')), taken
+    # from the oracle's O rounded to bf16, never from the output under test
+    o_b = torch.from_numpy(o_ref).to(torch.bfloat16)
+    fq = parity.cancel_floor(scale, o_b, do, k) if N == 1 else parity.GRAD_FLOOR
+    fk = parity.cancel_floor(scale, o_b, do, q) if N == 1 else parity.GRAD_FLOOR
     parity.check_grad(dq, dq_r, "dQ", what, floor=fq)
     parity.check_grad(dk, dk_r, "dK", what, floor=fk)
     parity.check_grad(dv, dv_r, "dV", what)

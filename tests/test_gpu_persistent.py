@@ -101,3 +101,27 @@ def test_multi_unit_backward_consistent(B, H, N, d, causal):
                 f"{what} run {run}: dK/dV changed between runs"
             assert (dq.float() - first[0].float()).abs().max().item() <= \
                 1e-2 * first[0].float().abs().max().item(), f"{what} run {run}: dQ drifted"
+
+
+@pytest.mark.parametrize("B,H,N,d", [(2, 8, 1280, 128), (1, 16, 1536, 128)])
+def test_split_last_round_against_oracle(B, H, N, d):
+    # The last round's units run as two halves whose dK, dV partial sums
+    # meet in the workspace.  Every row of every head that holds a
+    # last-round unit is compared with the fp64 oracle: B2 H8 N1280 leaves
+    # units 152..159 (head 15, key tiles 2..9), B1 H16 N1536 units 152..191
+    # (heads 12..15) on the 152-SM grid.
+    dev = device()
+    assert _splits(B, H, N, d, False), "shape no longer splits its last round"
+    q, k, v, do = W.make_qkv(B, H, N, d, seed=4100 + N + B)
+    scale = 1.0 / d ** 0.5
+    qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
+    o, lse = _forward(qd, kd, vd, scale, False)
+    dq, dk, dv = _backward(fa.fa_backward, qd, kd, vd, o, dod, lse, scale, False)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    heads = parity.last_round_heads(B, H, N, False, sms)
+    dq_r, dk_r, dv_r = parity.oracle_backward(q, k, v, do, scale, False, heads=heads)
+    sel = lambda t: torch.stack([t[b, h] for (b, h) in heads]).cpu()[None]
+    what = f"B{B} H{H} N{N} d{d} last-round heads {heads}"
+    parity.check_grad(sel(dk), dk_r, "dK", what)
+    parity.check_grad(sel(dv), dv_r, "dV", what)
+    parity.check_grad(sel(dq), dq_r, "dQ", what)
