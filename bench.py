@@ -58,6 +58,22 @@ def kernel_source_hash(files):
     return h.hexdigest()[:12]
 
 
+def workload_of(args):
+    """The named workload; --sparse-density replaces the random-tile density
+    of a block-sparse one (the sparsity-scaling runs)."""
+    import dataclasses
+
+    import fa_workloads as W
+    w = W.WORKLOADS[args.workload]
+    dens = getattr(args, "sparse_density", None)
+    if dens is not None:
+        if w.sparse_density is None:
+            raise SystemExit("--sparse-density applies to block-sparse workloads")
+        w = dataclasses.replace(w, sparse_density=float(dens),
+                                note=f"{w.note}; random-tile density {dens}")
+    return w
+
+
 def bwd_compulsory_bytes(rows_q, rows_kv, d, deterministic=False):
     """Bytes the backward main kernel must move at least once: Q, dO (bf16)
     and lse, D (fp32) per query row; K, V read and dK, dV written (bf16) per
@@ -167,7 +183,7 @@ def run_gpu(args, rank, world, dist):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     peaks = load_peaks()
-    w = W.WORKLOADS[args.workload]
+    w = workload_of(args)
     B, H, N, d = w.B, w.H, w.N, w.d
     Hkv = w.kv_heads
     varlen = w.varlen
@@ -516,6 +532,9 @@ def run_gpu(args, rank, world, dist):
                    "deterministic_backward": det,
                    **({"total_tokens": T, "max_seqlen": max_seqlen,
                        "seq_lens": [int(x) for x in np.diff(cu)]} if varlen else {}),
+                   **({"sparse_density": w.sparse_density,
+                       "kept_tiles": int(np.count_nonzero(mask)),
+                       "tiles": int(mask.size)} if sparse else {}),
                    "l2": "flushed before every timed step (256 MiB device write, outside events)",
                    "parallelism": f"replicas x{world} (independent heads per GPU)"},
         "fwd": {"ms": round(fwd_ms, 5), "tflops": round(fwd_tf, 2),
@@ -629,7 +648,7 @@ def run_reference(args, rank, world):
     import fa_workloads as W
     if rank != 0:
         return None
-    w = W.WORKLOADS[args.workload]
+    w = workload_of(args)
     sample, total, per_unit = oracle_job(w)
     nthreads = os.cpu_count() or 1
     per_step_budget = max(1.0, 150.0 / max(1, args.steps + args.warmup))
@@ -658,33 +677,43 @@ def run_reference(args, rank, world):
             "gpu_launches": 0}
 
 
+SWEEP_STAGES = {(128, 128): (2, 3, 4, 5), (128, 64): (4, 8), (128, 256): (2,),
+                (64, 128): (2, 4, 8), (64, 64): (8, 16), (64, 256): (2, 4)}
+
+
+def sweep_configs(d):
+    """(rows per CTA, key tile, K/V stages) the library builds for head dim d;
+    a 256-key tile takes one query tile per CTA."""
+    return [(rows, bc, st) for (dd, bc), sts in SWEEP_STAGES.items() if dd == d for st in sts
+            for rows in ((128,) if bc == 256 else (128, 256))]
+
+
 def run_tile_sweep(args):
-    """Block-size experiment: forward time per (rows per CTA, K/V stages),
-    one JSON line each.  DRAM bytes per configuration come from running this
-    mode under ncu (dram__bytes_read.sum + dram__bytes_write.sum)."""
+    """Block-size experiment: forward time per (rows per CTA, key tile,
+    K/V stages), one JSON line each.  DRAM bytes per configuration come from
+    running this mode under ncu (dram__bytes_read.sum +
+    dram__bytes_write.sum)."""
     import torch
 
     import fa_workloads as W
     import io_aware_exact_15_gb300 as fa
 
     dev = torch.device("cuda", 0)
-    w = W.WORKLOADS[args.workload]
+    w = workload_of(args)
     B, H, N, d = w.B, w.H, w.N, w.d
     q, k, v, _, _ = W.make_inputs(w, with_do=False)
     qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
     o = torch.empty_like(qd)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
-    stages = (2, 3, 4, 5) if d == 128 else (2, 4, 8)
     ff = W.fwd_flops(w)
     peak = load_peaks()["bf16_tflops"]
-    configs = [(rows, st) for rows in (128, 256) for st in stages]
-    for rows, st in configs + [("default", None)]:
+    for rows, bc, st in sweep_configs(d) + [("default", 128, None)]:
         def call():
             if st is None:
                 r = fa.fa_forward(qd, kd, vd, o, lse, B, H, N, d, w.scale, w.causal)
             else:
                 r = fa.fa_debug_forward_config(qd, kd, vd, o, lse, B, H, N, d, w.scale, w.causal,
-                                               rows, st)
+                                               rows, bc, st)
             if r != fa.FA_OK:
                 raise RuntimeError(fa.fa_status_string(r))
         for _ in range(args.warmup):
@@ -699,10 +728,12 @@ def run_tile_sweep(args):
         ms = a.elapsed_time(b) / args.steps
         nT = (N + 127) // 128
         br = 256 if rows == "default" else rows
-        # K and V bytes a CTA streams, times the CTAs (the tile-model IO term)
+        # K and V bytes a CTA streams, times the CTAs (the tile-model IO term:
+        # the row block sets the passes over K and V, the key tile does not)
         kv_passes = B * H * ((nT + 1) // 2 if br == 256 else nT)
         print(json.dumps({"sweep": "forward tile configuration", "workload": w.name,
-                          "rows_per_cta": br, "kv_stages": st if st else "fa_forward",
+                          "rows_per_cta": br, "key_tile": bc,
+                          "kv_stages": st if st else "fa_forward",
                           "ms": round(ms, 4), "tflops": round(ff / (ms * 1e-3) / 1e12, 1),
                           "frac_of_peak": round(ff / (ms * 1e-3) / 1e12 / peak, 4),
                           "tile_model_kv_bytes": int(kv_passes) * 2 * N * d * 2}), flush=True)
@@ -766,6 +797,8 @@ def main():
                     help="time fa_backward_deterministic instead of fa_backward")
     ap.add_argument("--tile-sweep", action="store_true",
                     help="time the forward per tile configuration (block-size experiment)")
+    ap.add_argument("--sparse-density", type=float, default=None,
+                    help="random-tile density of a block-sparse workload (default: its own)")
     ap.add_argument("--host-overhead", action="store_true",
                     help="time the host side of one fa_forward / fa_backward call")
     args = ap.parse_args()
@@ -796,7 +829,7 @@ def main():
     if rank == 0:
         import fa_workloads as W
         if not args.no_cpu_baseline and world >= 1:
-            res["cpu_baseline"] = cpu_baseline(W.WORKLOADS[args.workload])
+            res["cpu_baseline"] = cpu_baseline(workload_of(args))
         print(json.dumps(res), flush=True)
     if dist is not None:
         dist.barrier()

@@ -305,18 +305,27 @@ fa_status fa_debug_schedule(int N, int causal, const uint8_t* block_mask, int ma
 
 /*
  * fa_forward with its tile configuration chosen by the caller (the block-size
- * experiment of the hackmd summary, "IO Complexity Analysis": a larger
- * row block means fewer passes over K and V).
+ * experiment of the hackmd summary, "IO Complexity Analysis": changing the
+ * block size B_c changes the IO, and the runtime with it, until compute
+ * bounds it).
  *   rows_per_cta  128 (one query tile per CTA) or 256 (two; fa_forward's
  *                 choice)
- *   kv_stages     K/V shared-memory ring depth: 2..5 for d = 128 (5 is
- *                 fa_forward's), 2, 4 or 8 for d = 64 (8 is fa_forward's)
+ *   key_tile      keys per key tile, B_c: 64, 128 (fa_forward's) or 256;
+ *                 256 needs rows_per_cta = 128 (tensor memory holds S and O
+ *                 of one query tile then)
+ *   kv_stages     K/V shared-memory ring depth, one key or value tile per
+ *                 slot:
+ *                   d = 128: key_tile 128: 2..5 (5 is fa_forward's);
+ *                            64: 4 or 8; 256: 2
+ *                   d = 64:  key_tile 128: 2, 4 or 8 (8 is fa_forward's);
+ *                            64: 8 or 16; 256: 2 or 4
  * Dense or causal, no grouped K/V.  Other arguments and results as
  * fa_forward; unsupported choices give FA_ERR_UNSUPPORTED.
  */
 fa_status fa_debug_forward_config(const void* q, const void* k, const void* v, void* o,
                                   float* lse, int B, int H, int N, int d, float scale, int causal,
-                                  int rows_per_cta, int kv_stages, cudaStream_t stream);
+                                  int rows_per_cta, int key_tile, int kv_stages,
+                                  cudaStream_t stream);
 
 /*
  * One-tile tcgen05 check of the operand layouts the kernels use.

@@ -86,7 +86,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
             "fa_debug_schedule": ([I, I, P, I, P, Z, P, P, P, P, P], I),
             "fa_debug_mma_probe": ([P, P, P, I, I, P], I),
             "fa_forward_gqa": ([P, P, P, P, P, I, I, I, I, I, F, I, P], I),
-            "fa_debug_forward_config": ([P, P, P, P, P, I, I, I, I, F, I, I, I, P], I),
+            "fa_debug_forward_config": ([P, P, P, P, P, I, I, I, I, F, I, I, I, I, P], I),
             "fa_backward_gqa": ([P, P, P, P, P, P, P, P, P, I, I, I, I, I, F, I, P, Z, P], I),
             "fa_forward_varlen": ([P, P, P, P, P, P, I, I, I, I, I, I, F, I, F, U, UI, P], I),
             "fa_backward_varlen": ([P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, I, F, U,
@@ -272,10 +272,10 @@ def fa_debug_schedule(N, causal, block_mask, mask_heads, workspace, workspace_by
 
 
 def fa_debug_forward_config(q, k, v, o, lse, B, H, N, d, scale, causal, rows_per_cta,
-                            kv_stages, stream=None) -> int:
+                            key_tile, kv_stages, stream=None) -> int:
     return load().fa_debug_forward_config(_p(q), _p(k), _p(v), _p(o), _p(lse), B, H, N, d,
                                           float(scale), int(bool(causal)), int(rows_per_cta),
-                                          int(kv_stages), _s(stream))
+                                          int(key_tile), int(kv_stages), _s(stream))
 
 
 def fa_debug_mma_probe(a, b, c, mode, n, stream=None) -> int:

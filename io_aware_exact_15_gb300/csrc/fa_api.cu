@@ -339,6 +339,23 @@ fa_status make_dropout(float p_drop, unsigned long long seed, unsigned offset,
   return FA_OK;
 }
 
+// Configurations of the block-size sweep: (d, key tile) -> K/V ring
+// stages; a 256-key tile leaves TMEM room for one 128-row query tile only.
+bool sweep_config_ok(int d, int rows_per_cta, int key_tile, int kv_stages) {
+  if (rows_per_cta != 128 && rows_per_cta != 256) return false;
+  if (key_tile == 256 && rows_per_cta != 128) return false;
+  if (d == 128) {
+    if (key_tile == 128) return kv_stages >= 2 && kv_stages <= 5;
+    if (key_tile == 64) return kv_stages == 4 || kv_stages == 8;
+    if (key_tile == 256) return kv_stages == 2;
+  } else if (d == 64) {
+    if (key_tile == 128) return kv_stages == 2 || kv_stages == 4 || kv_stages == 8;
+    if (key_tile == 64) return kv_stages == 8 || kv_stages == 16;
+    if (key_tile == 256) return kv_stages == 2 || kv_stages == 4;
+  }
+  return false;
+}
+
 fa_status check_ws(void* ws, size_t have, size_t need) {
   if (!ws) return FA_ERR_INVALID_ARG;
   if (!aligned(ws, 256)) return FA_ERR_MISALIGNED;
@@ -352,9 +369,10 @@ fa_status check_ws(void* ws, size_t have, size_t need) {
 // does).  Direct-mapped, 16 entries per thread, no locking.
 struct MapKey {
   const void* base;
-  int BH, N, d, fp32;
+  int BH, N, d, fp32, box_rows;
   bool operator==(const MapKey& o) const {
-    return base == o.base && BH == o.BH && N == o.N && d == o.d && fp32 == o.fp32;
+    return base == o.base && BH == o.BH && N == o.N && d == o.d && fp32 == o.fp32 &&
+           box_rows == o.box_rows;
   }
 };
 struct MapSlot {
@@ -369,7 +387,7 @@ int map_slot(const MapKey& k) {
   uint64_t h = reinterpret_cast<uintptr_t>(k.base) >> 8;
   h ^= static_cast<uint64_t>(k.BH) * 0x9E3779B97F4A7C15ull;
   h ^= static_cast<uint64_t>(k.N) * 0xC2B2AE3D27D4EB4Full;
-  h ^= static_cast<uint64_t>(k.d * 2 + k.fp32) * 0x165667B19E3779F9ull;
+  h ^= static_cast<uint64_t>(k.d * 2 + k.fp32 + 1024 * k.box_rows) * 0x165667B19E3779F9ull;
   h ^= h >> 29;
   return static_cast<int>(h % kMapSlots);
 }
@@ -387,9 +405,9 @@ bool encode_map(CUtensorMap* map, const MapKey& key) {
                               static_cast<cuuint64_t>(key.BH)};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(key.d) * esz,
                                  static_cast<cuuint64_t>(key.N) * key.d * esz};
-  // bf16: 128-row x 64-column boxes; fp32 accumulator: 32 x 32 boxes (both
+  // bf16: box_rows x 64-column boxes; fp32 accumulator: 32 x 32 boxes (both
   // 128-byte rows, 128-byte swizzle)
-  const cuuint32_t box_bf16[3] = {64, static_cast<cuuint32_t>(kTile), 1};
+  const cuuint32_t box_bf16[3] = {64, static_cast<cuuint32_t>(key.box_rows), 1};
   const cuuint32_t box_f32[3] = {32, 32, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   const bool ok =
@@ -408,11 +426,11 @@ bool encode_map(CUtensorMap* map, const MapKey& key) {
 }  // namespace
 
 namespace fa {
-bool make_tile_map(CUtensorMap* map, const void* base, int BH, int N, int d) {
-  return encode_map(map, MapKey{base, BH, N, d, 0});
+bool make_tile_map(CUtensorMap* map, const void* base, int BH, int N, int d, int box_rows) {
+  return encode_map(map, MapKey{base, BH, N, d, 0, box_rows});
 }
 bool make_acc_map(CUtensorMap* map, const void* base, int BH, int N, int d) {
-  return encode_map(map, MapKey{base, BH, N, d, 1});
+  return encode_map(map, MapKey{base, BH, N, d, 1, 32});
 }
 }  // namespace fa
 
@@ -726,18 +744,17 @@ fa_status fa_debug_schedule(int N, int causal, const uint8_t* block_mask, int ma
 
 fa_status fa_debug_forward_config(const void* q, const void* k, const void* v, void* o,
                                   float* lse, int B, int H, int N, int d, float scale, int causal,
-                                  int rows_per_cta, int kv_stages, cudaStream_t stream) {
+                                  int rows_per_cta, int key_tile, int kv_stages,
+                                  cudaStream_t stream) {
   FA_TRY(check_fwd_args(q, k, v, o, lse, B, H, N, d, scale));
-  if (rows_per_cta != 128 && rows_per_cta != 256) return FA_ERR_UNSUPPORTED;
-  const bool ok_stages = (d == 128) ? (kv_stages >= 2 && kv_stages <= 5)
-                                    : (kv_stages == 2 || kv_stages == 4 || kv_stages == 8);
-  if (!ok_stages) return FA_ERR_UNSUPPORTED;
+  if (!sweep_config_ok(d, rows_per_cta, key_tile, kv_stages)) return FA_ERR_UNSUPPORTED;
   fa_status st = FA_OK;
   int* err = status_word(&st);
   if (!err) return st;
+  const int kbox = key_tile < kTile ? key_tile : kTile;
   CUtensorMap tq, tk, tv;
-  if (!fa::make_tile_map(&tq, q, B * H, N, d) || !fa::make_tile_map(&tk, k, B * H, N, d) ||
-      !fa::make_tile_map(&tv, v, B * H, N, d))
+  if (!fa::make_tile_map(&tq, q, B * H, N, d) || !fa::make_tile_map(&tk, k, B * H, N, d, kbox) ||
+      !fa::make_tile_map(&tv, v, B * H, N, d, kbox))
     return FA_ERR_CUDA;
   fa::FwdParams p;
   p.o = o;
@@ -752,7 +769,7 @@ fa_status fa_debug_forward_config(const void* q, const void* k, const void* v, v
   p.single_tile = rows_per_cta == 128 ? 1 : 0;
   p.err = err;
   p.wait_ns = wait_limit_ns();
-  FA_CUDA(fa::launch_forward_config(p, tq, tk, tv, kv_stages, stream));
+  FA_CUDA(fa::launch_forward_config(p, tq, tk, tv, kv_stages, key_tile, stream));
   return FA_OK;
 }
 

@@ -35,16 +35,22 @@
 namespace fa {
 namespace {
 
-template <int D, int NS_ = 0>
+// BC: keys per key tile (128 except in the block-size sweep: 64 or 256).
+template <int D, int NS_ = 0, int BC = kTile>
 struct FwdSmem {
   static constexpr int CH = D / 64;             // 128-byte column chunks per row
-  static constexpr int CHUNK = kTile * 128;     // [128 rows x 128 B] = 16 KB
-  static constexpr int TILE = CH * CHUNK;       // one 128 x D bf16 tile
+  static constexpr int CHUNK = kTile * 128;     // query tile: [128 rows x 128 B] = 16 KB
+  static constexpr int TILE = CH * CHUNK;       // one 128 x D bf16 query tile
+  static constexpr int KCHUNK = BC * 128;       // key / value tile: [BC rows x 128 B]
+  static constexpr int KTILE = CH * KCHUNK;     // one BC x D bf16 key or value tile
+  static constexpr int KBOX = BC < kTile ? BC : kTile;  // rows of one K/V TMA box
+  // query tiles whose S and O fit the 512 TMEM columns (2 BC + 2 D for two)
+  static constexpr int NQT = (2 * BC + 2 * D <= 512) ? 2 : 1;
   // K/V ring slots (one tile each); NS_ != 0 overrides for the tile sweep
   static constexpr int NS = NS_ != 0 ? NS_ : ((D == 64) ? 8 : 5);
   static constexpr int Q = 0;
   static constexpr int KV = Q + 2 * TILE;
-  static constexpr int BAR = KV + NS * TILE;
+  static constexpr int BAR = KV + NS * KTILE;
   static constexpr int B_Q = 0, B_KVF = 1, B_KVE = 1 + NS, B_SF = 1 + 2 * NS, B_PF = B_SF + 2,
                        B_OF = B_PF + 2, NBAR = B_OF + 1;
   static constexpr int MISC = BAR + NBAR * 8;
@@ -52,7 +58,8 @@ struct FwdSmem {
   // registers).  d = 64 would leave room for separate P columns after O1,
   // but that layout measured 8 % slower on the BERT-shaped workload.
   static constexpr int T_P = 0;
-  static constexpr int T_PSTRIDE = 128;
+  static constexpr int T_PSTRIDE = BC;
+  static constexpr int T_O = NQT * BC;  // O_s at T_O + s * D
   static constexpr int ALLOC = MISC + 16 + 1024;  // + slack for 1024-byte alignment
   static_assert(ALLOC <= 232448, "shared memory budget");
 };
@@ -62,11 +69,13 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleLog2 = 8.0f;  // lazy rescale threshold (factor 256)
 
-template <int D, int KIND, int NS_>
+template <int D, int KIND, int NS_, int BC>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const FwdParams p) {
-  using L = FwdSmem<D, NS_>;
+  using L = FwdSmem<D, NS_, BC>;
+  static_assert(BC == kTile || (NS_ != 0 && KIND == kPlain),
+                "key tiles other than 128 exist only in the plain sweep instantiations");
   grid_dep_wait();  // the previous kernel's writes are visible from here on
   grid_dep_launch();
   extern __shared__ uint8_t smem_raw[];
@@ -78,8 +87,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::MISC + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // one query tile per CTA only in the tile-sweep instantiations (NS_ != 0)
-  const bool single = NS_ != 0 && p.single_tile != 0;
+  // one query tile per CTA only in the tile-sweep instantiations (NS_ != 0),
+  // and always when TMEM holds a single query tile's S and O
+  const bool single = (NS_ != 0 && p.single_tile != 0) || L::NQT == 1;
   const int ntmax = (p.N + kTile - 1) / kTile;
   const int npairs = single ? ntmax : (ntmax + 1) / 2;
   const int BH = p.B * p.H;
@@ -109,8 +119,17 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   const size_t slice_rows = varlen ? static_cast<size_t>(p.total) : static_cast<size_t>(p.N);
   const int nT = (N + kTile - 1) / kTile;
 
-  FwdSchedule sch;
-  sch.init(pair, nT, p.causal != 0, p.lists, head, single);
+  FwdScheduleT<BC> sch;
+  sch.init(pair, nT, p.causal != 0, p.lists, head, single, (N + BC - 1) / BC);
+  // K_j or V_j into ring slot `pos`: CH column chunks of BC / KBOX boxes
+  auto load_kv = [&](int pos, const CUtensorMap* m, int kt) {
+#pragma unroll
+    for (int c = 0; c < L::CH; ++c)
+#pragma unroll
+      for (int h = 0; h < BC / L::KBOX; ++h)
+        tma_load_3d(sb + L::KV + pos * L::KTILE + c * L::KCHUNK + h * L::KBOX * 128, m,
+                    bar(L::B_KVF + pos), 64 * c, row0 + kt * BC + h * L::KBOX, zkv);
+  };
 
   // Thread 0 (the producer's lane) initialises the barriers and sends Q and
   // the first K/V pair at once, before the block-wide barrier and the TMEM
@@ -140,16 +159,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       tma_load_3d(sb + L::Q + c * L::CHUNK, &tq, bar(L::B_Q), 64 * c, row0 + y0, zq);
       tma_load_3d(sb + L::Q + L::TILE + c * L::CHUNK, &tq, bar(L::B_Q), 64 * c, row0 + y1, zq);
     }
-    FwdSchedule first = sch;  // the first key tile, without advancing sch
+    FwdScheduleT<BC> first = sch;  // the first key tile, without advancing sch
     int kt0, mem0;
     if (first.next(kt0, mem0)) {
 #pragma unroll
       for (int t = 0; t < 2; ++t) {  // ring slots 0 and 1
-        mbar_arrive_expect_tx(bar(L::B_KVF + t), L::TILE);
-#pragma unroll
-        for (int c = 0; c < L::CH; ++c)
-          tma_load_3d(sb + L::KV + t * L::TILE + c * L::CHUNK, t == 0 ? &tk : &tv,
-                      bar(L::B_KVF + t), 64 * c, row0 + kt0 * kTile, zkv);
+        mbar_arrive_expect_tx(bar(L::B_KVF + t), L::KTILE);
+        load_kv(t, t == 0 ? &tk : &tv, kt0);
       }
       pre_kv = true;
     }
@@ -184,11 +200,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(bar(L::B_KVF + pos), L::TILE);
-#pragma unroll
-          for (int c = 0; c < L::CH; ++c)
-            tma_load_3d(sb + L::KV + pos * L::TILE + c * L::CHUNK, t == 0 ? &tk : &tv,
-                        bar(L::B_KVF + pos), 64 * c, row0 + kt * kTile, zkv);
+          mbar_arrive_expect_tx(bar(L::B_KVF + pos), L::KTILE);
+          load_kv(pos, t == 0 ? &tk : &tv, kt);
           ++idx;
         }
       }
@@ -203,28 +216,29 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idS = idesc_bf16(128, 128, false, false);
+      constexpr uint32_t idS = idesc_bf16(128, BC, false, false);
       constexpr uint32_t idO = idesc_bf16(128, D, false, true);
       // descriptors are formed once per operand and advanced per k-step
       const uint64_t dq0 = desc_sw128(sb + L::Q, 16, 1024);
       const uint64_t dkv0 = desc_sw128(sb + L::KV, 16, 1024);  // K-major ring slot 0
-      const uint64_t dv0 = desc_sw128(sb + L::KV, L::CHUNK, 1024);  // MN-major ring slot 0
+      const uint64_t dv0 = desc_sw128(sb + L::KV, L::KCHUNK, 1024);  // MN-major ring slot 0
       auto issue_s = [&](int s, int kpos) {
         const uint64_t qa = desc_advance(dq0, s * L::TILE);
-        const uint64_t kb = desc_advance(dkv0, kpos * L::TILE);
+        const uint64_t kb = desc_advance(dkv0, kpos * L::KTILE);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * L::CHUNK + (kk & 3) * 32;
-          mma_bf16_ss(tmem + s * 128, desc_advance(qa, off), desc_advance(kb, off), idS, kk > 0);
+          const uint32_t in_row = (kk & 3) * 32;
+          mma_bf16_ss(tmem + s * BC, desc_advance(qa, (kk >> 2) * L::CHUNK + in_row),
+                      desc_advance(kb, (kk >> 2) * L::KCHUNK + in_row), idS, kk > 0);
         }
       };
-      // O_s += P_s V: P_s sits in TMEM (64 columns, two bf16 per column), V is
-      // MN-major in shared memory
+      // O_s += P_s V: P_s sits in TMEM (BC / 2 columns, two bf16 per column),
+      // V is MN-major in shared memory
       auto issue_pv = [&](int s, int vpos, bool acc) {
-        const uint64_t vb = desc_advance(dv0, vpos * L::TILE);
+        const uint64_t vb = desc_advance(dv0, vpos * L::KTILE);
 #pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk)
-          mma_bf16_ts(tmem + 256 + s * D, tmem + L::T_P + s * L::T_PSTRIDE + kk * 8,
+        for (int kk = 0; kk < BC / 16; ++kk)
+          mma_bf16_ts(tmem + L::T_O + s * D, tmem + L::T_P + s * L::T_PSTRIDE + kk * 8,
                       desc_advance(vb, kk * 2048), idO, (acc || kk > 0) ? 1u : 0u);
       };
       int kt, mem, kt_n = 0, mem_n = 0;
@@ -297,8 +311,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const bool active = sch.act[s];
     const int qrow = qt * kTile + r;
     const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
-    const uint32_t tS = tmem + lane_off + s * 128;
-    const uint32_t tO = tmem + lane_off + 256 + s * D;
+    const uint32_t tS = tmem + lane_off + s * BC;
+    const uint32_t tO = tmem + lane_off + L::T_O + s * D;
     const uint32_t tP = tmem + lane_off + L::T_P + s * L::T_PSTRIDE;
     const float sl2 = p.scale * kLog2e;
     const DropoutRng rng{p.drop.rk, p.drop.offset, p.drop.t * 0x01010101u};
@@ -311,34 +325,54 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       ok = __all_sync(0xffffffffu, wait_bar(bar(L::B_SF + s), cnt & 1, wc));
       if (!ok) break;
       tc_fence_after();
-      uint32_t sr[4][32];
+      // The scores of a key tile are read in register groups of up to 128
+      // keys (GC chunks of 32); a 256-key tile (block-size sweep) takes two
+      // groups, read once for the row max and again for the exponentials.
+      constexpr int GW = BC < kTile ? BC : kTile;
+      constexpr int NG = BC / GW;
+      constexpr int GC = GW / 32;
+      const int kbase = kt * BC;
+      const bool need_mask = (kbase + BC > N) || (p.causal && kbase + BC - 1 > qt * kTile);
+      uint32_t sr[GC][32];
+      auto load_group = [&](int g) {
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32 * c, sr[c]);
-      tmem_ld_wait();
+        for (int c = 0; c < GC; ++c) tmem_ld32(tS + g * GW + 32 * c, sr[c]);
+        tmem_ld_wait();
 #pragma unroll
-      for (int c = 0; c < 4; ++c) reg_fence(sr[c]);
-      const int kbase = kt * kTile;
-      const bool need_mask = (kbase + kTile > N) || (p.causal && kbase + kTile - 1 > qt * kTile);
-      if (need_mask) {
-        // keys kbase + i with i >= lim are masked (past N, or after this row
-        // when causal)
-        int lim = N - kbase;
-        if (p.causal && qrow - kbase + 1 < lim) lim = qrow - kbase + 1;
+        for (int c = 0; c < GC; ++c) reg_fence(sr[c]);
+        if (need_mask) {
+          // keys kbase + i with i >= lim are masked (past N, or after this
+          // row when causal)
+          int lim = N - kbase;
+          if (p.causal && qrow - kbase + 1 < lim) lim = qrow - kbase + 1;
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
+          for (int c = 0; c < GC; ++c)
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (32 * c + j >= lim) sr[c][j] = __float_as_uint(-INFINITY);
+            for (int j = 0; j < 32; ++j)
+              if (g * GW + 32 * c + j >= lim) sr[c][j] = __float_as_uint(-INFINITY);
+        }
+      };
+      float mx[GC];
+#pragma unroll
+      for (int c = 0; c < GC; ++c) mx[c] = -INFINITY;
+#pragma unroll
+      for (int g = 0; g < NG; ++g) {
+        load_group(g);
+#pragma unroll
+        for (int j = 0; j < 32; j += 2)  // two scores per three-input max
+#pragma unroll
+          for (int c = 0; c < GC; ++c)
+            mx[c] = fmax3(mx[c], __uint_as_float(sr[c][j]), __uint_as_float(sr[c][j + 1]));
       }
-      float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+      float mxa;
+      if constexpr (GC == 4) {
+        mxa = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+      } else {
+        mxa = mx[0];
 #pragma unroll
-      for (int j = 0; j < 32; j += 2) {  // two scores per three-input max
-        mx0 = fmax3(mx0, __uint_as_float(sr[0][j]), __uint_as_float(sr[0][j + 1]));
-        mx1 = fmax3(mx1, __uint_as_float(sr[1][j]), __uint_as_float(sr[1][j + 1]));
-        mx2 = fmax3(mx2, __uint_as_float(sr[2][j]), __uint_as_float(sr[2][j + 1]));
-        mx3 = fmax3(mx3, __uint_as_float(sr[3][j]), __uint_as_float(sr[3][j + 1]));
+        for (int c = 1; c < GC; ++c) mxa = fmaxf(mxa, mx[c]);
       }
-      const float m_new = fmaxf(m, fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2);
+      const float m_new = fmaxf(m, mxa * sl2);
       const bool resc = m_new > m + kRescaleLog2;
       const float alpha = resc ? ex2(m - m_new) : 1.f;
       if (resc) {
@@ -350,10 +384,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       const uint64_t sl2x2 = f2_pack(sl2, sl2), nmux2 = f2_pack(-mu, -mu);
       float ls0 = 0.f, ls1 = 0.f, ls2 = 0.f, ls3 = 0.f;  // row-sum partials
       PhiloxOut rw;
-      // P (bf16, two per 32-bit column) overwrites the first 64 columns of
-      // this tile's S, which are already in registers
+      // P (bf16, two per 32-bit column) overwrites the first BC / 2 columns
+      // of this tile's S, whose scores are already in registers (group g's
+      // P lands on columns of group 0, which the first pass has read)
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {  // 32 keys -> 16 columns per store
+      for (int g = 0; g < NG; ++g) {
+      if (NG > 1) load_group(g);
+#pragma unroll
+      for (int q = 0; q < GC; ++q) {  // 32 keys -> 16 columns per store
         // packed words overwrite the scores already consumed: group c4 reads
         // sr[q][8 c4 .. 8 c4 + 7] and writes sr[q][4 c4 .. 4 c4 + 3]
 #pragma unroll
@@ -379,7 +417,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           if (DROP) {
             // dropped weights leave the PV product (l keeps them); one
             // generator call covers keys 32 q + 16 (c4 / 2) .. + 15
-            if ((c4 & 1) == 0) rw = rng.group(kt * 8 + 2 * q + (c4 >> 1), qrow, bh);
+            if ((c4 & 1) == 0) rw = rng.group((kbase + g * GW) / 16 + 2 * q + (c4 >> 1), qrow, bh);
             const uint32_t m0 = DropoutRng::keep_bytes(rw.w[2 * (c4 & 1)], rng.t4);
             const uint32_t m1 = DropoutRng::keep_bytes(rw.w[2 * (c4 & 1) + 1], rng.t4);
             sr[q][4 * c4] &= pair_mask(m0, 0);
@@ -388,7 +426,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             sr[q][4 * c4 + 3] &= pair_mask(m1, 1);
           }
         }
-        tmem_st16(tP + 16 * q, *reinterpret_cast<const uint32_t(*)[16]>(&sr[q][0]));
+        tmem_st16(tP + g * (GW / 2) + 16 * q, *reinterpret_cast<const uint32_t(*)[16]>(&sr[q][0]));
+      }
       }
       // rescale O only after P is out of the registers (lower register pressure)
       if (rescale_o) {
@@ -472,38 +511,48 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   }
 }
 
-template <int D, int KIND, int NS_ = 0>
+template <int D, int KIND, int NS_ = 0, int BC = kTile>
 cudaError_t launch_fwd_d(const FwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                          const CUtensorMap& tv, cudaStream_t stream) {
-  using L = FwdSmem<D, NS_>;
+  using L = FwdSmem<D, NS_, BC>;
   static std::atomic<unsigned long long> attr_done{0};
   cudaError_t e = smem_attr_once(
-      attr_done, reinterpret_cast<const void*>(fa_fwd_kernel<D, KIND, NS_>), L::ALLOC);
+      attr_done, reinterpret_cast<const void*>(fa_fwd_kernel<D, KIND, NS_, BC>), L::ALLOC);
   if (e != cudaSuccess) return e;
   const int nT = (p.N + kTile - 1) / kTile;
-  const int npairs = (NS_ != 0 && p.single_tile) ? nT : (nT + 1) / 2;
+  const bool single = (NS_ != 0 && p.single_tile) || L::NQT == 1;
+  const int npairs = single ? nT : (nT + 1) / 2;
   const long long ctas = static_cast<long long>(npairs) * p.B * p.H;
-  return launch_pdl(fa_fwd_kernel<D, KIND, NS_>, dim3(static_cast<unsigned>(ctas)),
+  return launch_pdl(fa_fwd_kernel<D, KIND, NS_, BC>, dim3(static_cast<unsigned>(ctas)),
                     dim3(kFwdThreads), L::ALLOC, stream, tq, tk, tv, p);
 }
 
 }  // namespace
 
+// Block-size sweep configurations: (head dim, key tile, K/V ring stages).
+// Shared memory: two query tiles (2 x 128 x d x 2 B) plus `stages` ring
+// slots of one key or value tile each (key tile x d x 2 B).  TMEM: S (key
+// tile columns) and O (d columns) per query tile, at most 512 columns, so a
+// 256-key tile holds one query tile per CTA.
 cudaError_t launch_forward_config(const FwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
-                                  const CUtensorMap& tv, int kv_stages, cudaStream_t stream) {
-  if (p.d == 128) {
-    switch (kv_stages) {
-      case 2: return launch_fwd_d<128, kPlain, 2>(p, tq, tk, tv, stream);
-      case 3: return launch_fwd_d<128, kPlain, 3>(p, tq, tk, tv, stream);
-      case 4: return launch_fwd_d<128, kPlain, 4>(p, tq, tk, tv, stream);
-      case 5: return launch_fwd_d<128, kPlain, 5>(p, tq, tk, tv, stream);
-    }
-  } else if (p.d == 64) {
-    switch (kv_stages) {
-      case 2: return launch_fwd_d<64, kPlain, 2>(p, tq, tk, tv, stream);
-      case 4: return launch_fwd_d<64, kPlain, 4>(p, tq, tk, tv, stream);
-      case 8: return launch_fwd_d<64, kPlain, 8>(p, tq, tk, tv, stream);
-    }
+                                  const CUtensorMap& tv, int kv_stages, int key_tile,
+                                  cudaStream_t stream) {
+  const int code = p.d * 100000 + key_tile * 100 + kv_stages;
+  switch (code) {
+    case 12812802: return launch_fwd_d<128, kPlain, 2>(p, tq, tk, tv, stream);
+    case 12812803: return launch_fwd_d<128, kPlain, 3>(p, tq, tk, tv, stream);
+    case 12812804: return launch_fwd_d<128, kPlain, 4>(p, tq, tk, tv, stream);
+    case 12812805: return launch_fwd_d<128, kPlain, 5>(p, tq, tk, tv, stream);
+    case 12806404: return launch_fwd_d<128, kPlain, 4, 64>(p, tq, tk, tv, stream);
+    case 12806408: return launch_fwd_d<128, kPlain, 8, 64>(p, tq, tk, tv, stream);
+    case 12825602: return launch_fwd_d<128, kPlain, 2, 256>(p, tq, tk, tv, stream);
+    case 6412802: return launch_fwd_d<64, kPlain, 2>(p, tq, tk, tv, stream);
+    case 6412804: return launch_fwd_d<64, kPlain, 4>(p, tq, tk, tv, stream);
+    case 6412808: return launch_fwd_d<64, kPlain, 8>(p, tq, tk, tv, stream);
+    case 6406408: return launch_fwd_d<64, kPlain, 8, 64>(p, tq, tk, tv, stream);
+    case 6406416: return launch_fwd_d<64, kPlain, 16, 64>(p, tq, tk, tv, stream);
+    case 6425602: return launch_fwd_d<64, kPlain, 2, 256>(p, tq, tk, tv, stream);
+    case 6425604: return launch_fwd_d<64, kPlain, 4, 256>(p, tq, tk, tv, stream);
   }
   return cudaErrorInvalidValue;
 }

@@ -135,18 +135,22 @@ struct BwdParams {
 // dropout on P.
 enum KernelKind : int { kPlain = 0, kGrouped = 1, kGeneral = 2, kGeneralDropout = 3 };
 
-// 3-D bf16 view {d, N, B*H} of a [B, H, N, d] tensor, 128-row x 64-column
-// boxes with 128-byte swizzle.
-bool make_tile_map(CUtensorMap* map, const void* base, int BH, int N, int d);
+// 3-D bf16 view {d, N, B*H} of a [B, H, N, d] tensor, box_rows x 64-column
+// boxes (128 rows except the 64-key tiles of the block-size sweep) with
+// 128-byte swizzle.
+bool make_tile_map(CUtensorMap* map, const void* base, int BH, int N, int d,
+                   int box_rows = kTile);
 // 3-D fp32 view {d, N, B*H} of a [B, H, N, d] fp32 tensor, 32 x 32 boxes
 // (128-byte rows, 128-byte swizzle): the dQ accumulator for TMA reduce-add.
 bool make_acc_map(CUtensorMap* map, const void* base, int BH, int N, int d);
 
 cudaError_t launch_forward(const FwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                            const CUtensorMap& tv, cudaStream_t stream);
-// the forward with a chosen K/V ring depth (d = 128: 2..5, d = 64: 2, 4, 8)
+// the forward with a chosen key tile width (64, 128, 256) and K/V ring
+// depth; K and V maps must have min(key_tile, 128)-row boxes
 cudaError_t launch_forward_config(const FwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
-                                  const CUtensorMap& tv, int kv_stages, cudaStream_t stream);
+                                  const CUtensorMap& tv, int kv_stages, int key_tile,
+                                  cudaStream_t stream);
 cudaError_t launch_backward_main(const BwdParams& p, const CUtensorMap& tq,
                                  const CUtensorMap& tk, const CUtensorMap& tv,
                                  const CUtensorMap& tdo, const CUtensorMap& tdq,

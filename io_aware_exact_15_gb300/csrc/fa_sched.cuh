@@ -22,7 +22,12 @@
 
 namespace fa {
 
-struct FwdSchedule {
+// BC: keys per key tile.  Query tiles are always kTile = 128 rows; the key
+// tile width differs from 128 only in the block-size sweep (dense and causal
+// batches): key tile j of width BC holds an allowed key of query tile i iff
+// j * BC <= 128 * i + 127.  Block masks (128 x 128 tiles) need BC = 128.
+template <int BC>
+struct FwdScheduleT {
   int qt[2];
   bool act[2];
   bool causal, sparse;
@@ -31,22 +36,30 @@ struct FwdSchedule {
   int na, nb, ia, ib;
   int next_dense, end_dense;
 
-  // single: the CTA takes one query tile (index `pair`) instead of two
+  // last key tile that query tile t reaches under the causal rule
+  static FA_DEV int causal_last(int t) {
+    if constexpr (BC == kTile) return t;
+    return (kTile * t + kTile - 1) / BC;
+  }
+
+  // single: the CTA takes one query tile (index `pair`) instead of two;
+  // nT: query tiles of the sequence (key tiles: ceil(nT * 128 / BC))
   FA_DEV void init(int pair, int nT, bool causal_, const TileLists& L, int head,
-                   bool single = false) {
+                   bool single = false, int nkt = -1) {
     qt[0] = single ? pair : 2 * pair;
     qt[1] = qt[0] + 1;
     act[0] = true;
     act[1] = !single && qt[1] < nT;
     causal = causal_;
-    sparse = L.row_ptr != nullptr;
+    sparse = BC == kTile && L.row_ptr != nullptr;
     next_dense = 0;
     end_dense = 0;
     la = lb = nullptr;
     na = nb = ia = ib = 0;
     if (!sparse) {
-      end_dense = causal ? (act[1] ? qt[1] : qt[0]) + 1 : nT;
-      if (end_dense > nT) end_dense = nT;
+      if (nkt < 0) nkt = BC == kTile ? nT : (nT * kTile + BC - 1) / BC;
+      end_dense = causal ? causal_last(act[1] ? qt[1] : qt[0]) + 1 : nkt;
+      if (end_dense > nkt) end_dense = nkt;
       return;
     }
     const int hm = (L.mask_heads == 1) ? 0 : head;
@@ -71,7 +84,8 @@ struct FwdSchedule {
     if (!sparse) {
       if (next_dense >= end_dense) return false;
       kt = next_dense++;
-      mem = ((!causal || kt <= qt[0]) ? 1 : 0) | ((act[1] && (!causal || kt <= qt[1])) ? 2 : 0);
+      mem = ((!causal || kt <= causal_last(qt[0])) ? 1 : 0) |
+            ((act[1] && (!causal || kt <= causal_last(qt[1]))) ? 2 : 0);
       return true;
     }
     const int ka = ia < na ? la[ia] : INT_MAX;
@@ -90,6 +104,8 @@ struct FwdSchedule {
     return true;
   }
 };
+
+using FwdSchedule = FwdScheduleT<kTile>;
 
 struct BwdSchedule {
   bool sparse;
