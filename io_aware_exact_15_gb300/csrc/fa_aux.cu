@@ -12,66 +12,205 @@
 namespace fa {
 
 // ------------------------------------------------------------------ lists
-// One CTA per mask head.  CSR: for each query tile the ascending key tiles
-// whose mask byte is nonzero; CSC: for each key tile the ascending query
-// tiles ("Block-sparse FlashAttention": only nonzero blocks are visited).
-__global__ void __launch_bounds__(1024) fa_lists_kernel(const uint8_t* __restrict__ mask, int nT,
-                                                        int* row_ptr, int* col_idx, int* col_ptr,
-                                                        int* row_idx) {
+// CSR: for each query tile the ascending key tiles whose mask byte is
+// nonzero; CSC: for each key tile the ascending query tiles ("Block-sparse
+// FlashAttention": only nonzero blocks are visited).  One CTA of 32 warps
+// per mask head reads the mask in chunks of 16 columns (one 16-byte load
+// when the mask is 16-byte aligned and nT is a multiple of 16, else byte
+// loads), so that a warp covers 512 consecutive columns per access:
+//   CSR  a warp per row: row counts, then each lane places its chunk's
+//        columns after a prefix over the warp's lanes;
+//   CSC  warps split into 512-column strips x row ranges: per-range column
+//        counts, a prefix over ranges per column, then each lane walks its
+//        16 columns down its row range in ascending order.
+// Counts and prefix sums live in shared memory: 2 (nT + 1) + R nT ints, R
+// row ranges per strip (R nT <= 32 * 512 + 31 nT).
+constexpr int kListWarps = 32;
+
+struct ListLayout {
+  int nT, strips, ranges, rows_per_range;
+  __host__ __device__ static ListLayout of(int nT) {
+    ListLayout L;
+    L.nT = nT;
+    L.strips = (nT + 511) / 512;
+    L.ranges = kListWarps / L.strips > 0 ? kListWarps / L.strips : 1;
+    L.rows_per_range = (nT + L.ranges - 1) / L.ranges;
+    return L;
+  }
+  __host__ __device__ int smem_ints() const { return 2 * (nT + 1) + ranges * nT; }
+};
+
+// nonzero bits of columns c0 .. c0 + 15 of a mask row (bit k: column c0 + k;
+// columns >= nT read as zero)
+FA_DEV uint32_t chunk_bits(const uint8_t* row, int c0, int nT, bool vec) {
+  if (vec && c0 + 16 <= nT) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(row + c0));
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t bits = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      // 0xFF in each nonzero byte, then byte k -> bit k (one multiply moves
+      // the four low bits of the bytes to bits 28..31 with no carries)
+      const uint32_t nz = __vcmpne4(w[i], 0u);
+      bits |= (((nz & 0x01010101u) * 0x10204080u) >> 28) << (4 * i);
+    }
+    return bits;
+  }
+  uint32_t bits = 0;
+  for (int k = 0; k < 16 && c0 + k < nT; ++k) bits |= (row[c0 + k] != 0 ? 1u : 0u) << k;
+  return bits;
+}
+
+// exclusive prefix sum of a[0 .. n) in place, a[n] = total (whole block)
+FA_DEV void block_exclusive_scan(int* a, int n, int* warp_tot) {
+  const int t = threadIdx.x, nthr = blockDim.x, lane = t & 31, warp = t >> 5;
+  const int per = (n + nthr - 1) / nthr;
+  const int b = t * per, e = min(n, b + per);
+  int local = 0;
+  for (int i = b; i < e; ++i) local += a[i];
+  int incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int x = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += x;
+  }
+  if (lane == 31) warp_tot[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < (nthr >> 5) ? warp_tot[lane] : 0;
+    int wi = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int x = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += x;
+    }
+    if (lane < (nthr >> 5)) warp_tot[lane] = wi - w;  // exclusive warp offsets
+    if (lane == 31) warp_tot[32] = wi;                 // block total
+  }
+  __syncthreads();
+  int run = warp_tot[warp] + incl - local;
+  for (int i = b; i < e; ++i) {
+    const int x = a[i];
+    a[i] = run;
+    run += x;
+  }
+  if (t == 0) a[n] = warp_tot[32];
+  __syncthreads();
+}
+
+__global__ void __launch_bounds__(kListWarps * 32) fa_lists_kernel(
+    const uint8_t* __restrict__ mask, int nT, int* row_ptr, int* col_idx, int* col_ptr,
+    int* row_idx) {
   grid_dep_wait();  // the previous kernel's writes are visible from here on
   grid_dep_launch();
-  extern __shared__ int cnt[];  // [nT + 1]
+  extern __shared__ int lsm[];
+  __shared__ int warp_tot[33];
+  const ListLayout L = ListLayout::of(nT);
+  int* rc = lsm;                 // [nT + 1] row counts -> CSR offsets
+  int* cc = rc + (nT + 1);       // [nT + 1] column counts -> CSC offsets
+  int* rg = cc + (nT + 1);       // [ranges][nT] per-range column counts -> starts
   const int h = blockIdx.x;
   const uint8_t* m = mask + static_cast<size_t>(h) * nT * nT;
   int* rp = row_ptr + static_cast<size_t>(h) * (nT + 1);
   int* cp = col_ptr + static_cast<size_t>(h) * (nT + 1);
   int* ci = col_idx + static_cast<size_t>(h) * nT * nT;
   int* ri = row_idx + static_cast<size_t>(h) * nT * nT;
-  for (int pass = 0; pass < 2; ++pass) {
-    // pass 0: rows (CSR), pass 1: columns (CSC)
-    for (int a = threadIdx.x; a < nT; a += blockDim.x) {
-      int c = 0;
-      for (int b = 0; b < nT; ++b) {
-        const size_t e = pass == 0 ? static_cast<size_t>(a) * nT + b : static_cast<size_t>(b) * nT + a;
-        c += m[e] != 0;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const bool vec = (reinterpret_cast<uintptr_t>(mask) % 16 == 0) && (nT % 16 == 0);
+  auto row_of = [&](int r) { return m + static_cast<size_t>(r) * nT; };
+  // this warp's CSC strip and row range (warps past strips x ranges idle)
+  const int strip = warp % L.strips, range = warp / L.strips;
+  const bool csc_warp = range < L.ranges;
+  const int col0 = strip * 512 + 16 * lane;
+  const int r_lo = csc_warp ? min(nT, range * L.rows_per_range) : 0;
+  const int r_hi = csc_warp ? min(nT, r_lo + L.rows_per_range) : 0;
+
+  // ---- counts
+  for (int r = warp; r < nT; r += kListWarps) {
+    int c = 0;
+    for (int c0 = 16 * lane; c0 < nT; c0 += 512) c += __popc(chunk_bits(row_of(r), c0, nT, vec));
+    c = __reduce_add_sync(0xffffffffu, c);
+    if (lane == 0) rc[r] = c;
+  }
+  {
+    int cnt[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) cnt[k] = 0;
+    if (csc_warp && col0 < nT) {
+      for (int r = r_lo; r < r_hi; ++r) {
+        const uint32_t bits = chunk_bits(row_of(r), col0, nT, vec);
+#pragma unroll
+        for (int k = 0; k < 16; ++k) cnt[k] += (bits >> k) & 1u;
       }
-      cnt[a] = c;
+#pragma unroll
+      for (int k = 0; k < 16; ++k)
+        if (col0 + k < nT) rg[range * nT + col0 + k] = cnt[k];
     }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      int run = 0;
-      for (int a = 0; a < nT; ++a) {
-        const int c = cnt[a];
-        cnt[a] = run;
-        run += c;
+  }
+  __syncthreads();
+  // per column: starts of each row range, column totals
+  for (int c = threadIdx.x; c < nT; c += blockDim.x) {
+    int run = 0;
+    for (int g = 0; g < L.ranges; ++g) {
+      int* x = &rg[g * nT + c];
+      const int v = (g * L.rows_per_range < nT) ? *x : 0;
+      *x = run;
+      run += v;
+    }
+    cc[c] = run;
+  }
+  __syncthreads();
+  block_exclusive_scan(rc, nT, warp_tot);
+  block_exclusive_scan(cc, nT, warp_tot);
+  for (int a = threadIdx.x; a <= nT; a += blockDim.x) {
+    rp[a] = rc[a];
+    cp[a] = cc[a];
+  }
+
+  // ---- indices
+  for (int r = warp; r < nT; r += kListWarps) {
+    int base = rc[r];
+    for (int c0s = 0; c0s < nT; c0s += 512) {
+      const int c0 = c0s + 16 * lane;
+      const uint32_t bits = c0 < nT ? chunk_bits(row_of(r), c0, nT, vec) : 0u;
+      const int n = __popc(bits);
+      int incl = n;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int x = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += x;
       }
-      cnt[nT] = run;
+      int pos = base + incl - n;
+      for (uint32_t b = bits; b; b &= b - 1) ci[pos++] = c0 + __ffs(b) - 1;
+      base += __shfl_sync(0xffffffffu, incl, 31);
     }
-    __syncthreads();
-    int* ptr = pass == 0 ? rp : cp;
-    int* idx = pass == 0 ? ci : ri;
-    for (int a = threadIdx.x; a <= nT; a += blockDim.x) ptr[a] = cnt[a];
-    for (int a = threadIdx.x; a < nT; a += blockDim.x) {
-      int pos = cnt[a];
-      for (int b = 0; b < nT; ++b) {
-        const size_t e = pass == 0 ? static_cast<size_t>(a) * nT + b : static_cast<size_t>(b) * nT + a;
-        if (m[e] != 0) idx[pos++] = b;
-      }
+  }
+  if (csc_warp && col0 < nT) {
+    int pos[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) pos[k] = col0 + k < nT ? cc[col0 + k] + rg[range * nT + col0 + k] : 0;
+    for (int r = r_lo; r < r_hi; ++r) {
+      const uint32_t bits = chunk_bits(row_of(r), col0, nT, vec);
+#pragma unroll
+      for (int k = 0; k < 16; ++k)
+        if ((bits >> k) & 1u) ri[pos[k]++] = r;
     }
-    __syncthreads();
   }
 }
 
 cudaError_t launch_build_lists(const uint8_t* mask, int mask_heads, int nT, int* row_ptr,
                                int* col_idx, int* col_ptr, int* row_idx, cudaStream_t stream) {
-  const int smem = (nT + 1) * static_cast<int>(sizeof(int));
+  const int smem = ListLayout::of(nT).smem_ints() * static_cast<int>(sizeof(int));
   if (smem > 48 * 1024) {
-    cudaError_t e =
-        cudaFuncSetAttribute(fa_lists_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    static std::atomic<unsigned long long> attr_done{0};
+    // the largest layout (nT = 8192) once per device, so that no later call
+    // needs to raise it again
+    cudaError_t e = smem_attr_once(attr_done, reinterpret_cast<const void*>(fa_lists_kernel),
+                                   ListLayout::of(8192).smem_ints() * static_cast<int>(sizeof(int)));
     if (e != cudaSuccess) return e;
   }
-  return launch_pdl(fa_lists_kernel, dim3(mask_heads), dim3(1024), smem, stream, mask, nT, row_ptr,
-                    col_idx, col_ptr, row_idx);
+  return launch_pdl(fa_lists_kernel, dim3(mask_heads), dim3(kListWarps * 32), smem, stream, mask,
+                    nT, row_ptr, col_idx, col_ptr, row_idx);
 }
 
 // ------------------------------------------------------------------ backward helpers

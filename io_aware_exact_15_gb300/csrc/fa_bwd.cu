@@ -551,18 +551,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     auto drain_dq = [&](uint32_t m, int t, int gg) -> bool {
       if (!__all_sync(0xffffffffu, wait_bar(bar(L::B_DQF), m & 1, wc))) return false;
       tc_fence_after();
-      // SPLIT: the second 32 columns go straight into dq1
-      constexpr int NCH = SPLIT ? 1 : D / 64;
-      uint32_t dq[NCH][32];
-#pragma unroll
-      for (int c = 0; c < NCH; ++c) tmem_ld32(tDQ + 32 * c, dq[c]);
-      if (SPLIT) tmem_ld32(tDQ + 32, dq1);
-      tmem_ld_wait();
-#pragma unroll
-      for (int c = 0; c < NCH; ++c) reg_fence(dq[c]);
-      if (SPLIT) reg_fence(dq1);
-      tc_fence_before();
-      mbar_arrive(bar(L::B_DQE));
       // Reduce-add through the TMA engine: the warp stages its 32 rows x 32
       // columns (4 KB, 128-byte swizzle), for d = 64 in its own staging
       // buffer, for d = 128 (the first 32 of its 64 columns) in its own rows
@@ -572,27 +560,62 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // receive exact zeros, since their P and dS rows are 0).
       const uint32_t stage =
           (L::OWN_STG ? sb + L::STG + half * L::CHUNK : dsbuf) + q4 * 4096;
-      if (SPLIT) {  // second half later, from the P rows
-        t1 = t;
-        g1 = gg;
-        dq1_live = true;
-      }
-#pragma unroll
-      for (int c = 0; c < NCH; ++c) {
-        if (c > 0 || L::OWN_STG) {  // the box staged here before has been read
-          if (lane == 0) bulk_wait_read_all();
-          __syncwarp();
-        }
+      auto stage_box = [&](const uint32_t (&x)[32], int c) {
 #pragma unroll
         for (int u = 0; u < 8; ++u)
-          st_shared_v4(stage + sw128_offset(lane, u), dq[c][4 * u], dq[c][4 * u + 1],
-                       dq[c][4 * u + 2], dq[c][4 * u + 3]);
+          st_shared_v4(stage + sw128_offset(lane, u), x[4 * u], x[4 * u + 1], x[4 * u + 2],
+                       x[4 * u + 3]);
         fence_async_smem();
         __syncwarp();
         if (lane == 0) {
           tma_reduce_add_3d(&tdq, stage, (D / 2) * half + 32 * c,
                             un.row0 + t * kTile + 32 * q4, un.bq0 + gg);
           bulk_commit();
+        }
+      };
+      if constexpr (!SPLIT && D == 128) {
+        // (d = 128 with dropout) one 32-column box in registers at a time:
+        // the first leaves before the second is read, which releases the
+        // TMEM columns a little later but keeps the drain within the
+        // register budget next to P's packed row
+        uint32_t dq[32];
+        tmem_ld32(tDQ, dq);
+        tmem_ld_wait();
+        reg_fence(dq);
+        stage_box(dq, 0);
+        tmem_ld32(tDQ + 32, dq);
+        tmem_ld_wait();
+        reg_fence(dq);
+        tc_fence_before();
+        mbar_arrive(bar(L::B_DQE));
+        if (lane == 0) bulk_wait_read_all();  // the first box has been read
+        __syncwarp();
+        stage_box(dq, 1);
+      } else {
+        // SPLIT: the second 32 columns go straight into dq1
+        constexpr int NCH = SPLIT ? 1 : D / 64;
+        uint32_t dq[NCH][32];
+#pragma unroll
+        for (int c = 0; c < NCH; ++c) tmem_ld32(tDQ + 32 * c, dq[c]);
+        if (SPLIT) tmem_ld32(tDQ + 32, dq1);
+        tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < NCH; ++c) reg_fence(dq[c]);
+        if (SPLIT) reg_fence(dq1);
+        tc_fence_before();
+        mbar_arrive(bar(L::B_DQE));
+        if (SPLIT) {  // second half later, from the P rows
+          t1 = t;
+          g1 = gg;
+          dq1_live = true;
+        }
+#pragma unroll
+        for (int c = 0; c < NCH; ++c) {
+          if (c > 0 || L::OWN_STG) {  // the box staged here before has been read
+            if (lane == 0) bulk_wait_read_all();
+            __syncwarp();
+          }
+          stage_box(dq[c], c);
         }
       }
       // d = 128: the staging rows are this warp's dS rows: the wait for the

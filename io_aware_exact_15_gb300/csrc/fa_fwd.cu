@@ -36,7 +36,10 @@ namespace fa {
 namespace {
 
 // BC: keys per key tile (128 except in the block-size sweep: 64 or 256).
-template <int D, int NS_ = 0, int BC = kTile>
+// CMP: the compact form of a one-query-tile CTA: 6 warps, tensor memory and
+// shared memory sized for one tile, so that two CTAs can share an SM where
+// both fit (at most 256 TMEM columns and ~113 KB of shared memory each).
+template <int D, int NS_ = 0, int BC = kTile, bool CMP = false>
 struct FwdSmem {
   static constexpr int CH = D / 64;             // 128-byte column chunks per row
   static constexpr int CHUNK = kTile * 128;     // query tile: [128 rows x 128 B] = 16 KB
@@ -44,12 +47,20 @@ struct FwdSmem {
   static constexpr int KCHUNK = BC * 128;       // key / value tile: [BC rows x 128 B]
   static constexpr int KTILE = CH * KCHUNK;     // one BC x D bf16 key or value tile
   static constexpr int KBOX = BC < kTile ? BC : kTile;  // rows of one K/V TMA box
-  // query tiles whose S and O fit the 512 TMEM columns (2 BC + 2 D for two)
-  static constexpr int NQT = (2 * BC + 2 * D <= 512) ? 2 : 1;
+  // query tiles per CTA in tensor memory (S and O of each: BC + D columns)
+  static constexpr int NQT = CMP ? 1 : 2;
+  static_assert(NQT * (BC + D) <= 512, "tensor memory budget");
+  static constexpr int QT = CMP ? 1 : 2;  // query tiles in shared memory
+  static constexpr int THREADS = CMP ? 192 : 320;
+  // columns allocated: the power of two that holds S and O of every tile
+  static constexpr int TCOLS = CMP ? (NQT * (BC + D) <= 128   ? 128
+                                      : NQT * (BC + D) <= 256 ? 256
+                                                              : 512)
+                                   : 512;
   // K/V ring slots (one tile each); NS_ != 0 overrides for the tile sweep
   static constexpr int NS = NS_ != 0 ? NS_ : ((D == 64) ? 8 : 5);
   static constexpr int Q = 0;
-  static constexpr int KV = Q + 2 * TILE;
+  static constexpr int KV = Q + QT * TILE;
   static constexpr int BAR = KV + NS * KTILE;
   static constexpr int B_Q = 0, B_KVF = 1, B_KVE = 1 + NS, B_SF = 1 + 2 * NS, B_PF = B_SF + 2,
                        B_OF = B_PF + 2, NBAR = B_OF + 1;
@@ -62,18 +73,20 @@ struct FwdSmem {
   static constexpr int T_O = NQT * BC;  // O_s at T_O + s * D
   static constexpr int ALLOC = MISC + 16 + 1024;  // + slack for 1024-byte alignment
   static_assert(ALLOC <= 232448, "shared memory budget");
+  // CTAs per SM the launch bounds ask for (registers then capped at 168)
+  static constexpr int MINB = (CMP && TCOLS <= 256 && ALLOC <= 113 * 1024) ? 2 : 1;
 };
 
-constexpr int kFwdThreads = 320;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleLog2 = 8.0f;  // lazy rescale threshold (factor 256)
 
-template <int D, int KIND, int NS_, int BC>
-__global__ void __launch_bounds__(kFwdThreads, 1)
+template <int D, int KIND, int NS_, int BC, bool CMP>
+__global__ void __launch_bounds__(FwdSmem<D, NS_, BC, CMP>::THREADS,
+                                  FwdSmem<D, NS_, BC, CMP>::MINB)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const FwdParams p) {
-  using L = FwdSmem<D, NS_, BC>;
+  using L = FwdSmem<D, NS_, BC, CMP>;
   static_assert(BC == kTile || (NS_ != 0 && KIND == kPlain),
                 "key tiles other than 128 exist only in the plain sweep instantiations");
   grid_dep_wait();  // the previous kernel's writes are visible from here on
@@ -87,9 +100,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::MISC + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // one query tile per CTA only in the tile-sweep instantiations (NS_ != 0),
-  // and always when TMEM holds a single query tile's S and O
-  const bool single = (NS_ != 0 && p.single_tile != 0) || L::NQT == 1;
+  // one query tile per CTA: the compact instantiations
+  constexpr bool single = L::NQT == 1;
   const int ntmax = (p.N + kTile - 1) / kTile;
   const int npairs = single ? ntmax : (ntmax + 1) / 2;
   const int BH = p.B * p.H;
@@ -153,11 +165,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     prefetch_tmap(&tv);
     const int y0 = sch.qt[0] * kTile;
     const int y1 = (sch.act[1] ? sch.qt[1] : sch.qt[0]) * kTile;
-    mbar_arrive_expect_tx(bar(L::B_Q), 2 * L::TILE);
+    mbar_arrive_expect_tx(bar(L::B_Q), L::QT * L::TILE);
 #pragma unroll
     for (int c = 0; c < L::CH; ++c) {
       tma_load_3d(sb + L::Q + c * L::CHUNK, &tq, bar(L::B_Q), 64 * c, row0 + y0, zq);
-      tma_load_3d(sb + L::Q + L::TILE + c * L::CHUNK, &tq, bar(L::B_Q), 64 * c, row0 + y1, zq);
+      if (L::QT == 2)
+        tma_load_3d(sb + L::Q + L::TILE + c * L::CHUNK, &tq, bar(L::B_Q), 64 * c, row0 + y1, zq);
     }
     FwdScheduleT<BC> first = sch;  // the first key tile, without advancing sch
     int kt0, mem0;
@@ -171,7 +184,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     }
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_alloc(smem_u32(tmem_slot), L::TCOLS);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -507,24 +520,23 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    tmem_dealloc(tmem, L::TCOLS);
   }
 }
 
-template <int D, int KIND, int NS_ = 0, int BC = kTile>
+template <int D, int KIND, int NS_ = 0, int BC = kTile, bool CMP = false>
 cudaError_t launch_fwd_d(const FwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                          const CUtensorMap& tv, cudaStream_t stream) {
-  using L = FwdSmem<D, NS_, BC>;
+  using L = FwdSmem<D, NS_, BC, CMP>;
   static std::atomic<unsigned long long> attr_done{0};
   cudaError_t e = smem_attr_once(
-      attr_done, reinterpret_cast<const void*>(fa_fwd_kernel<D, KIND, NS_, BC>), L::ALLOC);
+      attr_done, reinterpret_cast<const void*>(fa_fwd_kernel<D, KIND, NS_, BC, CMP>), L::ALLOC);
   if (e != cudaSuccess) return e;
   const int nT = (p.N + kTile - 1) / kTile;
-  const bool single = (NS_ != 0 && p.single_tile) || L::NQT == 1;
-  const int npairs = single ? nT : (nT + 1) / 2;
+  const int npairs = L::NQT == 1 ? nT : (nT + 1) / 2;
   const long long ctas = static_cast<long long>(npairs) * p.B * p.H;
-  return launch_pdl(fa_fwd_kernel<D, KIND, NS_, BC>, dim3(static_cast<unsigned>(ctas)),
-                    dim3(kFwdThreads), L::ALLOC, stream, tq, tk, tv, p);
+  return launch_pdl(fa_fwd_kernel<D, KIND, NS_, BC, CMP>, dim3(static_cast<unsigned>(ctas)),
+                    dim3(L::THREADS), L::ALLOC, stream, tq, tk, tv, p);
 }
 
 }  // namespace
@@ -538,6 +550,25 @@ cudaError_t launch_forward_config(const FwdParams& p, const CUtensorMap& tq, con
                                   const CUtensorMap& tv, int kv_stages, int key_tile,
                                   cudaStream_t stream) {
   const int code = p.d * 100000 + key_tile * 100 + kv_stages;
+  if (p.single_tile) {  // one query tile per CTA: the compact form
+    switch (code) {
+      case 12812802: return launch_fwd_d<128, kPlain, 2, 128, true>(p, tq, tk, tv, stream);
+      case 12812803: return launch_fwd_d<128, kPlain, 3, 128, true>(p, tq, tk, tv, stream);
+      case 12812804: return launch_fwd_d<128, kPlain, 4, 128, true>(p, tq, tk, tv, stream);
+      case 12812805: return launch_fwd_d<128, kPlain, 5, 128, true>(p, tq, tk, tv, stream);
+      case 12806404: return launch_fwd_d<128, kPlain, 4, 64, true>(p, tq, tk, tv, stream);
+      case 12806408: return launch_fwd_d<128, kPlain, 8, 64, true>(p, tq, tk, tv, stream);
+      case 12825602: return launch_fwd_d<128, kPlain, 2, 256, true>(p, tq, tk, tv, stream);
+      case 6412802: return launch_fwd_d<64, kPlain, 2, 128, true>(p, tq, tk, tv, stream);
+      case 6412804: return launch_fwd_d<64, kPlain, 4, 128, true>(p, tq, tk, tv, stream);
+      case 6412808: return launch_fwd_d<64, kPlain, 8, 128, true>(p, tq, tk, tv, stream);
+      case 6406408: return launch_fwd_d<64, kPlain, 8, 64, true>(p, tq, tk, tv, stream);
+      case 6406416: return launch_fwd_d<64, kPlain, 16, 64, true>(p, tq, tk, tv, stream);
+      case 6425602: return launch_fwd_d<64, kPlain, 2, 256, true>(p, tq, tk, tv, stream);
+      case 6425604: return launch_fwd_d<64, kPlain, 4, 256, true>(p, tq, tk, tv, stream);
+    }
+    return cudaErrorInvalidValue;
+  }
   switch (code) {
     case 12812802: return launch_fwd_d<128, kPlain, 2>(p, tq, tk, tv, stream);
     case 12812803: return launch_fwd_d<128, kPlain, 3>(p, tq, tk, tv, stream);
@@ -545,14 +576,11 @@ cudaError_t launch_forward_config(const FwdParams& p, const CUtensorMap& tq, con
     case 12812805: return launch_fwd_d<128, kPlain, 5>(p, tq, tk, tv, stream);
     case 12806404: return launch_fwd_d<128, kPlain, 4, 64>(p, tq, tk, tv, stream);
     case 12806408: return launch_fwd_d<128, kPlain, 8, 64>(p, tq, tk, tv, stream);
-    case 12825602: return launch_fwd_d<128, kPlain, 2, 256>(p, tq, tk, tv, stream);
     case 6412802: return launch_fwd_d<64, kPlain, 2>(p, tq, tk, tv, stream);
     case 6412804: return launch_fwd_d<64, kPlain, 4>(p, tq, tk, tv, stream);
     case 6412808: return launch_fwd_d<64, kPlain, 8>(p, tq, tk, tv, stream);
     case 6406408: return launch_fwd_d<64, kPlain, 8, 64>(p, tq, tk, tv, stream);
     case 6406416: return launch_fwd_d<64, kPlain, 16, 64>(p, tq, tk, tv, stream);
-    case 6425602: return launch_fwd_d<64, kPlain, 2, 256>(p, tq, tk, tv, stream);
-    case 6425604: return launch_fwd_d<64, kPlain, 4, 256>(p, tq, tk, tv, stream);
   }
   return cudaErrorInvalidValue;
 }

@@ -89,11 +89,17 @@ def test_blocksparse_64k_sampled_rows():
 
 # ---------------------------------------------------------------- integer work
 
-def _lists_on_gpu(mask, N, dev):
+def _lists_on_gpu(mask, N, dev, offset=0):
+    """offset: bytes by which the mask's device copy is shifted off its
+    allocation's alignment (the builder reads 16 bytes at a time only from a
+    16-byte aligned mask)."""
     mh, nT, _ = mask.shape
     nbytes = fa.fa_blocksparse_workspace_size(1, mh, N, 64, mh)
     ws = torch.full((nbytes,), 0x7F, dtype=torch.uint8, device=dev)
-    md = torch.from_numpy(np.ascontiguousarray(mask)).to(dev)
+    flat = torch.from_numpy(np.ascontiguousarray(mask).reshape(-1))
+    buf = torch.zeros(offset + flat.numel(), dtype=torch.uint8, device=dev)
+    buf[offset:] = flat.to(dev)
+    md = buf[offset:]
     assert fa.fa_blocksparse_build_lists(md, mh, N, ws, nbytes) == fa.FA_OK
     status_ok()
     words = ws.view(torch.int32).cpu().numpy()
@@ -105,15 +111,19 @@ def _lists_on_gpu(mask, N, dev):
     return rp, ci, cp, ri
 
 
-@pytest.mark.parametrize("N,mh,density", [(128, 1, 1.0), (1000, 2, 0.3), (65536, 1, None)])
-def test_tile_lists_bit_exact(N, mh, density):
+@pytest.mark.parametrize("N,mh,density,offset", [
+    (128, 1, 1.0, 0), (1000, 2, 0.3, 0), (65536, 1, None, 0), (4096, 3, 0.2, 1),
+    (4096, 1, 0.5, 0), (76800, 1, 0.01, 0), (262144, 1, 0.002, 0), (20000, 2, 0.05, 3)])
+def test_tile_lists_bit_exact(N, mh, density, offset):
+    # one mask tile row fits a warp's 512-column access (65536), several do
+    # (76800: 600 tiles, 262144: 2048), aligned and misaligned masks
     dev = device()
     nT = (N + 127) // 128
     if density is None:
         mask = W.band_random_block_mask(N, seed=2005, density=0.05)
     else:
         mask = W.random_block_mask(mh, nT, seed=N, density=density)
-    rp, ci, cp, ri = _lists_on_gpu(mask, N, dev)
+    rp, ci, cp, ri = _lists_on_gpu(mask, N, dev, offset)
     rp_o, ci_o, cp_o, ri_o = oracle.mask_lists(mask)
     assert np.array_equal(rp, rp_o) and np.array_equal(cp, cp_o)
     for h in range(mask.shape[0]):
