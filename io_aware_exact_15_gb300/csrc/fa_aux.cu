@@ -100,7 +100,7 @@ FA_DEV void block_exclusive_scan(int* a, int n, int* warp_tot) {
 
 __global__ void __launch_bounds__(kListWarps * 32) fa_lists_kernel(
     const uint8_t* __restrict__ mask, int nT, int* row_ptr, int* col_idx, int* col_ptr,
-    int* row_idx) {
+    int* row_idx, int* unit_order) {
   grid_dep_wait();  // the previous kernel's writes are visible from here on
   grid_dep_launch();
   extern __shared__ int lsm[];
@@ -115,6 +115,7 @@ __global__ void __launch_bounds__(kListWarps * 32) fa_lists_kernel(
   int* cp = col_ptr + static_cast<size_t>(h) * (nT + 1);
   int* ci = col_idx + static_cast<size_t>(h) * nT * nT;
   int* ri = row_idx + static_cast<size_t>(h) * nT * nT;
+  int* uo = unit_order + static_cast<size_t>(h) * nT;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool vec = (reinterpret_cast<uintptr_t>(mask) % 16 == 0) && (nT % 16 == 0);
   auto row_of = [&](int r) { return m + static_cast<size_t>(r) * nT; };
@@ -196,10 +197,23 @@ __global__ void __launch_bounds__(kListWarps * 32) fa_lists_kernel(
         if ((bits >> k) & 1u) ri[pos[k]++] = r;
     }
   }
+  // ---- backward unit order: key tiles by descending CSC length, ties by
+  // index (a key tile's rank counts the tiles that come before it), so that
+  // long units (a kept column of every query tile) start first
+  for (int t = threadIdx.x; t < nT; t += blockDim.x) {
+    const int ct = cc[t + 1] - cc[t];
+    int rank = 0;
+    for (int j = 0; j < nT; ++j) {
+      const int cj = cc[j + 1] - cc[j];
+      rank += (cj > ct) || (cj == ct && j < t);
+    }
+    uo[rank] = t;
+  }
 }
 
 cudaError_t launch_build_lists(const uint8_t* mask, int mask_heads, int nT, int* row_ptr,
-                               int* col_idx, int* col_ptr, int* row_idx, cudaStream_t stream) {
+                               int* col_idx, int* col_ptr, int* row_idx, int* unit_order,
+                               cudaStream_t stream) {
   const int smem = ListLayout::of(nT).smem_ints() * static_cast<int>(sizeof(int));
   if (smem > 48 * 1024) {
     static std::atomic<unsigned long long> attr_done{0};
@@ -210,7 +224,7 @@ cudaError_t launch_build_lists(const uint8_t* mask, int mask_heads, int nT, int*
     if (e != cudaSuccess) return e;
   }
   return launch_pdl(fa_lists_kernel, dim3(mask_heads), dim3(kListWarps * 32), smem, stream, mask,
-                    nT, row_ptr, col_idx, col_ptr, row_idx);
+                    nT, row_ptr, col_idx, col_ptr, row_idx, unit_order);
 }
 
 // ------------------------------------------------------------------ backward helpers

@@ -107,7 +107,18 @@ template <bool GQA>
 FA_DEV bool bwd_unit(int u, const BwdParams& p, int Hkv, int G, int ntmax, bool varlen,
                      BwdUnit& w) {
   int bkv;
-  bwd_cta_coords(u, p.B * Hkv, ntmax, p.causal != 0, bkv, w.kt);
+  if (p.lists.unit_order != nullptr) {
+    // block mask: rank-major over the key tiles ordered longest first (a
+    // kept column of every query tile is a unit nT times as long as an
+    // average one), every head of a rank together
+    const int BHkv = p.B * Hkv;
+    const int rank = u / BHkv;
+    bkv = u - rank * BHkv;
+    const int hm = p.lists.mask_heads == 1 ? 0 : bkv % p.H;
+    w.kt = p.lists.unit_order[hm * ntmax + rank];
+  } else {
+    bwd_cta_coords(u, p.B * Hkv, ntmax, p.causal != 0, bkv, w.kt);
+  }
   w.N = p.N;
   w.row0 = 0;
   w.zkv = bkv;

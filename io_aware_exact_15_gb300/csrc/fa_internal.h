@@ -64,11 +64,14 @@ constexpr int kTile = 128;  // query rows and keys per tile (Br = Bc = 128)
 //   csr: row_ptr [mask_heads][nT+1] (head-local offsets),
 //        col_idx [mask_heads][nT*nT] (ascending key tiles of each query tile)
 //   csc: col_ptr / row_idx, the same for each key tile (ascending query tiles)
+//   unit_order [mask_heads][nT]: key tiles by descending CSC length (ties by
+//        index): the order in which the backward takes its units
 struct TileLists {
   const int* row_ptr = nullptr;
   const int* col_idx = nullptr;
   const int* col_ptr = nullptr;
   const int* row_idx = nullptr;
+  const int* unit_order = nullptr;
   int mask_heads = 0;
   int nT = 0;
 };
@@ -178,7 +181,8 @@ cudaError_t launch_bwd_preprocess(const void* o, const void* dO, float* delta, f
 cudaError_t launch_dq_convert(const float* dq_acc, void* dq, long long n, float scale,
                               cudaStream_t stream);
 cudaError_t launch_build_lists(const uint8_t* mask, int mask_heads, int nT, int* row_ptr,
-                               int* col_idx, int* col_ptr, int* row_idx, cudaStream_t stream);
+                               int* col_idx, int* col_ptr, int* row_idx, int* unit_order,
+                               cudaStream_t stream);
 // schedule export (tests): per query tile the key tiles the forward visits
 // and per key tile the query tiles the backward visits
 cudaError_t launch_schedule_export(int N, int causal, const TileLists& lists, int heads,

@@ -108,7 +108,8 @@ def _lists_on_gpu(mask, N, dev, offset=0):
     base = 2 * mh * (nT + 1)
     ci = words[base:base + mh * nT * nT].reshape(mh, nT * nT)
     ri = words[base + mh * nT * nT:base + 2 * mh * nT * nT].reshape(mh, nT * nT)
-    return rp, ci, cp, ri
+    uo = words[base + 2 * mh * nT * nT:base + 2 * mh * nT * nT + mh * nT].reshape(mh, nT)
+    return rp, ci, cp, ri, uo
 
 
 @pytest.mark.parametrize("N,mh,density,offset", [
@@ -123,12 +124,14 @@ def test_tile_lists_bit_exact(N, mh, density, offset):
         mask = W.band_random_block_mask(N, seed=2005, density=0.05)
     else:
         mask = W.random_block_mask(mh, nT, seed=N, density=density)
-    rp, ci, cp, ri = _lists_on_gpu(mask, N, dev, offset)
+    rp, ci, cp, ri, uo = _lists_on_gpu(mask, N, dev, offset)
     rp_o, ci_o, cp_o, ri_o = oracle.mask_lists(mask)
     assert np.array_equal(rp, rp_o) and np.array_equal(cp, cp_o)
     for h in range(mask.shape[0]):
         assert np.array_equal(ci[h, :rp[h, -1]], ci_o[h])
         assert np.array_equal(ri[h, :cp[h, -1]], ri_o[h])
+        # backward order: key tiles by descending column count, ties by index
+        assert np.array_equal(uo[h], np.argsort(-np.diff(cp_o[h]), kind="stable"))
 
 
 def _schedule(N, causal, mask, dev):
