@@ -103,11 +103,11 @@ struct BwdUnit {
 
 // Unit u -> its geometry.  False when the key tile lies past the end of its
 // (variable-length) sequence; every role of the CTA skips such a unit alike.
-template <bool GQA>
+template <bool GQA, bool SPARSE>
 FA_DEV bool bwd_unit(int u, const BwdParams& p, int Hkv, int G, int ntmax, bool varlen,
                      BwdUnit& w) {
   int bkv;
-  if (p.lists.unit_order != nullptr) {
+  if (SPARSE) {
     // block mask: rank-major over the key tiles ordered longest first (a
     // kept column of every query tile is a unit nT times as long as an
     // average one), every head of a rank together
@@ -145,8 +145,9 @@ FA_DEV bool bwd_unit(int u, const BwdParams& p, int Hkv, int G, int ntmax, bool 
 // drains and its dV, dK leave TMEM, and the Q / dO rings and every step
 // barrier run on across units.
 // DQ = false: no dQ product and no reduce-adds (dQ comes from the query-tile
-// pass of the deterministic backward)
-template <int D, int KIND, bool DQ = true>
+// pass of the deterministic backward).  SPARSE: a block mask's lists (plain
+// kind), units in the lists' longest-first order.
+template <int D, int KIND, bool DQ = true, bool SPARSE = false>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     fa_bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
@@ -184,7 +185,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                            : static_cast<int>(blockIdx.x));
   };
   auto unit_at = [&](int u, BwdUnit& w) {
-    return bwd_unit<GQA>(u, p, Hkv, G, ntmax, varlen, w);
+    return bwd_unit<GQA, SPARSE>(u, p, Hkv, G, ntmax, varlen, w);
   };
   // Split last round: when the last round's units fill at most half the
   // grid, each runs as two halves of its query-tile walk on two CTAs.  Only
@@ -197,7 +198,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int nround = (nunits + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x);
   const int last0 = (nround - 1) * static_cast<int>(gridDim.x);  // first unit of the last round
   const int mlast = nunits - last0;
-  const bool split = D == 128 && p.part != nullptr && p.lists.col_ptr == nullptr && !varlen && nround > 1 &&
+  const bool split = D == 128 && !SPARSE && p.part != nullptr && !varlen && nround > 1 &&
                      2 * mlast <= static_cast<int>(gridDim.x) && mlast <= p.nslot &&
                      G * (p.causal ? 1 : ntmax) >= 8;
   // k-th item of this CTA: unit u and half uh (-1: the whole unit); false
@@ -952,14 +953,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
 }
 
-template <int D, int KIND, bool DQ = true>
+template <int D, int KIND, bool DQ = true, bool SPARSE = false>
 cudaError_t launch_bwd_d(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                          const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq,
                          cudaStream_t stream) {
   using L = BwdSmem<D>;
   static std::atomic<unsigned long long> attr_done{0};
   cudaError_t e = smem_attr_once(
-      attr_done, reinterpret_cast<const void*>(fa_bwd_kernel<D, KIND, DQ>), L::ALLOC);
+      attr_done, reinterpret_cast<const void*>(fa_bwd_kernel<D, KIND, DQ, SPARSE>), L::ALLOC);
   if (e != cudaSuccess) return e;
   const int nT = (p.N + kTile - 1) / kTile;
   const long long units = static_cast<long long>(nT) * p.B * (p.Hkv > 0 ? p.Hkv : p.H);
@@ -968,7 +969,7 @@ cudaError_t launch_bwd_d(const BwdParams& p, const CUtensorMap& tq, const CUtens
   const int sms = sm_count();
   if (sms <= 0) return cudaErrorInvalidDevice;
   const long long ctas = units < sms ? units : sms;
-  return launch_pdl(fa_bwd_kernel<D, KIND, DQ>, dim3(static_cast<unsigned>(ctas)),
+  return launch_pdl(fa_bwd_kernel<D, KIND, DQ, SPARSE>, dim3(static_cast<unsigned>(ctas)),
                     dim3(kBwdThreads), L::ALLOC, stream, tq, tk, tv, tdo, tdq, p);
 }
 
@@ -984,6 +985,12 @@ cudaError_t launch_backward_main(const BwdParams& p, const CUtensorMap& tq, cons
     if (kind != kPlain) return cudaErrorInvalidValue;
     if (p.d == 64) return launch_bwd_d<64, kPlain, false>(p, tq, tk, tv, tdo, tdq, stream);
     if (p.d == 128) return launch_bwd_d<128, kPlain, false>(p, tq, tk, tv, tdo, tdq, stream);
+    return cudaErrorInvalidValue;
+  }
+  if (p.lists.col_ptr != nullptr) {  // block mask: plain layout only
+    if (kind != kPlain || p.lists.unit_order == nullptr) return cudaErrorInvalidValue;
+    if (p.d == 64) return launch_bwd_d<64, kPlain, true, true>(p, tq, tk, tv, tdo, tdq, stream);
+    if (p.d == 128) return launch_bwd_d<128, kPlain, true, true>(p, tq, tk, tv, tdo, tdq, stream);
     return cudaErrorInvalidValue;
   }
   if (p.d == 64) {

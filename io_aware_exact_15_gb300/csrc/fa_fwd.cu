@@ -57,8 +57,9 @@ struct FwdSmem {
                                       : NQT * (BC + D) <= 256 ? 256
                                                               : 512)
                                    : 512;
-  // K/V ring slots (one tile each); NS_ != 0 overrides for the tile sweep
-  static constexpr int NS = NS_ != 0 ? NS_ : ((D == 64) ? 8 : 5);
+  // K/V ring slots (one tile each); NS_ != 0 overrides for the tile sweep.
+  // The compact form keeps its shared memory within half an SM's.
+  static constexpr int NS = NS_ != 0 ? NS_ : CMP ? ((D == 64) ? 4 : 2) : ((D == 64) ? 8 : 5);
   static constexpr int Q = 0;
   static constexpr int KV = Q + QT * TILE;
   static constexpr int BAR = KV + NS * KTILE;
@@ -585,23 +586,38 @@ cudaError_t launch_forward_config(const FwdParams& p, const CUtensorMap& tq, con
   return cudaErrorInvalidValue;
 }
 
+template <int D, bool CMP>
+cudaError_t launch_forward_kind(int kind, const FwdParams& p, const CUtensorMap& tq,
+                                const CUtensorMap& tk, const CUtensorMap& tv,
+                                cudaStream_t stream) {
+  if (kind == kGeneralDropout)
+    return launch_fwd_d<D, kGeneralDropout, 0, kTile, CMP>(p, tq, tk, tv, stream);
+  if (kind == kGeneral) return launch_fwd_d<D, kGeneral, 0, kTile, CMP>(p, tq, tk, tv, stream);
+  if (kind == kGrouped) return launch_fwd_d<D, kGrouped, 0, kTile, CMP>(p, tq, tk, tv, stream);
+  return launch_fwd_d<D, kPlain, 0, kTile, CMP>(p, tq, tk, tv, stream);
+}
+
 cudaError_t launch_forward(const FwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                            const CUtensorMap& tv, cudaStream_t stream) {
   const int kind = p.drop.t ? kGeneralDropout
                    : p.cu_seqlens ? kGeneral
                    : (p.Hkv > 0 && p.Hkv != p.H) ? kGrouped : kPlain;
-  if (p.d == 64) {
-    if (kind == kGeneralDropout) return launch_fwd_d<64, kGeneralDropout>(p, tq, tk, tv, stream);
-    if (kind == kGeneral) return launch_fwd_d<64, kGeneral>(p, tq, tk, tv, stream);
-    if (kind == kGrouped) return launch_fwd_d<64, kGrouped>(p, tq, tk, tv, stream);
-    return launch_fwd_d<64, kPlain>(p, tq, tk, tv, stream);
-  }
-  if (p.d == 128) {
-    if (kind == kGeneralDropout) return launch_fwd_d<128, kGeneralDropout>(p, tq, tk, tv, stream);
-    if (kind == kGeneral) return launch_fwd_d<128, kGeneral>(p, tq, tk, tv, stream);
-    if (kind == kGrouped) return launch_fwd_d<128, kGrouped>(p, tq, tk, tv, stream);
-    return launch_fwd_d<128, kPlain>(p, tq, tk, tv, stream);
-  }
+  // Small grids (at most four waves of two-tile CTAs: BERT- or GPT-2-sized
+  // batches) run the compact form, one query tile per CTA and two CTAs per
+  // SM: one CTA's start and end overlap the other's steps, and the finer
+  // grain evens out the last wave (measured: B8 H12 N1024 causal d = 64
+  // forward 33.2 -> 29.6 us, B8 H16 N512 20.2 -> 19.4 us; at B4 H16 N4096 the
+  // two-tile form is 4 % faster at d = 64 and 8 % at d = 128).
+  const int nT = (p.N + kTile - 1) / kTile;
+  const long long pairs = static_cast<long long>((nT + 1) / 2) * p.B * p.H;
+  const int sms = sm_count();
+  const bool compact = sms > 0 && pairs <= 4LL * sms;
+  if (p.d == 64)
+    return compact ? launch_forward_kind<64, true>(kind, p, tq, tk, tv, stream)
+                   : launch_forward_kind<64, false>(kind, p, tq, tk, tv, stream);
+  if (p.d == 128)
+    return compact ? launch_forward_kind<128, true>(kind, p, tq, tk, tv, stream)
+                   : launch_forward_kind<128, false>(kind, p, tq, tk, tv, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -31,6 +31,17 @@ def test_forward_small_full(N, d, causal):
     o, lse = run_forward(q, k, v, scale, causal, dev)
     o_ref, lse_ref = parity.oracle_forward(q, k, v, scale, causal)
     parity.check_forward(o, lse, o_ref, lse_ref, f"N={N} d={d} causal={causal}")
+    # grids this small run the compact one-tile form; the two-tile form of
+    # long sequences (same ring depth) on the same ragged lengths
+    B, H = 2, 2
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    o2 = torch.full_like(qd, float("nan"))
+    lse2 = torch.full((B, H, N), float("nan"), dtype=torch.float32, device=dev)
+    assert fa.fa_debug_forward_config(qd, kd, vd, o2, lse2, B, H, N, d, scale, causal, 256, 128,
+                                      8 if d == 64 else 5) == fa.FA_OK
+    status_ok()
+    parity.check_forward(o2.cpu(), lse2.cpu(), o_ref, lse_ref,
+                         f"two-tile form N={N} d={d} causal={causal}")
 
 
 def test_forward_scale_and_peaked_keys():

@@ -159,3 +159,31 @@ def test_varlen_workload_sampled_rows():
         parity.check_grad(dq[None, :, sl][:, :, rows], dq_r, "dQ", f"seq {i}")
         parity.check_grad(dk[None, :, sl][:, :, rows], dk_r, "dK", f"seq {i}")
         parity.check_grad(dv[None, :, sl][:, :, rows], dv_r, "dV", f"seq {i}")
+
+
+@pytest.mark.parametrize("p_drop", [0.0, 0.2])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("d", [64, 128])
+def test_varlen_large_batch_two_tile_path(d, causal, p_drop):
+    # Ten sequences up to 1100 tokens with 16 query heads over 4 K/V heads:
+    # 5 query-tile pairs x 10 x 16 = 800 CTAs of two tiles, more than the
+    # forward's small-grid limit (4 x 152), so the two-tile form runs here
+    # (the small batches above take the compact one-tile form).
+    dev = device()
+    rng = np.random.default_rng(77 + d + causal)
+    lens = [1100, 0, 1] + [int(x) for x in rng.integers(200, 1101, 7)]
+    H, Hkv = 16, 4
+    q, k, v, do, cu = make(H, Hkv, lens, d, seed=sum(lens) + d + causal)
+    scale = 1.0 / d ** 0.5
+    drop = (p_drop, 0x5EED + d, 11) if p_drop > 0 else (0.0, 0, 0)
+    o, lse, dq, dk, dv = run(q, k, v, do, cu, scale, causal, dev, drop=drop)
+    what = f"large varlen d={d} causal={causal} p={p_drop}"
+    f = parity.f64
+    od = drop if p_drop > 0 else None
+    o_ref, lse_ref = oracle.forward_varlen(f(q), f(k), f(v), cu, scale, causal=causal, dropout=od)
+    parity.check_forward(o, lse, o_ref, lse_ref, what, o_scale=parity.keep_scale(p_drop))
+    dq_r, dk_r, dv_r = oracle.backward_varlen(f(q), f(k), f(v), f(do), cu, scale, causal=causal,
+                                              dropout=od)
+    parity.check_grad(dq, dq_r, "dQ", what)
+    parity.check_grad(dk, dk_r, "dK", what)
+    parity.check_grad(dv, dv_r, "dV", what)
