@@ -677,6 +677,21 @@ def run_reference(args, rank, world):
             "gpu_launches": 0}
 
 
+def tile_model_kv_bytes(B, H, N, d, rows, causal):
+    """K and V bytes the forward's CTAs stream with no reuse between CTAs
+    (the K/V term of the tile IO model): every CTA of `rows` query rows reads
+    every 128-key tile it needs, all of them (dense) or those up to its last
+    row (causal).  The row block, not the key tile, sets this."""
+    nT = (N + 127) // 128
+    per = rows // 128
+    ctas = (nT + per - 1) // per
+    if causal:
+        tiles = sum(min(nT, per * (c + 1)) for c in range(ctas))
+    else:
+        tiles = ctas * nT
+    return int(B * H * tiles * 2 * 128 * d * 2)
+
+
 SWEEP_STAGES = {(128, 128): (2, 3, 4, 5), (128, 64): (4, 8), (128, 256): (2,),
                 (64, 128): (2, 4, 8), (64, 64): (8, 16), (64, 256): (2, 4)}
 
@@ -726,17 +741,14 @@ def run_tile_sweep(args):
         b.record()
         torch.cuda.synchronize()
         ms = a.elapsed_time(b) / args.steps
-        nT = (N + 127) // 128
         br = 256 if rows == "default" else rows
-        # K and V bytes a CTA streams, times the CTAs (the tile-model IO term:
-        # the row block sets the passes over K and V, the key tile does not)
-        kv_passes = B * H * ((nT + 1) // 2 if br == 256 else nT)
         print(json.dumps({"sweep": "forward tile configuration", "workload": w.name,
                           "rows_per_cta": br, "key_tile": bc,
                           "kv_stages": st if st else "fa_forward",
                           "ms": round(ms, 4), "tflops": round(ff / (ms * 1e-3) / 1e12, 1),
                           "frac_of_peak": round(ff / (ms * 1e-3) / 1e12 / peak, 4),
-                          "tile_model_kv_bytes": int(kv_passes) * 2 * N * d * 2}), flush=True)
+                          "tile_model_kv_bytes": tile_model_kv_bytes(B, H, N, d, br,
+                                                                     w.causal)}), flush=True)
     if fa.fa_get_device_status() != fa.FA_OK:
         raise RuntimeError("device status after the sweep")
 

@@ -240,7 +240,7 @@ fa_status fa_backward_dropout(const void* q, const void* k, const void* v, const
                               size_t workspace_bytes, cudaStream_t stream);
 
 /* Bytes of workspace the block-sparse calls need: the CSR and CSC tile
- * lists of the mask (4 * mask_heads * (2*(nT+1) + 2*nT*nT + nT) bytes,
+ * lists of the mask (4 * mask_heads * (2*(nT+1) + 2*nT*nT + nT + 1) bytes,
  * rounded up to 256) followed by the fa_backward workspace.  The forward uses
  * only the list part. */
 size_t fa_blocksparse_workspace_size(int B, int H, int N, int d, int mask_heads);
@@ -254,8 +254,11 @@ size_t fa_blocksparse_workspace_size(int B, int H, int N, int d, int mask_heads)
  *   col_idx int32 [mask_heads, nT*nT]  ascending key tiles of each query tile
  *   row_idx int32 [mask_heads, nT*nT]  ascending query tiles of each key tile
  *   order   int32 [mask_heads, nT]     key tiles by descending row_idx list
- *                                      length, ties by index: the order in
- *                                      which the backward takes key tiles
+ *                                      length, ties by index
+ *   nlong   int32 [mask_heads]         how many key tiles have more than
+ *                                      twice the mean list length
+ * The backward takes the nlong longest key tiles of every head first, then
+ * each head's other key tiles in that order, head by head.
  * Integer work, bit-exact.  nT must be <= 8192.
  */
 fa_status fa_blocksparse_build_lists(const uint8_t* block_mask, int mask_heads, int N,

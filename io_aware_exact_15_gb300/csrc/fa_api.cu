@@ -158,7 +158,7 @@ BwdWorkspace bwd_ws(void* ws, int B, int H, int N, int d) {
 
 size_t lists_bytes(int N, int mask_heads) {
   const size_t nT = static_cast<size_t>(num_tiles(N));
-  return align256(sizeof(int) * mask_heads * (2 * (nT + 1) + 2 * nT * nT + nT));
+  return align256(sizeof(int) * mask_heads * (2 * (nT + 1) + 2 * nT * nT + nT + 1));
 }
 
 fa::TileLists lists_in(void* ws, int N, int mask_heads) {
@@ -170,6 +170,7 @@ fa::TileLists lists_in(void* ws, int N, int mask_heads) {
   L.col_idx = base + 2 * mask_heads * (nT + 1);
   L.row_idx = L.col_idx + mask_heads * nT * nT;
   L.unit_order = L.row_idx + mask_heads * nT * nT;
+  L.nlong = L.unit_order + mask_heads * nT;
   L.mask_heads = mask_heads;
   L.nT = static_cast<int>(nT);
   return L;
@@ -180,7 +181,7 @@ fa_status build_lists(const uint8_t* mask, int mask_heads, int N, void* ws, cuda
   FA_CUDA(fa::launch_build_lists(mask, mask_heads, L.nT, const_cast<int*>(L.row_ptr),
                                  const_cast<int*>(L.col_idx), const_cast<int*>(L.col_ptr),
                                  const_cast<int*>(L.row_idx), const_cast<int*>(L.unit_order),
-                                 stream));
+                                 const_cast<int*>(L.nlong), stream));
   return FA_OK;
 }
 

@@ -100,10 +100,10 @@ FA_DEV void block_exclusive_scan(int* a, int n, int* warp_tot) {
 
 __global__ void __launch_bounds__(kListWarps * 32) fa_lists_kernel(
     const uint8_t* __restrict__ mask, int nT, int* row_ptr, int* col_idx, int* col_ptr,
-    int* row_idx, int* unit_order) {
+    int* row_idx, int* unit_order, int* nlong) {
   grid_dep_wait();  // the previous kernel's writes are visible from here on
   grid_dep_launch();
-  extern __shared__ int lsm[];
+  extern __shared__ __align__(16) int lsm[];
   __shared__ int warp_tot[33];
   const ListLayout L = ListLayout::of(nT);
   int* rc = lsm;                 // [nT + 1] row counts -> CSR offsets
@@ -198,22 +198,39 @@ __global__ void __launch_bounds__(kListWarps * 32) fa_lists_kernel(
     }
   }
   // ---- backward unit order: key tiles by descending CSC length, ties by
-  // index (a key tile's rank counts the tiles that come before it), so that
-  // long units (a kept column of every query tile) start first
+  // index (a key tile's rank counts the tiles that come before it), and how
+  // many of them are long (more than twice the mean length: e.g. a kept
+  // column of every query tile), which the backward starts first
+  __syncthreads();  // the CSC pass has read its starts from rg
+  int* cnt = rg + ((4 - ((2 * (nT + 1)) & 3)) & 3);  // 16-byte aligned, [nT4]
+  const int nT4 = (nT + 3) & ~3;
+  for (int t = threadIdx.x; t < nT4; t += blockDim.x) cnt[t] = t < nT ? cc[t + 1] - cc[t] : -1;
+  __shared__ int nlong_s;
+  if (threadIdx.x == 0) nlong_s = 0;
+  __syncthreads();
+  const long long total = cc[nT];
+  const int4* c4 = reinterpret_cast<const int4*>(cnt);
   for (int t = threadIdx.x; t < nT; t += blockDim.x) {
-    const int ct = cc[t + 1] - cc[t];
+    const int ct = cnt[t];
     int rank = 0;
-    for (int j = 0; j < nT; ++j) {
-      const int cj = cc[j + 1] - cc[j];
-      rank += (cj > ct) || (cj == ct && j < t);
+    for (int j4 = 0; j4 < nT4 / 4; ++j4) {
+      const int4 v = c4[j4];
+      const int j = 4 * j4;
+      rank += (v.x > ct) || (v.x == ct && j < t);
+      rank += (v.y > ct) || (v.y == ct && j + 1 < t);
+      rank += (v.z > ct) || (v.z == ct && j + 2 < t);
+      rank += (v.w > ct) || (v.w == ct && j + 3 < t);
     }
     uo[rank] = t;
+    if (static_cast<long long>(ct) * nT > 2 * total) atomicAdd(&nlong_s, 1);
   }
+  __syncthreads();
+  if (threadIdx.x == 0) nlong[h] = nlong_s;
 }
 
 cudaError_t launch_build_lists(const uint8_t* mask, int mask_heads, int nT, int* row_ptr,
                                int* col_idx, int* col_ptr, int* row_idx, int* unit_order,
-                               cudaStream_t stream) {
+                               int* nlong, cudaStream_t stream) {
   const int smem = ListLayout::of(nT).smem_ints() * static_cast<int>(sizeof(int));
   if (smem > 48 * 1024) {
     static std::atomic<unsigned long long> attr_done{0};
@@ -224,7 +241,7 @@ cudaError_t launch_build_lists(const uint8_t* mask, int mask_heads, int nT, int*
     if (e != cudaSuccess) return e;
   }
   return launch_pdl(fa_lists_kernel, dim3(mask_heads), dim3(kListWarps * 32), smem, stream, mask,
-                    nT, row_ptr, col_idx, col_ptr, row_idx, unit_order);
+                    nT, row_ptr, col_idx, col_ptr, row_idx, unit_order, nlong);
 }
 
 // ------------------------------------------------------------------ backward helpers

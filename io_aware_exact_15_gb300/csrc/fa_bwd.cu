@@ -105,15 +105,25 @@ struct BwdUnit {
 // (variable-length) sequence; every role of the CTA skips such a unit alike.
 template <bool GQA, bool SPARSE>
 FA_DEV bool bwd_unit(int u, const BwdParams& p, int Hkv, int G, int ntmax, bool varlen,
-                     BwdUnit& w) {
+                     int nlong, BwdUnit& w) {
   int bkv;
   if (SPARSE) {
-    // block mask: rank-major over the key tiles ordered longest first (a
-    // kept column of every query tile is a unit nT times as long as an
-    // average one), every head of a rank together
+    // block mask, key tiles of each head ordered longest first: the nlong
+    // long ones of every head come first, rank-major (a kept column of every
+    // query tile is a unit as long as dozens of others: started late it
+    // would end the kernel late), then the rest head by head, so that one
+    // head's Q and dO stay in L2 while its units run
     const int BHkv = p.B * Hkv;
-    const int rank = u / BHkv;
-    bkv = u - rank * BHkv;
+    const int n1 = nlong * BHkv;
+    int rank;
+    if (u < n1) {
+      rank = u / BHkv;
+      bkv = u - rank * BHkv;
+    } else {
+      const int v = u - n1, per = ntmax - nlong;
+      bkv = v / per;
+      rank = nlong + (v - bkv * per);
+    }
     const int hm = p.lists.mask_heads == 1 ? 0 : bkv % p.H;
     w.kt = p.lists.unit_order[hm * ntmax + rank];
   } else {
@@ -184,8 +194,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     return base + ((k & 1) ? static_cast<int>(gridDim.x - 1 - blockIdx.x)
                            : static_cast<int>(blockIdx.x));
   };
+  // block mask: the most long key tiles any mask head has (the same for
+  // every role of every CTA), read once the lists are visible (below)
+  int nlong = 0;
   auto unit_at = [&](int u, BwdUnit& w) {
-    return bwd_unit<GQA, SPARSE>(u, p, Hkv, G, ntmax, varlen, w);
+    return bwd_unit<GQA, SPARSE>(u, p, Hkv, G, ntmax, varlen, nlong, w);
   };
   // Split last round: when the last round's units fill at most half the
   // grid, each runs as two halves of its query-tile walk on two CTAs.  Only
@@ -265,6 +278,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   grid_dep_wait();  // the previous kernel's writes are visible from here on
   const uint32_t tmem = *tmem_slot;
   const WaitCtl wc{abort_flag, p.err, p.wait_ns};
+  if (SPARSE)
+    for (int h = 0; h < p.lists.mask_heads; ++h) nlong = max(nlong, p.lists.nlong[h]);
 
   using Sched = BwdPartSchedule<Sched0>;
 
@@ -988,7 +1003,8 @@ cudaError_t launch_backward_main(const BwdParams& p, const CUtensorMap& tq, cons
     return cudaErrorInvalidValue;
   }
   if (p.lists.col_ptr != nullptr) {  // block mask: plain layout only
-    if (kind != kPlain || p.lists.unit_order == nullptr) return cudaErrorInvalidValue;
+    if (kind != kPlain || p.lists.unit_order == nullptr || p.lists.nlong == nullptr)
+      return cudaErrorInvalidValue;
     if (p.d == 64) return launch_bwd_d<64, kPlain, true, true>(p, tq, tk, tv, tdo, tdq, stream);
     if (p.d == 128) return launch_bwd_d<128, kPlain, true, true>(p, tq, tk, tv, tdo, tdq, stream);
     return cudaErrorInvalidValue;

@@ -66,12 +66,14 @@ constexpr int kTile = 128;  // query rows and keys per tile (Br = Bc = 128)
 //   csc: col_ptr / row_idx, the same for each key tile (ascending query tiles)
 //   unit_order [mask_heads][nT]: key tiles by descending CSC length (ties by
 //        index): the order in which the backward takes its units
+//   nlong [mask_heads]: how many of them are longer than twice the mean
 struct TileLists {
   const int* row_ptr = nullptr;
   const int* col_idx = nullptr;
   const int* col_ptr = nullptr;
   const int* row_idx = nullptr;
   const int* unit_order = nullptr;
+  const int* nlong = nullptr;
   int mask_heads = 0;
   int nT = 0;
 };
@@ -182,7 +184,7 @@ cudaError_t launch_dq_convert(const float* dq_acc, void* dq, long long n, float 
                               cudaStream_t stream);
 cudaError_t launch_build_lists(const uint8_t* mask, int mask_heads, int nT, int* row_ptr,
                                int* col_idx, int* col_ptr, int* row_idx, int* unit_order,
-                               cudaStream_t stream);
+                               int* nlong, cudaStream_t stream);
 // schedule export (tests): per query tile the key tiles the forward visits
 // and per key tile the query tiles the backward visits
 cudaError_t launch_schedule_export(int N, int causal, const TileLists& lists, int heads,

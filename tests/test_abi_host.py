@@ -40,7 +40,7 @@ def test_workspace_sizes():
     a256 = lambda x: (x + 255) // 256 * 256
     assert fa.fa_backward_workspace_size(B, H, N, d) == a256(4 * rows) + a256(4 * rows * d)
     nT = (N + 127) // 128
-    lists = a256(4 * 1 * (2 * (nT + 1) + 2 * nT * nT + nT))
+    lists = a256(4 * 1 * (2 * (nT + 1) + 2 * nT * nT + nT + 1))
     assert fa.fa_blocksparse_workspace_size(B, H, N, d, 1) == lists + \
         fa.fa_backward_workspace_size(B, H, N, d)
     assert fa.fa_backward_workspace_size(0, 1, 1, 64) == 0

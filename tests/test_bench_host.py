@@ -65,3 +65,15 @@ def test_oracle_job_units_and_flops(name):
     heads = w.H if w.varlen else w.B * w.H
     assert total == heads
     assert per_unit * total == pytest.approx(W.fwd_bwd_flops(w))
+
+
+def test_tile_model_kv_bytes():
+    # dense: every CTA streams all nT key tiles (K and V, 128 x d bf16 each)
+    tile = 2 * 128 * 64 * 2
+    assert bench.tile_model_kv_bytes(1, 1, 512, 64, 256, False) == 2 * 4 * tile
+    assert bench.tile_model_kv_bytes(1, 1, 512, 64, 128, False) == 4 * 4 * tile
+    # causal, 128-row CTAs: 1 + 2 + 3 + 4 tiles; 256-row CTAs: 2 + 4
+    assert bench.tile_model_kv_bytes(1, 1, 512, 64, 128, True) == 10 * tile
+    assert bench.tile_model_kv_bytes(1, 1, 512, 64, 256, True) == 6 * tile
+    # ragged: N = 300 has 3 tiles; the last 256-row CTA reaches tile 2 only
+    assert bench.tile_model_kv_bytes(1, 1, 300, 64, 256, True) == (2 + 3) * tile

@@ -108,8 +108,10 @@ def _lists_on_gpu(mask, N, dev, offset=0):
     base = 2 * mh * (nT + 1)
     ci = words[base:base + mh * nT * nT].reshape(mh, nT * nT)
     ri = words[base + mh * nT * nT:base + 2 * mh * nT * nT].reshape(mh, nT * nT)
-    uo = words[base + 2 * mh * nT * nT:base + 2 * mh * nT * nT + mh * nT].reshape(mh, nT)
-    return rp, ci, cp, ri, uo
+    o0 = base + 2 * mh * nT * nT
+    uo = words[o0:o0 + mh * nT].reshape(mh, nT)
+    nl = words[o0 + mh * nT:o0 + mh * nT + mh]
+    return rp, ci, cp, ri, uo, nl
 
 
 @pytest.mark.parametrize("N,mh,density,offset", [
@@ -124,14 +126,17 @@ def test_tile_lists_bit_exact(N, mh, density, offset):
         mask = W.band_random_block_mask(N, seed=2005, density=0.05)
     else:
         mask = W.random_block_mask(mh, nT, seed=N, density=density)
-    rp, ci, cp, ri, uo = _lists_on_gpu(mask, N, dev, offset)
+    rp, ci, cp, ri, uo, nl = _lists_on_gpu(mask, N, dev, offset)
     rp_o, ci_o, cp_o, ri_o = oracle.mask_lists(mask)
     assert np.array_equal(rp, rp_o) and np.array_equal(cp, cp_o)
     for h in range(mask.shape[0]):
         assert np.array_equal(ci[h, :rp[h, -1]], ci_o[h])
         assert np.array_equal(ri[h, :cp[h, -1]], ri_o[h])
-        # backward order: key tiles by descending column count, ties by index
-        assert np.array_equal(uo[h], np.argsort(-np.diff(cp_o[h]), kind="stable"))
+        # backward order: key tiles by descending column count, ties by index;
+        # long key tiles: count above twice the mean (count * nT > 2 * nnz)
+        cnt = np.diff(cp_o[h])
+        assert np.array_equal(uo[h], np.argsort(-cnt, kind="stable"))
+        assert nl[h] == int(np.count_nonzero(cnt.astype(np.int64) * nT > 2 * int(cnt.sum())))
 
 
 def _schedule(N, causal, mask, dev):
