@@ -73,7 +73,8 @@ fa_status fa_forward(const void* q, const void* k, const void* v, void* o, float
  * than 64 key tiles (B*H*ceil(N/128)) also min(tiles/2, 96) slots of
  * 128 KiB plus 8 bytes each (at most 12 MiB): fp32 dK, dV partial sums
  * of key tiles whose query-tile walk the last round of the persistent
- * backward splits between two SMs.  O(B*H*N*d), never O(N^2). */
+ * backward splits between two SMs; then one int (the block-sparse
+ * backward's next-unit counter).  O(B*H*N*d), never O(N^2). */
 size_t fa_backward_workspace_size(int B, int H, int N, int d);
 
 /*

@@ -122,6 +122,7 @@ struct BwdWorkspace {
   float* dq_acc;
   float* part;     // split-last-round partials: [nslot][2][128][d] fp32
   int* part_cnt;   // [2 * nslot]
+  int* unit_counter;  // [1] next unit of the block-sparse backward
   int nslot;
 };
 
@@ -138,7 +139,7 @@ size_t bwd_ws_bytes(int B, int H, int N, int d) {
   const size_t rows = static_cast<size_t>(B) * H * N;
   const size_t ns = static_cast<size_t>(split_slots(B, H, N, d));
   return align256(rows * sizeof(float)) + align256(rows * d * sizeof(float)) +
-         align256(ns * 2 * kTile * d * sizeof(float)) + align256(2 * ns * sizeof(int));
+         align256(ns * 2 * kTile * d * sizeof(float)) + align256((2 * ns + 1) * sizeof(int));
 }
 
 BwdWorkspace bwd_ws(void* ws, int B, int H, int N, int d) {
@@ -153,6 +154,7 @@ BwdWorkspace bwd_ws(void* ws, int B, int H, int N, int d) {
   w.part = reinterpret_cast<float*>(base);
   base += align256(static_cast<size_t>(w.nslot) * 2 * kTile * d * sizeof(float));
   w.part_cnt = reinterpret_cast<int*>(base);
+  w.unit_counter = w.part_cnt + 2 * w.nslot;
   return w;
 }
 
@@ -267,6 +269,7 @@ fa_status backward_main_impl(const void* q, const void* k, const void* v, const 
   p.cu_seqlens = vl.cu_seqlens;
   p.total = vl.total;
   p.drop = drop;
+  p.unit_counter = w.unit_counter;
   if (!lists && w.nslot > 0) {  // the split last round (not with a block mask)
     p.part = w.part;
     p.part_cnt = w.part_cnt;
@@ -478,7 +481,7 @@ fa_status fa_backward_preprocess(const void* o, const void* dO, int B, int H, in
   FA_TRY(check_ptr16(dO));
   FA_TRY(check_ws(workspace, workspace_bytes, bwd_ws_bytes(B, H, N, d)));
   const BwdWorkspace w = bwd_ws(workspace, B, H, N, d);
-  FA_CUDA(fa::launch_bwd_preprocess(o, dO, w.delta, w.dq_acc, w.part_cnt, 2LL * w.nslot,
+  FA_CUDA(fa::launch_bwd_preprocess(o, dO, w.delta, w.dq_acc, w.part_cnt, 2LL * w.nslot + 1,
                                     static_cast<long long>(B) * H * N, d, stream));
   return FA_OK;
 }

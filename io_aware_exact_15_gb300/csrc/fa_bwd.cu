@@ -65,10 +65,13 @@ struct BwdSmem {
   static constexpr int B_KV = 0, B_QF = 1, B_QE = B_QF + NQ, B_DOF = B_QE + NQ,
                        B_DOE = B_DOF + NDO, B_SF = B_DOE + NDO, B_DPF = B_SF + 1,
                        B_PR = B_DPF + 1, B_DSR = B_PR + 1, B_DQF = B_DSR + 1, B_DQE = B_DQF + 1,
-                       B_FIN = B_DQE + 1, B_SPL = B_FIN + 1, B_EPI = B_SPL + 1,
-                       NBAR = B_EPI + 1;
+                       B_FIN = B_DQE + 1, B_SPL = B_FIN + 1, B_EPI = B_SPL + 1;
+  // ring of unit indices handed out by the producer (block-sparse kernel)
+  static constexpr int NU = 4;
+  static constexpr int B_UF = B_EPI + 1, B_UE = B_UF + NU, NBAR = B_UE + NU;
   static constexpr int MISC = BAR + NBAR * 8;
-  static constexpr int ALLOC = MISC + 16 + 1024;
+  static constexpr int RING = MISC + 16;  // NU ints
+  static constexpr int ALLOC = RING + 4 * NU + 1024;
   static_assert(ALLOC <= 232448, "shared memory budget");
   // TMEM columns
   static constexpr int T_S = 0, T_DP = 128, T_DV = 256, T_DK = 256 + D;
@@ -214,10 +217,39 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const bool split = D == 128 && !SPARSE && p.part != nullptr && !varlen && nround > 1 &&
                      2 * mlast <= static_cast<int>(gridDim.x) && mlast <= p.nslot &&
                      G * (p.causal ? 1 : ntmax) >= 8;
+  // Block mask: units are handed out at run time.  A CTA's first unit is
+  // its index; after that the producer takes the next unit index from a
+  // counter in the workspace and passes it to the other roles through a
+  // ring of NU slots (a slot is refilled once the issuer and all 256
+  // compute threads have read it).  Units come in the lists' order (long
+  // key tiles first), so the CTAs that draw a long unit take fewer others:
+  // with a fixed round-robin deal, a unit as long as dozens of others kept
+  // its CTA busy long after the rest had finished.
+  volatile int* ring = reinterpret_cast<volatile int*>(smem + L::RING);
+  const WaitCtl wcu{abort_flag, p.err, p.wait_ns};
+  auto dyn_item = [&](int k, int& u) -> bool {
+    const int slot = k % L::NU;
+    const uint32_t ph = static_cast<uint32_t>(k / L::NU) & 1;
+    if (warp == 0) {  // the producer's lane: publish
+      if (k >= L::NU && !wait_bar(bar(L::B_UE + slot), ph ^ 1, wcu)) return false;
+      int uu = k == 0 ? static_cast<int>(blockIdx.x)
+                      : static_cast<int>(gridDim.x) + atomicAdd(p.unit_counter, 1);
+      if (uu >= nunits) uu = -1;
+      ring[slot] = uu;
+      mbar_arrive(bar(L::B_UF + slot));
+      u = uu;
+      return uu >= 0;
+    }
+    if (!wait_bar(bar(L::B_UF + slot), ph, wcu)) return false;
+    u = ring[slot];
+    mbar_arrive(bar(L::B_UE + slot));
+    return u >= 0;
+  };
   // k-th item of this CTA: unit u and half uh (-1: the whole unit); false
   // when the CTA has no k-th item
   auto item_of = [&](int k, int& u, int& uh) {
     uh = -1;
+    if (SPARSE) return dyn_item(k, u);
     if (!split || k < nround - 1) {
       u = unit_of(k);
       return u < nunits;
@@ -265,6 +297,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(bar(L::B_FIN), 1);
     mbar_init(bar(L::B_SPL), 256);
     mbar_init(bar(L::B_EPI), 256);
+    for (int s = 0; s < L::NU; ++s) {
+      mbar_init(bar(L::B_UF + s), 1);
+      mbar_init(bar(L::B_UE + s), 1 + 256);  // the issuer's lane, the compute threads
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }

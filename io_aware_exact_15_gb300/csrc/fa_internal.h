@@ -131,6 +131,8 @@ struct BwdParams {
   float* part = nullptr;
   int* part_cnt = nullptr;
   int nslot = 0;
+  // block mask: next-unit counter (zero on entry; the preprocess zeroes it)
+  int* unit_counter = nullptr;
   int* err = nullptr;
   uint64_t wait_ns = 0;
 };

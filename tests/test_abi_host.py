@@ -38,7 +38,9 @@ def test_workspace_sizes():
     B, H, N, d = 2, 3, 300, 64
     rows = B * H * N
     a256 = lambda x: (x + 255) // 256 * 256
-    assert fa.fa_backward_workspace_size(B, H, N, d) == a256(4 * rows) + a256(4 * rows * d)
+    # D, the fp32 dQ accumulator, one counter word (the block-sparse backward's
+    # next unit)
+    assert fa.fa_backward_workspace_size(B, H, N, d) == a256(4 * rows) + a256(4 * rows * d) + 256
     nT = (N + 127) // 128
     lists = a256(4 * 1 * (2 * (nT + 1) + 2 * nT * nT + nT + 1))
     assert fa.fa_blocksparse_workspace_size(B, H, N, d, 1) == lists + \
@@ -53,9 +55,11 @@ def test_workspace_sizes():
     for (B, H, N), ns in (((2, 8, 2048), 96), ((1, 5, 2048), 40), ((1, 4, 2048), 0)):
         rows = B * H * N
         assert fa.fa_backward_workspace_size(B, H, N, 128) == \
-            a256(4 * rows) + a256(4 * rows * 128) + a256(ns * 2 * 128 * 128 * 4) + a256(8 * ns)
+            a256(4 * rows) + a256(4 * rows * 128) + a256(ns * 2 * 128 * 128 * 4) + \
+            a256(8 * ns + 4)
     rows = 2 * 8 * 2048
-    assert fa.fa_backward_workspace_size(2, 8, 2048, 64) == a256(4 * rows) + a256(4 * rows * 64)
+    assert fa.fa_backward_workspace_size(2, 8, 2048, 64) == \
+        a256(4 * rows) + a256(4 * rows * 64) + 256
 
 
 def test_noalloc_scratch_row_limits():
