@@ -126,7 +126,9 @@ __global__ void __launch_bounds__(kListWarps * 32) fa_lists_kernel(
   const int r_lo = csc_warp ? min(nT, range * L.rows_per_range) : 0;
   const int r_hi = csc_warp ? min(nT, r_lo + L.rows_per_range) : 0;
 
-  // ---- counts
+  // ---- counts (the row loops are unrolled so that several rows' loads are
+  // in flight at once: one CTA has few warps to hide load latency with)
+#pragma unroll 4
   for (int r = warp; r < nT; r += kListWarps) {
     int c = 0;
     for (int c0 = 16 * lane; c0 < nT; c0 += 512) c += __popc(chunk_bits(row_of(r), c0, nT, vec));
@@ -169,6 +171,7 @@ __global__ void __launch_bounds__(kListWarps * 32) fa_lists_kernel(
   }
 
   // ---- indices
+#pragma unroll 2
   for (int r = warp; r < nT; r += kListWarps) {
     int base = rc[r];
     for (int c0s = 0; c0s < nT; c0s += 512) {
