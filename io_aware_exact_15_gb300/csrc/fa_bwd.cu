@@ -159,8 +159,9 @@ FA_DEV bool bwd_unit(int u, const BwdParams& p, int Hkv, int G, int ntmax, bool 
 // barrier run on across units.
 // DQ = false: no dQ product and no reduce-adds (dQ comes from the query-tile
 // pass of the deterministic backward).  SPARSE: a block mask's lists (plain
-// kind), units in the lists' longest-first order.
-template <int D, int KIND, bool DQ = true, bool SPARSE = false>
+// kind), units in the lists' longest-first order.  DYN: units handed out at
+// run time (block masks and causal batches, whose units differ in length).
+template <int D, int KIND, bool DQ = true, bool SPARSE = false, bool DYN = SPARSE>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     fa_bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
@@ -214,10 +215,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int nround = (nunits + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x);
   const int last0 = (nround - 1) * static_cast<int>(gridDim.x);  // first unit of the last round
   const int mlast = nunits - last0;
-  const bool split = D == 128 && !SPARSE && p.part != nullptr && !varlen && nround > 1 &&
+  const bool split = D == 128 && !DYN && p.part != nullptr && !varlen && nround > 1 &&
                      2 * mlast <= static_cast<int>(gridDim.x) && mlast <= p.nslot &&
                      G * (p.causal ? 1 : ntmax) >= 8;
-  // Block mask: units are handed out at run time.  A CTA's first unit is
+  // Block mask or causal batch: units are handed out at run time.  A CTA's first unit is
   // its index; after that the producer takes the next unit index from a
   // counter in the workspace and passes it to the other roles through a
   // ring of NU slots (a slot is refilled once the issuer and all 256
@@ -249,7 +250,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   // when the CTA has no k-th item
   auto item_of = [&](int k, int& u, int& uh) {
     uh = -1;
-    if (SPARSE) return dyn_item(k, u);
+    if (DYN) return dyn_item(k, u);
     if (!split || k < nround - 1) {
       u = unit_of(k);
       return u < nunits;
@@ -1004,14 +1005,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
 }
 
-template <int D, int KIND, bool DQ = true, bool SPARSE = false>
+template <int D, int KIND, bool DQ = true, bool SPARSE = false, bool DYN = SPARSE>
 cudaError_t launch_bwd_d(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                          const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq,
                          cudaStream_t stream) {
   using L = BwdSmem<D>;
   static std::atomic<unsigned long long> attr_done{0};
   cudaError_t e = smem_attr_once(
-      attr_done, reinterpret_cast<const void*>(fa_bwd_kernel<D, KIND, DQ, SPARSE>), L::ALLOC);
+      attr_done, reinterpret_cast<const void*>(fa_bwd_kernel<D, KIND, DQ, SPARSE, DYN>),
+      L::ALLOC);
   if (e != cudaSuccess) return e;
   const int nT = (p.N + kTile - 1) / kTile;
   const long long units = static_cast<long long>(nT) * p.B * (p.Hkv > 0 ? p.Hkv : p.H);
@@ -1020,7 +1022,7 @@ cudaError_t launch_bwd_d(const BwdParams& p, const CUtensorMap& tq, const CUtens
   const int sms = sm_count();
   if (sms <= 0) return cudaErrorInvalidDevice;
   const long long ctas = units < sms ? units : sms;
-  return launch_pdl(fa_bwd_kernel<D, KIND, DQ, SPARSE>, dim3(static_cast<unsigned>(ctas)),
+  return launch_pdl(fa_bwd_kernel<D, KIND, DQ, SPARSE, DYN>, dim3(static_cast<unsigned>(ctas)),
                     dim3(kBwdThreads), L::ALLOC, stream, tq, tk, tv, tdo, tdq, p);
 }
 
@@ -1050,6 +1052,8 @@ cudaError_t launch_backward_main(const BwdParams& p, const CUtensorMap& tq, cons
       return launch_bwd_d<64, kGeneralDropout>(p, tq, tk, tv, tdo, tdq, stream);
     if (kind == kGeneral) return launch_bwd_d<64, kGeneral>(p, tq, tk, tv, tdo, tdq, stream);
     if (kind == kGrouped) return launch_bwd_d<64, kGrouped>(p, tq, tk, tv, tdo, tdq, stream);
+    if (p.causal)  // causal units differ in length: handed out at run time
+      return launch_bwd_d<64, kPlain, true, false, true>(p, tq, tk, tv, tdo, tdq, stream);
     return launch_bwd_d<64, kPlain>(p, tq, tk, tv, tdo, tdq, stream);
   }
   if (p.d == 128) {
@@ -1057,6 +1061,8 @@ cudaError_t launch_backward_main(const BwdParams& p, const CUtensorMap& tq, cons
       return launch_bwd_d<128, kGeneralDropout>(p, tq, tk, tv, tdo, tdq, stream);
     if (kind == kGeneral) return launch_bwd_d<128, kGeneral>(p, tq, tk, tv, tdo, tdq, stream);
     if (kind == kGrouped) return launch_bwd_d<128, kGrouped>(p, tq, tk, tv, tdo, tdq, stream);
+    if (p.causal)
+      return launch_bwd_d<128, kPlain, true, false, true>(p, tq, tk, tv, tdo, tdq, stream);
     return launch_bwd_d<128, kPlain>(p, tq, tk, tv, tdo, tdq, stream);
   }
   return cudaErrorInvalidValue;
