@@ -652,8 +652,10 @@ def run_reference(args, rank, world):
     sample, total, per_unit = oracle_job(w)
     nthreads = os.cpu_count() or 1
     per_step_budget = max(1.0, 150.0 / max(1, args.steps + args.warmup))
-    n, _ = calibrate_units(sample, total, nthreads, per_step_budget)
-    for _ in range(args.warmup):
+    n, (n_cal, dt_cal) = calibrate_units(sample, total, nthreads, per_step_budget)
+    # a calibration run of exactly one step's sample is that step's warm-up
+    done = 1 if n == n_cal else 0
+    for _ in range(max(0, args.warmup - done)):
         sample(n, nthreads)
     times = []
     for _ in range(args.steps):
