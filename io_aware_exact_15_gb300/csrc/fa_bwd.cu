@@ -27,7 +27,10 @@
 //               the next MMAs
 //   warps 2-3   idle
 // At the end of a unit warps 4-7 write dV_j and warps 8-11 write scale * dK_j
-// (whole rows, through their rows of the P buffer).
+// (whole rows, through their rows of the P buffer).  Units are dealt to the
+// CTAs round-robin in zig-zag (dense, causal) or, with a block mask, handed
+// out at run time from a counter (their lengths can differ by dozens of
+// times).
 // TMEM: S [0,128) dP [128,256) dV [256,256+d) dK [256+d,256+2d);
 //       dQ at [384,448) for d = 64 and over the dP columns for d = 128.
 #include <math.h>
