@@ -728,20 +728,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int qrow = qt * kTile + r;
         const bool live = qrow < N && lse_c != -INFINITY;
         const float lse2 = live ? lse_c * kLog2e : 0.f;
-        // keep bits of this thread's 64 keys (bit k of kb[c]: key 32 c + k),
-        // drawn before the wait for the scores, which they do not depend on
-        uint32_t kb[2] = {0u, 0u};
-        if (DROP) {
-#pragma unroll 1
-          for (int g4 = 0; g4 < 4; ++g4) {
-            const PhiloxOut rw = rng.group((kcol0 >> 4) + g4, qrow, un.bh_base + un.bq0 + g);
-            uint32_t nib = 0u;
-#pragma unroll
-            for (int w = 0; w < 4; ++w)
-              nib |= keep_nibble(DropoutRng::keep_bytes(rw.w[w], rng.t4)) << (4 * w);
-            kb[g4 >> 1] |= nib << (16 * (g4 & 1));
-          }
-        }
         // P = exp2(S * scale * log2e - lse * log2e); masked entries 0
         ok = __all_sync(0xffffffffu, wait_bar(bar(L::B_SF), n & 1, wc));
         if (!ok) break;
@@ -775,19 +761,28 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           }
           pw[i] = live ? pack_bf16(a, b) : 0u;
         }
+        // keep bits of this thread's 64 keys (bit k of kb[c]: key 32 c + k)
+        uint32_t kb[2] = {0u, 0u};
         p_rows_free();
         if (DROP) {
-          // the dV product takes the dropped weights z * P; dS needs P and z.
-          // Mask of the bf16 pair i (keys 2 i, 2 i + 1) from its two keep bits.
-          auto pm = [&](int i) {
-            const uint32_t two = (kb[i >> 4] >> ((2 * i) & 31)) & 3u;
-            return ((two & 1u) * 0x0000FFFFu) | ((two >> 1) * 0xFFFF0000u);
-          };
+          // the dV product takes the dropped weights z * P; dS needs P and z
 #pragma unroll
-          for (int u = 0; u < 8; ++u)
-            st_shared_v4(pbuf + sw128_offset(r, u), pw[4 * u] & pm(4 * u),
-                         pw[4 * u + 1] & pm(4 * u + 1), pw[4 * u + 2] & pm(4 * u + 2),
-                         pw[4 * u + 3] & pm(4 * u + 3));
+          for (int g4 = 0; g4 < 4; ++g4) {
+            const PhiloxOut rw = rng.group((kcol0 >> 4) + g4, qrow, un.bh_base + un.bq0 + g);
+            uint32_t mk[4];
+#pragma unroll
+            for (int w = 0; w < 4; ++w) mk[w] = DropoutRng::keep_bytes(rw.w[w], rng.t4);
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+              const uint32_t* pp = &pw[8 * g4 + 4 * hh];
+              st_shared_v4(pbuf + sw128_offset(r, 2 * g4 + hh), pp[0] & pair_mask(mk[2 * hh], 0),
+                           pp[1] & pair_mask(mk[2 * hh], 1), pp[2] & pair_mask(mk[2 * hh + 1], 0),
+                           pp[3] & pair_mask(mk[2 * hh + 1], 1));
+            }
+            kb[g4 >> 1] |= (keep_nibble(mk[0]) | (keep_nibble(mk[1]) << 4) |
+                            (keep_nibble(mk[2]) << 8) | (keep_nibble(mk[3]) << 12))
+                           << (16 * (g4 & 1));
+          }
         } else {
 #pragma unroll
           for (int u = 0; u < 8; ++u)
