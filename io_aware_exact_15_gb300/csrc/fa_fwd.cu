@@ -341,24 +341,6 @@ __global__ void __launch_bounds__(FwdSmem<D, NS_, BC, CMP>::THREADS,
     int kt, mem;
     while (ok && sch.next(kt, mem)) {
       if (!(mem & (1 << s))) continue;
-      // dropout: this row's keep bits of the key tile (bit j of kb[c]: key
-      // 32 c + j), drawn before the wait for the scores, which they do not
-      // depend on, so that the generator runs while the S product does
-      uint32_t kb[DROP ? BC / 32 : 1];
-      if (DROP) {
-#pragma unroll 1
-        for (int g16 = 0; g16 < BC / 16; ++g16) {
-          const PhiloxOut rw = rng.group(kt * (BC / 16) + g16, qrow, bh);
-          uint32_t nib = 0u;
-#pragma unroll
-          for (int w = 0; w < 4; ++w)
-            nib |= keep_nibble(DropoutRng::keep_bytes(rw.w[w], rng.t4)) << (4 * w);
-          if ((g16 & 1) == 0)
-            kb[g16 >> 1] = nib;
-          else
-            kb[g16 >> 1] |= nib << 16;
-        }
-      }
       ok = __all_sync(0xffffffffu, wait_bar(bar(L::B_SF + s), cnt & 1, wc));
       if (!ok) break;
       tc_fence_after();
@@ -420,6 +402,7 @@ __global__ void __launch_bounds__(FwdSmem<D, NS_, BC, CMP>::THREADS,
       const float mu = (m == -INFINITY) ? 0.f : m;
       const uint64_t sl2x2 = f2_pack(sl2, sl2), nmux2 = f2_pack(-mu, -mu);
       float ls0 = 0.f, ls1 = 0.f, ls2 = 0.f, ls3 = 0.f;  // row-sum partials
+      PhiloxOut rw;
       // P (bf16, two per 32-bit column) overwrites the first BC / 2 columns
       // of this tile's S, whose scores are already in registers (group g's
       // P lands on columns of group 0, which the first pass has read)
@@ -451,14 +434,15 @@ __global__ void __launch_bounds__(FwdSmem<D, NS_, BC, CMP>::THREADS,
           acc_bf16x2(ls0, ls1, sr[q][4 * c4 + 2]);
           acc_bf16x2(ls2, ls3, sr[q][4 * c4 + 3]);
           if (DROP) {
-            // dropped weights leave the PV product (l keeps them): the bf16
-            // pair of keys 2 i, 2 i + 1 keeps each half whose bit is set
-            const uint32_t bits = kb[(g * GW + 32 * q) >> 5] >> (8 * c4);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const uint32_t two = (bits >> (2 * j)) & 3u;
-              sr[q][4 * c4 + j] &= ((two & 1u) * 0x0000FFFFu) | ((two >> 1) * 0xFFFF0000u);
-            }
+            // dropped weights leave the PV product (l keeps them); one
+            // generator call covers keys 32 q + 16 (c4 / 2) .. + 15
+            if ((c4 & 1) == 0) rw = rng.group((kbase + g * GW) / 16 + 2 * q + (c4 >> 1), qrow, bh);
+            const uint32_t m0 = DropoutRng::keep_bytes(rw.w[2 * (c4 & 1)], rng.t4);
+            const uint32_t m1 = DropoutRng::keep_bytes(rw.w[2 * (c4 & 1) + 1], rng.t4);
+            sr[q][4 * c4] &= pair_mask(m0, 0);
+            sr[q][4 * c4 + 1] &= pair_mask(m0, 1);
+            sr[q][4 * c4 + 2] &= pair_mask(m1, 0);
+            sr[q][4 * c4 + 3] &= pair_mask(m1, 1);
           }
         }
         tmem_st16(tP + g * (GW / 2) + 16 * q, *reinterpret_cast<const uint32_t(*)[16]>(&sr[q][0]));
