@@ -96,7 +96,7 @@ fa_status fa_backward(const void* q, const void* k, const void* v, const void* o
                       cudaStream_t stream);
 
 /* Backward step 1: D_i = <dO_i, O_i> (fp32) into the workspace and zero the
- * workspace's dQ accumulator. */
+ * workspace's dQ accumulator and its counters. */
 fa_status fa_backward_preprocess(const void* o, const void* dO, int B, int H, int N, int d,
                                  void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
@@ -105,8 +105,8 @@ fa_status fa_backward_preprocess(const void* o, const void* dO, int B, int H, in
  * accumulator.  Run it once after each fa_backward_preprocess of the same
  * problem on the same workspace: the preprocess also clears the counters
  * with which split key tiles of the last round hand over their partial
- * dK, dV sums, and a second run on the same workspace would find them
- * used. */
+ * dK, dV sums (and the block-sparse backward hands out its units), and a
+ * second run on the same workspace would find them used. */
 fa_status fa_backward_main(const void* q, const void* k, const void* v, const void* dO,
                            const float* lse, void* dk, void* dv, int B, int H, int N, int d,
                            float scale, int causal, void* workspace, size_t workspace_bytes,
