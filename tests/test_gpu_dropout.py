@@ -55,16 +55,18 @@ def test_dropout_small_full(N, p, d, causal):
     parity.check_grad(dv, dv_r, "dV", what)
 
 
-@pytest.mark.parametrize("d", [64, 128])
-def test_forward_keep_bits_are_exact(d):
+@pytest.mark.parametrize("d,H", [(64, 2), (128, 2), (64, 320), (128, 160)])
+def test_forward_keep_bits_are_exact(d, H):
     """Q = 0 makes every weight 1 before normalisation, p = 1/2 makes the
     keep scale 2, and V puts weight 2^(j // d) on column j mod d of key j,
     so with N = 8 d every intermediate is exact and O_ic * N / 2 is the
     8-bit number whose bit t is the keep decision of key t d + c.  That
     reads out the kernel's decision for every (row, key), to be equal to
-    the oracle's keep rule."""
+    the oracle's keep rule.  H = 2 runs the compact one-tile form (the
+    softmax warps draw the bits); 320 and 160 heads make grids of 640
+    two-tile CTAs, where two warps of their own draw them."""
     dev = device()
-    B, H, N = 1, 2, 8 * d
+    B, N = 1, 8 * d
     q = torch.zeros((B, H, N, d), dtype=torch.bfloat16)
     g = torch.Generator().manual_seed(3)
     k = W.randn_bf16((B, H, N, d), g)
@@ -81,8 +83,8 @@ def test_forward_keep_bits_are_exact(d):
     status_ok()
     code = o.float().cpu().numpy() * (N / 2)
     assert np.array_equal(code, np.rint(code)), "O is not an exact multiple of 2/N"
-    code = code.astype(np.int64)                                   # [B, H, N, d]
-    bits = (code[..., None] >> np.arange(8)) & 1                   # [B, H, N, d, 8]
+    code = code.astype(np.uint8)                                   # [B, H, N, d]
+    bits = (code[..., None] >> np.arange(8, dtype=np.uint8)) & 1   # [B, H, N, d, 8]
     z_gpu = bits.transpose(0, 1, 2, 4, 3).reshape(B, H, N, N)      # key = t d + c
     z_ref = oracle.dropout_keep(seed, offset, 0.5, B, H, N)
     assert np.array_equal(z_gpu, z_ref), f"{int((z_gpu != z_ref).sum())} keep bits differ"
