@@ -44,10 +44,7 @@ namespace {
 // CMP: the compact form of a one-query-tile CTA: 6 warps, tensor memory and
 // shared memory sized for one tile, so that two CTAs can share an SM where
 // both fit (at most 256 TMEM columns and ~113 KB of shared memory each).
-// KB: dropout in the two-tile form: warps 10-11 draw the keep bits of
-// query tiles 0-1 into a ring of per-row 128-bit masks that the softmax
-// warps read, so that the generator runs beside the softmax, not in it.
-template <int D, int NS_ = 0, int BC = kTile, bool CMP = false, bool KB = false>
+template <int D, int NS_ = 0, int BC = kTile, bool CMP = false>
 struct FwdSmem {
   static constexpr int CH = D / 64;             // 128-byte column chunks per row
   static constexpr int CHUNK = kTile * 128;     // query tile: [128 rows x 128 B] = 16 KB
@@ -59,7 +56,7 @@ struct FwdSmem {
   static constexpr int NQT = CMP ? 1 : 2;
   static_assert(NQT * (BC + D) <= 512, "tensor memory budget");
   static constexpr int QT = CMP ? 1 : 2;  // query tiles in shared memory
-  static constexpr int THREADS = CMP ? 192 : KB ? 384 : 320;
+  static constexpr int THREADS = CMP ? 192 : 320;
   // columns allocated: the power of two that holds S and O of every tile
   static constexpr int TCOLS = CMP ? (NQT * (BC + D) <= 128   ? 128
                                       : NQT * (BC + D) <= 256 ? 256
@@ -67,20 +64,12 @@ struct FwdSmem {
                                    : 512;
   // K/V ring slots (one tile each); NS_ != 0 overrides for the tile sweep.
   // The compact form keeps its shared memory within half an SM's.
-  // With keep-bit warps the d = 128 ring has 4 slots (as fast as 5 in the
-  // block-size sweep) to leave room for the masks.
-  static constexpr int NS = NS_ != 0 ? NS_
-                            : CMP   ? ((D == 64) ? 4 : 2)
-                                    : ((D == 64) ? 8 : (KB ? 4 : 5));
+  static constexpr int NS = NS_ != 0 ? NS_ : CMP ? ((D == 64) ? 4 : 2) : ((D == 64) ? 8 : 5);
   static constexpr int Q = 0;
   static constexpr int KV = Q + QT * TILE;
-  // keep-bit ring: [tile][slot][128 rows][4 words]
-  static constexpr int KBR = 2;
-  static constexpr int KBUF = KV + NS * KTILE;
-  static constexpr int BAR = KBUF + (KB ? 2 * KBR * kTile * 16 : 0);
+  static constexpr int BAR = KV + NS * KTILE;
   static constexpr int B_Q = 0, B_KVF = 1, B_KVE = 1 + NS, B_SF = 1 + 2 * NS, B_PF = B_SF + 2,
-                       B_OF = B_PF + 2, B_KF = B_OF + 1, B_KE = B_KF + 2 * KBR,
-                       NBAR = B_KE + 2 * KBR;
+                       B_OF = B_PF + 2, NBAR = B_OF + 1;
   static constexpr int MISC = BAR + NBAR * 8;
   // TMEM columns of P_s: the first 64 columns of S_s (already read into
   // registers).  d = 64 would leave room for separate P columns after O1,
@@ -99,13 +88,11 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleLog2 = 8.0f;  // lazy rescale threshold (factor 256)
 
 template <int D, int KIND, int NS_, int BC, bool CMP>
-__global__ void __launch_bounds__(
-    FwdSmem<D, NS_, BC, CMP, KIND == kGeneralDropout && !CMP>::THREADS,
-    FwdSmem<D, NS_, BC, CMP, KIND == kGeneralDropout && !CMP>::MINB)
+__global__ void __launch_bounds__(FwdSmem<D, NS_, BC, CMP>::THREADS,
+                                  FwdSmem<D, NS_, BC, CMP>::MINB)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const FwdParams p) {
-  constexpr bool KB = KIND == kGeneralDropout && !CMP;
-  using L = FwdSmem<D, NS_, BC, CMP, KB>;
+  using L = FwdSmem<D, NS_, BC, CMP>;
   static_assert(BC == kTile || (NS_ != 0 && KIND == kPlain),
                 "key tiles other than 128 exist only in the plain sweep instantiations");
   grid_dep_wait();  // the previous kernel's writes are visible from here on
@@ -177,11 +164,6 @@ __global__ void __launch_bounds__(
       mbar_init(bar(L::B_PF + s), 128);
     }
     mbar_init(bar(L::B_OF), 1);
-    if (KB)
-      for (int i = 0; i < 2 * L::KBR; ++i) {
-        mbar_init(bar(L::B_KF + i), 32);   // the tile's keep-bit warp
-        mbar_init(bar(L::B_KE + i), 128);  // the tile's softmax threads
-      }
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&tq);
@@ -339,48 +321,6 @@ __global__ void __launch_bounds__(
       mma_commit(bar(L::B_OF));
       drain_bar(bar(L::B_OF), 0, p.wait_ns);
     }
-  } else if (KB && warp >= 10) {
-    // ------------------------------------------------------ keep-bit warps
-    // Warp 10 + s draws, for every key tile that query tile s meets, the keep
-    // bits of the tile's 128 rows (lane l: rows l, l + 32, l + 64, l + 96),
-    // 128 bits per row (bit j of word c: key 32 c + j), into ring slot
-    // (step mod KBR), up to KBR steps ahead of the softmax.
-    const int s = warp - 10;
-    const int qt = sch.qt[s];
-    const DropoutRng rng{p.drop.rk, p.drop.offset, p.drop.t * 0x01010101u};
-    uint32_t cntk = 0;
-    bool ok = true;
-    int kt, mem;
-    while (ok && sch.next(kt, mem)) {
-      if (!(mem & (1 << s))) continue;
-      const int slot = cntk % L::KBR;
-      if (cntk >= L::KBR) {
-        ok = __all_sync(0xffffffffu, wait_bar(bar(L::B_KE + s * L::KBR + slot),
-                                              ((cntk / L::KBR) - 1) & 1, wc));
-        if (!ok) break;
-      }
-      const uint32_t dst = sb + L::KBUF + (s * L::KBR + slot) * kTile * 16;
-#pragma unroll 1
-      for (int rr = 0; rr < 4; ++rr) {
-        const int r = lane + 32 * rr;
-        uint32_t kb[4];
-#pragma unroll
-        for (int g16 = 0; g16 < 8; ++g16) {
-          const PhiloxOut rw = rng.group(kt * 8 + g16, qt * kTile + r, bh);
-          uint32_t nib = 0u;
-#pragma unroll
-          for (int w = 0; w < 4; ++w)
-            nib |= keep_nibble(DropoutRng::keep_bytes(rw.w[w], rng.t4)) << (4 * w);
-          if ((g16 & 1) == 0)
-            kb[g16 >> 1] = nib;
-          else
-            kb[g16 >> 1] |= nib << 16;
-        }
-        st_shared_v4(dst + r * 16, kb[0], kb[1], kb[2], kb[3]);
-      }
-      mbar_arrive(bar(L::B_KF + s * L::KBR + slot));
-      ++cntk;
-    }
   } else {
     // ------------------------------------------------------ softmax warps
     const int s = (warp - 2) >> 2;
@@ -463,20 +403,6 @@ __global__ void __launch_bounds__(
       const uint64_t sl2x2 = f2_pack(sl2, sl2), nmux2 = f2_pack(-mu, -mu);
       float ls0 = 0.f, ls1 = 0.f, ls2 = 0.f, ls3 = 0.f;  // row-sum partials
       PhiloxOut rw;
-      // keep bits of this row for the key tile, from the keep-bit warp
-      uint32_t kbm[4] = {0u, 0u, 0u, 0u};
-      if (KB) {
-        const int slot = cnt % L::KBR;
-        ok = __all_sync(0xffffffffu, wait_bar(bar(L::B_KF + s * L::KBR + slot),
-                                              (cnt / L::KBR) & 1, wc));
-        if (!ok) break;
-        const uint4 v = ld_shared_v4(sb + L::KBUF + (s * L::KBR + slot) * kTile * 16 + r * 16);
-        kbm[0] = v.x;
-        kbm[1] = v.y;
-        kbm[2] = v.z;
-        kbm[3] = v.w;
-        mbar_arrive(bar(L::B_KE + s * L::KBR + slot));
-      }
       // P (bf16, two per 32-bit column) overwrites the first BC / 2 columns
       // of this tile's S, whose scores are already in registers (group g's
       // P lands on columns of group 0, which the first pass has read)
@@ -507,16 +433,7 @@ __global__ void __launch_bounds__(
           acc_bf16x2(ls2, ls3, sr[q][4 * c4 + 1]);
           acc_bf16x2(ls0, ls1, sr[q][4 * c4 + 2]);
           acc_bf16x2(ls2, ls3, sr[q][4 * c4 + 3]);
-          if (KB) {
-            // dropped weights leave the PV product (l keeps them): the bf16
-            // pair of keys 2 i, 2 i + 1 keeps each half whose bit is set
-            const uint32_t bits = kbm[q] >> (8 * c4);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const uint32_t two = (bits >> (2 * j)) & 3u;
-              sr[q][4 * c4 + j] &= ((two & 1u) * 0x0000FFFFu) | ((two >> 1) * 0xFFFF0000u);
-            }
-          } else if (DROP) {
+          if (DROP) {
             // dropped weights leave the PV product (l keeps them); one
             // generator call covers keys 32 q + 16 (c4 / 2) .. + 15
             if ((c4 & 1) == 0) rw = rng.group((kbase + g * GW) / 16 + 2 * q + (c4 >> 1), qrow, bh);
@@ -616,7 +533,7 @@ __global__ void __launch_bounds__(
 template <int D, int KIND, int NS_ = 0, int BC = kTile, bool CMP = false>
 cudaError_t launch_fwd_d(const FwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                          const CUtensorMap& tv, cudaStream_t stream) {
-  using L = FwdSmem<D, NS_, BC, CMP, KIND == kGeneralDropout && !CMP>;
+  using L = FwdSmem<D, NS_, BC, CMP>;
   static std::atomic<unsigned long long> attr_done{0};
   cudaError_t e = smem_attr_once(
       attr_done, reinterpret_cast<const void*>(fa_fwd_kernel<D, KIND, NS_, BC, CMP>), L::ALLOC);
