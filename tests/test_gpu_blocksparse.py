@@ -187,21 +187,26 @@ def test_schedules_bit_exact(N, mask_kind, causal):
             assert bc[h, a] == len(bexp) and bl[h, a, :bc[h, a]].tolist() == bexp
 
 
-@pytest.mark.parametrize("causal", [False, True])
-def test_blocksparse_backward_dynamic_units(causal):
+@pytest.mark.parametrize("causal,per_head", [(False, False), (True, False), (False, True)])
+def test_blocksparse_backward_dynamic_units(causal, per_head):
     # Units are handed out at run time, long key tiles first: two kept
     # columns of every query tile, empty columns, a random 10 %, 256 units
-    # on the 152 SMs.  Every output against the oracle; two runs give the
-    # same dK, dV bit for bit (a unit's sums never depend on which CTA ran
-    # it) and dQ to rounding.
+    # on the 152 SMs; with per-head masks the heads have different long
+    # columns and counts (the backward takes the largest count for all).
+    # Every output against the oracle; two runs give the same dK, dV bit
+    # for bit (a unit's sums never depend on which CTA ran it) and dQ to
+    # rounding.
     dev = device()
     B, H, N, d = 2, 2, 8192, 64
     nT = N // 128
-    mask = W.random_block_mask(1, nT, seed=31, density=0.10)
+    mask = W.random_block_mask(H if per_head else 1, nT, seed=31, density=0.10)
     mask[0, :, 0] = 1
     mask[0, :, 17] = 1
     mask[0, :, 40:44] = 0
     mask[0, 5, 40] = 1
+    if per_head:
+        mask[1, :, 3] = 1
+        mask[1, :, 50:52] = 0
     q, k, v, do = W.make_qkv(B, H, N, d, seed=4242 + causal)
     scale = 1.0 / d ** 0.5
     a = run_sparse(q, k, v, do, scale, causal, mask, dev)
