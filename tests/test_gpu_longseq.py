@@ -19,6 +19,8 @@ subset of that size: the first and last head, the first and last head
 holding a unit of the persistent backward's last round (on d = 128 dense
 shapes those units run as two halves on two CTAs), and seeded others.
 """
+import dataclasses
+
 import pytest
 
 from gpu_common import device, status_ok, torch
@@ -33,10 +35,27 @@ SHAPES = [f"longseq_{kind}_n{N}_d{d}" for kind in ("causal", "dense")
           for d in (64, 128) for N in (2048, 4096, 8192, 16384)]
 
 
+# Ragged lengths (no multiple of 128) at grids of 1280 two-tile forward CTAs
+# and 2560 backward units: the last query and key tiles are partial in
+# every head, in the launch forms long sequences take.
+RAGGED = [dataclasses.replace(W.WORKLOADS[f"longseq_{kind}_n4096_d{d}"], N=n, B=4,
+                              name=f"ragged_{kind}_n{n}_d{d}")
+          for kind in ("causal", "dense") for d, n in ((64, 4999), (128, 5000))]
+
+
+@pytest.mark.parametrize("w", RAGGED, ids=lambda w: w.name)
+def test_long_ragged_sequence_parity(w):
+    check_long(w)
+
+
 @pytest.mark.parametrize("name", SHAPES)
 def test_long_sequence_parity(name):
+    check_long(W.WORKLOADS[name])
+
+
+def check_long(w):
     dev = device()
-    w = W.WORKLOADS[name]
+    name = w.name
     B, H, N, d = w.B, w.H, w.N, w.d
     q, k, v, do, _ = W.make_inputs(w)
     qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))

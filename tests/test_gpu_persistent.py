@@ -103,13 +103,14 @@ def test_multi_unit_backward_consistent(B, H, N, d, causal):
                 1e-2 * first[0].float().abs().max().item(), f"{what} run {run}: dQ drifted"
 
 
-@pytest.mark.parametrize("B,H,N,d", [(2, 8, 1280, 128), (1, 16, 1536, 128)])
+@pytest.mark.parametrize("B,H,N,d", [(2, 8, 1280, 128), (1, 16, 1536, 128), (2, 8, 5000, 128)])
 def test_split_last_round_against_oracle(B, H, N, d):
     # The last round's units run as two halves whose dK, dV partial sums
     # meet in the workspace.  Every row of every head that holds a
     # last-round unit is compared with the fp64 oracle: B2 H8 N1280 leaves
     # units 152..159 (head 15, key tiles 2..9), B1 H16 N1536 units 152..191
-    # (heads 12..15) on the 152-SM grid.
+    # (heads 12..15) on the 152-SM grid; B2 H8 N5000 units 608..639 (head
+    # 15), whose halves walk 40 query tiles, the last one partial.
     dev = device()
     assert _splits(B, H, N, d, False), "shape no longer splits its last round"
     q, k, v, do = W.make_qkv(B, H, N, d, seed=4100 + N + B)
