@@ -613,10 +613,14 @@ cudaError_t launch_forward(const FwdParams& p, const CUtensorMap& tq, const CUte
   // grain evens out the last wave (measured: B8 H12 N1024 causal d = 64
   // forward 33.2 -> 29.6 us, B8 H16 N512 20.2 -> 19.4 us; at B4 H16 N4096 the
   // two-tile form is 4 % faster at d = 64 and 8 % at d = 128).
+  // Block masks also run the compact form at every size: a two-tile CTA
+  // walks the union of its two query tiles' kept key tiles, and with
+  // scattered masks most of those steps hold one tile only (one MMA chain
+  // per SM instead of two).
   const int nT = (p.N + kTile - 1) / kTile;
   const long long pairs = static_cast<long long>((nT + 1) / 2) * p.B * p.H;
   const int sms = sm_count();
-  const bool compact = sms > 0 && pairs <= 4LL * sms;
+  const bool compact = p.lists.row_ptr != nullptr || (sms > 0 && pairs <= 4LL * sms);
   if (p.d == 64)
     return compact ? launch_forward_kind<64, true>(kind, p, tq, tk, tv, stream)
                    : launch_forward_kind<64, false>(kind, p, tq, tk, tv, stream);
