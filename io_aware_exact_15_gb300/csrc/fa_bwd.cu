@@ -248,6 +248,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       u = uu;
       return uu >= 0;
     }
+    if (warp == 1) {  // the issuer warp: every lane reads the slot, one arrives
+      if (!__all_sync(0xffffffffu, wait_bar(bar(L::B_UF + slot), ph, wcu))) return false;
+      u = __shfl_sync(0xffffffffu, ring[slot], 0);
+      if (lane == 0) mbar_arrive(bar(L::B_UE + slot));
+      return u >= 0;
+    }
     if (!wait_bar(bar(L::B_UF + slot), ph, wcu)) return false;
     u = ring[slot];
     mbar_arrive(bar(L::B_UE + slot));
@@ -402,7 +408,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp runs the issuer: waits and tests are warp votes, so
+    // its control flow and operand descriptors are warp-uniform, and the
+    // elected lane issues each MMA and commit (a single-lane issuer spent
+    // ~90 cycles per MMA instruction).
+    {
+      auto uwait = [&](uint32_t b, uint32_t ph) {
+        return __all_sync(0xffffffffu, wait_bar(b, ph, wc));
+      };
+      auto utry = [&](uint32_t b, uint32_t ph) { return __all_sync(0xffffffffu, mbar_try(b, ph)); };
+      auto ecommit = [&](uint32_t b) {
+        if (elect_one()) mma_commit(b);
+      };
       constexpr uint32_t idSS = idesc_bf16(128, 128, false, false);  // S, dP
       constexpr uint32_t idTT = idesc_bf16(128, D, true, true);      // dV, dK
       constexpr uint32_t idDQ = idesc_bf16(128, D, false, true);     // dQ
@@ -417,17 +434,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       auto mnmaj = [&](uint32_t a) { return desc_advance(dm0, a - sb); };
       auto qk_step = [&](uint32_t dst, uint32_t a, uint32_t b, int kk) {
         const uint32_t off = (kk >> 2) * L::CHUNK + (kk & 3) * 32;
-        mma_bf16_ss(dst, kmaj(a + off), kmaj(b + off), idSS, kk > 0);
+        const uint64_t da = kmaj(a + off), db = kmaj(b + off);
+        if (elect_one()) mma_bf16_ss(dst, da, db, idSS, kk > 0);
       };
       // Y[128 k x D] += X^T[128 k x 128 q] Z[128 q x D]; X stored [q][k]
       auto tt_step = [&](uint32_t dst, uint32_t x, uint32_t z, bool acc, int kk) {
-        mma_bf16_ss(dst, mnmaj(x + kk * 2048), mnmaj(z + kk * 2048), idTT,
-                    (acc || kk > 0) ? 1u : 0u);
+        const uint64_t da = mnmaj(x + kk * 2048), db = mnmaj(z + kk * 2048);
+        if (elect_one()) mma_bf16_ss(dst, da, db, idTT, (acc || kk > 0) ? 1u : 0u);
       };
       // dQ[128 q x D] = dS[128 q x 128 k] K[128 k x D]
       auto dq_step = [&](uint32_t dst, int kk) {
         const uint32_t aoff = (kk >> 2) * L::CHUNK + (kk & 3) * 32;
-        mma_bf16_ss(dst, kmaj(sb + L::DS + aoff), mnmaj(sb + L::K + kk * 2048), idDQ, kk > 0);
+        const uint64_t da = kmaj(sb + L::DS + aoff), db = mnmaj(sb + L::K + kk * 2048);
+        if (elect_one()) mma_bf16_ss(dst, da, db, idDQ, kk > 0);
       };
       auto issue_qk = [&](uint32_t dst, uint32_t a, uint32_t b) {
 #pragma unroll
@@ -451,23 +470,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         Sched sch;
         start(un, uh, sch);
         int qt, qt_n, g_unused;
-        ok = wait_bar(bar(L::B_KV), ku & 1, wc);
+        ok = uwait(bar(L::B_KV), ku & 1);
         bool have = ok && sch.next(qt, g_unused, p.lists);
         uint32_t nu = 0;  // steps of this unit
         if (ok && have) {
-          ok = wait_bar(bar(L::B_QF + n % L::NQ), (n / L::NQ) & 1, wc);
+          ok = uwait(bar(L::B_QF + n % L::NQ), (n / L::NQ) & 1);
           if (ok) {
             tc_fence_after();
             issue_qk(tS, sb + L::QR + (n % L::NQ) * L::TILE, sb + L::K);
-            mma_commit(bar(L::B_SF));
+            ecommit(bar(L::B_SF));
             // d = 128: the previous unit's last dQ shares the dP columns
-            if (DQ && D != 64 && n > 0) ok = wait_bar(bar(L::B_DQE), (n - 1) & 1, wc);
+            if (DQ && D != 64 && n > 0) ok = uwait(bar(L::B_DQE), (n - 1) & 1);
           }
-          if (ok) ok = wait_bar(bar(L::B_DOF + n % L::NDO), (n / L::NDO) & 1, wc);
+          if (ok) ok = uwait(bar(L::B_DOF + n % L::NDO), (n / L::NDO) & 1);
           if (ok) {
             tc_fence_after();
             issue_qk(tDP, sb + L::DOR + (n % L::NDO) * L::TILE, sb + L::V);
-            mma_commit(bar(L::B_DPF));
+            ecommit(bar(L::B_DPF));
           }
         }
         while (ok && have) {
@@ -476,63 +495,63 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           const uint32_t n1 = n + 1;
           // dV += P^T dO_i once P is in shared memory, interleaved with the
           // next S when its Q tile is already in (the S columns were read)
-          if (!(ok = wait_bar(bar(L::B_PR), n & 1, wc))) break;
+          if (!(ok = uwait(bar(L::B_PR), n & 1))) break;
           tc_fence_after();
           const uint32_t qn = sb + L::QR + (n1 % L::NQ) * L::TILE;
           const uint32_t dov = sb + L::DOR + dpos * L::TILE;
-          if (have_n && mbar_try(bar(L::B_QF + n1 % L::NQ), (n1 / L::NQ) & 1)) {
+          if (have_n && utry(bar(L::B_QF + n1 % L::NQ), (n1 / L::NQ) & 1)) {
             tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < kTile / 16; ++kk) {
               tt_step(tDV, sb + L::P, dov, nu > 0, kk);
               if (kk < D / 16) qk_step(tS, qn, sb + L::K, kk);
             }
-            mma_commit(bar(L::B_DOE + dpos));
-            mma_commit(bar(L::B_SF));
+            ecommit(bar(L::B_DOE + dpos));
+            ecommit(bar(L::B_SF));
           } else {
             issue_tt(tDV, sb + L::P, dov, nu > 0);
-            mma_commit(bar(L::B_DOE + dpos));
+            ecommit(bar(L::B_DOE + dpos));
             if (have_n) {
-              if (!(ok = wait_bar(bar(L::B_QF + n1 % L::NQ), (n1 / L::NQ) & 1, wc))) break;
+              if (!(ok = uwait(bar(L::B_QF + n1 % L::NQ), (n1 / L::NQ) & 1))) break;
               tc_fence_after();
               issue_qk(tS, qn, sb + L::K);
-              mma_commit(bar(L::B_SF));
+              ecommit(bar(L::B_SF));
             }
           }
           // dK += dS^T Q_i and dQ_i = dS K once dS is in shared memory,
           // interleaved when the dQ columns are free
-          if (!(ok = wait_bar(bar(L::B_DSR), n & 1, wc))) break;
+          if (!(ok = uwait(bar(L::B_DSR), n & 1))) break;
           tc_fence_after();
           const uint32_t qv = sb + L::QR + qpos * L::TILE;
           if (!DQ) {
             issue_tt(tDK, sb + L::DS, qv, nu > 0);
-            mma_commit(bar(L::B_QE + qpos));
-          } else if (D != 64 || n == 0 || mbar_try(bar(L::B_DQE), (n - 1) & 1)) {
+            ecommit(bar(L::B_QE + qpos));
+          } else if (D != 64 || n == 0 || utry(bar(L::B_DQE), (n - 1) & 1)) {
             tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < kTile / 16; ++kk) {
               tt_step(tDK, sb + L::DS, qv, nu > 0, kk);
               dq_step(tDQ, kk);
             }
-            mma_commit(bar(L::B_QE + qpos));
-            mma_commit(bar(L::B_DQF));
+            ecommit(bar(L::B_QE + qpos));
+            ecommit(bar(L::B_DQF));
           } else {
             issue_tt(tDK, sb + L::DS, qv, nu > 0);
-            mma_commit(bar(L::B_QE + qpos));
-            if (!(ok = wait_bar(bar(L::B_DQE), (n - 1) & 1, wc))) break;
+            ecommit(bar(L::B_QE + qpos));
+            if (!(ok = uwait(bar(L::B_DQE), (n - 1) & 1))) break;
             tc_fence_after();
             issue_dq(tDQ);
-            mma_commit(bar(L::B_DQF));
+            ecommit(bar(L::B_DQF));
           }
           if (have_n) {
             if (DQ && D != 64) {  // dQ_i shares the dP columns: wait until it is read out
-              if (!(ok = wait_bar(bar(L::B_DQE), n & 1, wc))) break;
+              if (!(ok = uwait(bar(L::B_DQE), n & 1))) break;
               tc_fence_after();
             }
-            if (!(ok = wait_bar(bar(L::B_DOF + n1 % L::NDO), (n1 / L::NDO) & 1, wc))) break;
+            if (!(ok = uwait(bar(L::B_DOF + n1 % L::NDO), (n1 / L::NDO) & 1))) break;
             tc_fence_after();
             issue_qk(tDP, sb + L::DOR + (n1 % L::NDO) * L::TILE, sb + L::V);
-            mma_commit(bar(L::B_DPF));
+            ecommit(bar(L::B_DPF));
           }
           qt = qt_n;
           have = have_n;
@@ -545,8 +564,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         // issued nothing the compute warps gate, so its commit could land
         // right after the previous unit's, two phases ahead of a compute warp
         // still to wait for that one: it waits until they have.
-        if (nu == 0 && ku > 0 && !wait_bar(bar(L::B_EPI), (ku - 1) & 1, wc)) ok = false;
-        mma_commit(bar(L::B_FIN));
+        if (nu == 0 && ku > 0 && !uwait(bar(L::B_EPI), (ku - 1) & 1)) ok = false;
+        ecommit(bar(L::B_FIN));
         ++ku;
       }
       if (ku > 0) drain_bar(bar(L::B_FIN), (ku - 1) & 1, p.wait_ns);

@@ -234,7 +234,17 @@ __global__ void __launch_bounds__(FwdSmem<D, NS_, BC, CMP>::THREADS,
     }
   } else if (warp == 1) {
     // ------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp runs the issuer (waits and tests are warp votes, so
+    // control flow and operand descriptors are warp-uniform) and the
+    // elected lane issues each MMA and commit.
+    {
+      auto uwait = [&](uint32_t b, uint32_t ph) {
+        return __all_sync(0xffffffffu, wait_bar(b, ph, wc));
+      };
+      auto utry = [&](uint32_t b, uint32_t ph) { return __all_sync(0xffffffffu, mbar_try(b, ph)); };
+      auto ecommit = [&](uint32_t b) {
+        if (elect_one()) mma_commit(b);
+      };
       constexpr uint32_t idS = idesc_bf16(128, BC, false, false);
       constexpr uint32_t idO = idesc_bf16(128, D, false, true);
       // descriptors are formed once per operand and advanced per k-step
@@ -247,8 +257,9 @@ __global__ void __launch_bounds__(FwdSmem<D, NS_, BC, CMP>::THREADS,
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t in_row = (kk & 3) * 32;
-          mma_bf16_ss(tmem + s * BC, desc_advance(qa, (kk >> 2) * L::CHUNK + in_row),
-                      desc_advance(kb, (kk >> 2) * L::KCHUNK + in_row), idS, kk > 0);
+          const uint64_t da = desc_advance(qa, (kk >> 2) * L::CHUNK + in_row);
+          const uint64_t db = desc_advance(kb, (kk >> 2) * L::KCHUNK + in_row);
+          if (elect_one()) mma_bf16_ss(tmem + s * BC, da, db, idS, kk > 0);
         }
       };
       // O_s += P_s V: P_s sits in TMEM (BC / 2 columns, two bf16 per column),
@@ -256,33 +267,36 @@ __global__ void __launch_bounds__(FwdSmem<D, NS_, BC, CMP>::THREADS,
       auto issue_pv = [&](int s, int vpos, bool acc) {
         const uint64_t vb = desc_advance(dv0, vpos * L::KTILE);
 #pragma unroll
-        for (int kk = 0; kk < BC / 16; ++kk)
-          mma_bf16_ts(tmem + L::T_O + s * D, tmem + L::T_P + s * L::T_PSTRIDE + kk * 8,
-                      desc_advance(vb, kk * 2048), idO, (acc || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < BC / 16; ++kk) {
+          const uint64_t db = desc_advance(vb, kk * 2048);
+          if (elect_one())
+            mma_bf16_ts(tmem + L::T_O + s * D, tmem + L::T_P + s * L::T_PSTRIDE + kk * 8, db, idO,
+                        (acc || kk > 0) ? 1u : 0u);
+        }
       };
       int kt, mem, kt_n = 0, mem_n = 0;
       uint32_t idx = 0;
       uint32_t cnt01 = 0;  // participations of slot 0 (low 16 bits) and slot 1 (high)
-      bool ok = wait_bar(bar(L::B_Q), 0, wc);
+      bool ok = uwait(bar(L::B_Q), 0);
       bool have = sch.next(kt, mem);
       if (ok && have) {
         const int kpos = idx % L::NS;
-        ok = wait_bar(bar(L::B_KVF + kpos), (idx / L::NS) & 1, wc);
+        ok = uwait(bar(L::B_KVF + kpos), (idx / L::NS) & 1);
         if (ok) {
           tc_fence_after();
           for (int s = 0; s < 2; ++s)
             if (mem & (1 << s)) {
               issue_s(s, kpos);
-              mma_commit(bar(L::B_SF + s));
+              ecommit(bar(L::B_SF + s));
             }
-          mma_commit(bar(L::B_KVE + kpos));
+          ecommit(bar(L::B_KVE + kpos));
           ++idx;
         }
       }
       while (ok && have) {
         const bool have_n = sch.next(kt_n, mem_n);
         const int vpos = idx % L::NS;
-        ok = wait_bar(bar(L::B_KVF + vpos), (idx / L::NS) & 1, wc);
+        ok = uwait(bar(L::B_KVF + vpos), (idx / L::NS) & 1);
         ++idx;
         if (!ok) break;
         tc_fence_after();
@@ -290,7 +304,7 @@ __global__ void __launch_bounds__(FwdSmem<D, NS_, BC, CMP>::THREADS,
         for (int s = 0; s < 2 && ok; ++s) {
           if (mem & (1 << s)) {
             const uint32_t cs = (cnt01 >> (16 * s)) & 0xFFFFu;
-            ok = wait_bar(bar(L::B_PF + s), cs & 1, wc);
+            ok = uwait(bar(L::B_PF + s), cs & 1);
             if (!ok) break;
             tc_fence_after();
             issue_pv(s, vpos, cs > 0);
@@ -299,18 +313,18 @@ __global__ void __launch_bounds__(FwdSmem<D, NS_, BC, CMP>::THREADS,
           if (have_n && (mem_n & (1 << s))) {
             if (kpos < 0) {
               kpos = idx % L::NS;
-              ok = wait_bar(bar(L::B_KVF + kpos), (idx / L::NS) & 1, wc);
+              ok = uwait(bar(L::B_KVF + kpos), (idx / L::NS) & 1);
               if (!ok) break;
               tc_fence_after();
             }
             issue_s(s, kpos);
-            mma_commit(bar(L::B_SF + s));
+            ecommit(bar(L::B_SF + s));
           }
         }
         if (!ok) break;
-        mma_commit(bar(L::B_KVE + vpos));
+        ecommit(bar(L::B_KVE + vpos));
         if (kpos >= 0) {
-          mma_commit(bar(L::B_KVE + kpos));
+          ecommit(bar(L::B_KVE + kpos));
           ++idx;
         }
         kt = kt_n;
@@ -318,7 +332,7 @@ __global__ void __launch_bounds__(FwdSmem<D, NS_, BC, CMP>::THREADS,
         have = have_n;
       }
       // every MMA issued above completes before o_full fires
-      mma_commit(bar(L::B_OF));
+      ecommit(bar(L::B_OF));
       drain_bar(bar(L::B_OF), 0, p.wait_ns);
     }
   } else {

@@ -173,6 +173,20 @@ FA_DEV void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32
       "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// One lane of a converged warp, picked by the hardware.  An MMA-issuing warp
+// runs its loop with every lane (control flow and operand descriptors the
+// same in all of them) and lets the elected lane issue each tcgen05
+// instruction.
+FA_DEV bool elect_one() {
+  uint32_t e;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "elect.sync _|p, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(e));
+  return e != 0;
+}
+
 // Arrive once on `bar` when every tcgen05 op issued so far by this thread is done.
 FA_DEV void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
