@@ -763,22 +763,31 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         int lim = N - kcol0;
         if (p.causal && qrow - kcol0 + 1 < lim) lim = qrow - kcol0 + 1;
         uint32_t pw[32];  // pw[i]: keys 2i, 2i+1 of this thread's 64 columns
-        const uint64_t sl2x2 = f2_pack(sl2, sl2), nlse2x2 = f2_pack(-lse2, -lse2);
+        // a row with no live statistics gets the bias -inf: all its P are 0
+        const float nb = live ? -lse2 : -INFINITY;
+        const uint64_t sl2x2 = f2_pack(sl2, sl2), nlse2x2 = f2_pack(nb, nb);
+        // scale * S * log2 e - lse * log2 e for two keys in one fp32 x2 FMA
+        auto arg2 = [&](int i) {
+          return f2_fma(f2_pack(__uint_as_float(sv[i >> 4][(2 * i) & 31]),
+                                __uint_as_float(sv[i >> 4][(2 * i + 1) & 31])),
+                        sl2x2, nlse2x2);
+        };
+        if (need_mask) {  // (warp-uniform) the tile crosses N or the diagonal
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          // scale * S * log2 e - lse * log2 e for two keys in one fp32 x2 FMA
-          float a, b;
-          f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[i >> 4][(2 * i) & 31]),
-                                   __uint_as_float(sv[i >> 4][(2 * i + 1) & 31])),
-                           sl2x2, nlse2x2),
-                    a, b);
-          a = ex2(a);
-          b = ex2(b);
-          if (need_mask) {
-            if (2 * i >= lim) a = 0.f;
-            if (2 * i + 1 >= lim) b = 0.f;
+          for (int i = 0; i < 32; ++i) {
+            float a, b;
+            f2_unpack(arg2(i), a, b);
+            a = 2 * i < lim ? ex2(a) : 0.f;
+            b = 2 * i + 1 < lim ? ex2(b) : 0.f;
+            pw[i] = pack_bf16(a, b);
           }
-          pw[i] = live ? pack_bf16(a, b) : 0u;
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            float a, b;
+            f2_unpack(arg2(i), a, b);
+            pw[i] = pack_bf16(ex2(a), ex2(b));
+          }
         }
         // keep bits of this thread's 64 keys (bit k of kb[c]: key 32 c + k)
         uint32_t kb[2] = {0u, 0u};
