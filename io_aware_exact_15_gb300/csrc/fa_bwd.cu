@@ -847,12 +847,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 d0 = ((kb[c] >> (8 * g + 2 * j)) & 1u) ? d0 * p.drop.scale : 0.f;
                 d1 = ((kb[c] >> (8 * g + 2 * j + 1)) & 1u) ? d1 * p.drop.scale : 0.f;
               }
-              // P o (dP - D) for the two keys in fp32 x2
+              // P o (dP - D) for the two keys: dP - D in fp32 x2, rounded to
+              // bf16 (the dS written is bf16 anyway), times the packed bf16 P
               float x0, x1;
-              f2_unpack(f2_mul(f2_pack(bf16_lo(pp), bf16_hi(pp)),
-                               f2_sub(f2_pack(d0, d1), dltx2)),
-                        x0, x1);
-              w[j] = pack_bf16(x0, x1);
+              f2_unpack(f2_sub(f2_pack(d0, d1), dltx2), x0, x1);
+              w[j] = mul_bf16x2(pp, pack_bf16(x0, x1));
             }
             if (!L::OWN_STG && c == 0 && g == 0) {  // the previous dQ staging in these rows has been read
               if (lane == 0) bulk_wait_read_all();

@@ -338,6 +338,12 @@ FA_DEV uint32_t pack_bf16(float lo, float hi) {
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
 }
+// elementwise product of two packed bf16x2 words, rounded once to bf16
+FA_DEV uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
 // the two halves of a packed bf16x2 word as fp32 (exact)
 FA_DEV float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 FA_DEV float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
