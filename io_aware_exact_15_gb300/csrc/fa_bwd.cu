@@ -510,16 +510,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             issue_qk(tS, qn, sb + L::K);
             ecommit(bar(L::B_SF));
           }
-          // dK += dS^T Q_i and dQ_i = dS K once dS is in shared memory,
-          // interleaved when the dQ columns are free
+          // dK += dS^T Q_i and dQ_i = dS K once dS is in shared memory.
+          // d = 64: dQ first, committed on its own, so that its drain (into a
+          // staging buffer of its own) overlaps dK.  d = 128: interleaved,
+          // and dQ's completion is signalled only with dK's, because the
+          // drain stages dQ in the dS rows that dK reads.
           if (!(ok = uwait(bar(L::B_DSR), n & 1))) break;
           tc_fence_after();
           const uint32_t qv = sb + L::QR + qpos * L::TILE;
           if (!DQ) {
             issue_tt(tDK, sb + L::DS, qv, nu > 0);
             ecommit(bar(L::B_QE + qpos));
-          } else if (D != 64 || n == 0 || utry(bar(L::B_DQE), (n - 1) & 1)) {
+          } else if (L::OWN_STG && (n == 0 || utry(bar(L::B_DQE), (n - 1) & 1))) {
             tc_fence_after();
+            issue_dq(tDQ);
+            ecommit(bar(L::B_DQF));
+            issue_tt(tDK, sb + L::DS, qv, nu > 0);
+            ecommit(bar(L::B_QE + qpos));
+          } else if (!L::OWN_STG) {
 #pragma unroll
             for (int kk = 0; kk < kTile / 16; ++kk) {
               tt_step(tDK, sb + L::DS, qv, nu > 0, kk);
