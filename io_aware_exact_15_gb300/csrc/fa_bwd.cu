@@ -423,9 +423,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       constexpr uint32_t idSS = idesc_bf16(128, 128, false, false);  // S, dP
       constexpr uint32_t idTT = idesc_bf16(128, D, true, true);      // dV, dK
       constexpr uint32_t idDQ = idesc_bf16(128, D, false, true);     // dQ
-      // One k-step (K = 16) of each product.  A chain of k-steps into one
-      // accumulator is latency-bound on the tensor core, so independent
-      // chains are issued interleaved step by step where the data allows.
+      // One k-step (K = 16) of each product.  The products go out in the
+      // order the compute warps consume their results (dV before the next
+      // S, dQ before dK at d = 64); only dK and dQ at d = 128 run
+      // interleaved k-step by k-step, since dQ's completion may only be
+      // signalled with dK's there.
       // X[128 q x 128 k] = A[128 x D] B[128 x D]^T, both K-major
       // operand descriptors: K-major (qk) or MN-major (tt, dq B), advanced per
       // k-step from the descriptor of the operand's first byte
