@@ -14,7 +14,8 @@
 // dK and dV; persistent CTAs, one per SM, take the units in turn):
 //   warp 0      TMA producer: K_j, V_j once per unit; Q_i through an NQ-slot
 //               ring and dO_i through an NDO-slot ring (128-byte swizzle)
-//   warp 1      allocates 512 TMEM columns; lane 0 issues the five MMAs
+//   warp 1      allocates 512 TMEM columns; an elected lane issues the five
+//               MMAs (the whole warp runs the issue loop)
 //   warps 4-11  one thread per query row and half of the key columns (warps
 //               4-7: keys 0-63, warps 8-11: keys 64-127): P from S and lse
 //               (ex2 with the scale folded in) and dS from dP and D, both

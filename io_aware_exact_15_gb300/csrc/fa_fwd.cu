@@ -9,7 +9,8 @@
 // GB300 design (one CTA = one head x two 128-row query tiles):
 //   warp 0      TMA producer: both Q tiles once, then K_j, V_j through an
 //               NS-deep ring of 128 x d tiles (128-byte swizzle)
-//   warp 1      allocates 512 TMEM columns; lane 0 issues every tcgen05.mma:
+//   warp 1      allocates 512 TMEM columns; an elected lane issues every
+//               tcgen05.mma (the whole warp runs the issue loop):
 //               S_s = Q_s K_j^T (fp32 in TMEM) and O_s += P_s V_j
 //   warps 2-5   softmax for query tile 0, warps 6-9 for query tile 1: one
 //               thread per query row reads its 128 scores from TMEM, applies
