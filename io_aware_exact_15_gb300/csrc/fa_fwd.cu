@@ -27,7 +27,8 @@
 // issue order, so P_s is read before the next scores overwrite it.  The K/V
 // ring is 5 (d = 128) or 8 (d = 64) tiles.
 //
-// Compact form (grids of at most four waves of two-tile CTAs): one query
+// Compact form (grids of at most four waves of two-tile CTAs, and every
+// grid with a block mask): one query
 // tile per CTA, warps 0-5 only, 256 TMEM columns (S [0,128), O [128,128+d)),
 // a 2 (d = 128) or 4 (d = 64) tile ring, so that two CTAs share an SM.  The
 // block-size sweep also builds key tiles of 64 and 256 keys (template BC).
